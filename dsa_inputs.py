@@ -1,0 +1,154 @@
+"""Seeded synthetic inputs for the dynamic-sparse-attention step.
+
+This module is shared by the tests, the benchmark and the smoke check, and
+feeds both the CUDA library and the CPU oracle the very same bytes. It holds
+none of the method's arithmetic: it draws random tensors, rounds them to the
+storage dtypes, and (for an INT8 cache) quantises them the way the synthetic
+workload recipe states. Nothing here scores, selects or attends.
+
+Workloads (the five shapes the library is measured on; the names say what
+they are):
+
+* ``decode_4k``      batch 1, 1 query token, context 4,096, 8 query heads over
+                      2 KV heads, BF16 Q/K/V, top_k 512.
+* ``grouped_decode_32k``  batch 4, 8 query tokens each, context 32,768,
+                      24 query heads over 2 KV heads, BF16 query, FP16 KV,
+                      top_k 2,048.
+* ``decode_128k``    batch 1, 1 query token, context 131,072 (64 chunks of
+                      2,048 keys), 24/2 heads, BF16 query, FP16 KV, top_k
+                      2,048; 1 % of the index keys get a +3 sigma bias.
+* ``prefill_8k_on_32k``  batch 1, 8,192 new tokens after a 32,768-token past
+                      (cache length 40,960), 24/2 heads, BF16 throughout,
+                      top_k 2,048.
+* ``decode_256k_int8``  batch 1, 8 query tokens, context 262,144 (128 chunks),
+                      INT8 KV with a per-token per-head fp32 absmax scale,
+                      BF16 query, top_k 2,048.
+
+Every workload has 16 index heads of dim 64 (BF16 qI/kI ~ N(0,1), fp32 head
+weights w ~ U(0,1)) and head dim 128; Q/K/V ~ N(0,1).
+
+Positions: the cache holds ``T`` rows and the ``S`` new query tokens are its
+last ``S`` rows, so query ``s`` sits at position ``T - S + s`` and sees keys
+``0 .. T - S + s`` (causal, including itself).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional
+
+import torch
+
+# storage dtypes by name
+DTYPES = {"bf16": torch.bfloat16, "fp16": torch.float16, "int8": torch.int8,
+          "fp32": torch.float32}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    q_len: int            # S: new query tokens per sequence
+    total_len: int        # T: cache rows visible to the last query token
+    num_q_heads: int
+    num_kv_heads: int
+    top_k: int
+    q_dtype: str = "bf16"
+    kv_dtype: str = "bf16"
+    head_dim: int = 128
+    idx_heads: int = 16
+    idx_dim: int = 64
+    bias_frac: float = 0.0   # fraction of index keys given a +3 sigma shift
+    capacity: Optional[int] = None  # cache rows allocated (>= total_len)
+    seed: int = 1000
+
+    @property
+    def cap(self) -> int:
+        return self.capacity if self.capacity is not None else self.total_len
+
+    @property
+    def query_tokens(self) -> int:
+        return self.batch * self.q_len
+
+
+WORKLOADS: Dict[str, Workload] = {
+    "decode_4k": Workload("decode_4k", 1, 1, 4096, 8, 2, 512,
+                          "bf16", "bf16", seed=1001),
+    "grouped_decode_32k": Workload("grouped_decode_32k", 4, 8, 32768, 24, 2,
+                                   2048, "bf16", "fp16", seed=1002),
+    "decode_128k": Workload("decode_128k", 1, 1, 131072, 24, 2, 2048,
+                            "bf16", "fp16", bias_frac=0.01, seed=1003),
+    "prefill_8k_on_32k": Workload("prefill_8k_on_32k", 1, 8192, 40960, 24, 2,
+                                  2048, "bf16", "bf16", seed=1004),
+    "decode_256k_int8": Workload("decode_256k_int8", 1, 8, 262144, 24, 2, 2048,
+                                 "bf16", "int8", seed=1005),
+}
+
+
+def quantize_int8(x: torch.Tensor):
+    """Absmax INT8 codes over the last dim: scale = max|x|/127, code =
+    clamp(round-half-even(x/scale), -127, 127); an all-zero row gets scale 0
+    and codes 0. Returns (codes int8, scale fp32 with the last dim dropped)."""
+    x = x.to(torch.float32)
+    amax = x.abs().amax(dim=-1)
+    scale = amax / 127.0
+    safe = torch.where(scale > 0, scale, torch.ones_like(scale))
+    codes = torch.round(x / safe.unsqueeze(-1)).clamp_(-127, 127)
+    codes = torch.where(scale.unsqueeze(-1) > 0, codes, torch.zeros_like(codes))
+    return codes.to(torch.int8), scale.contiguous()
+
+
+def make_inputs(wl: Workload, seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """CPU tensors for one workload, drawn in a fixed order from one seeded
+    generator: qI, w, kI, bias mask, q, K, V.
+
+    Returns a dict with qI [B,S,HI,DI] bf16, w [B,S,HI] fp32, kI [B,cap,DI]
+    bf16, q [B,S,Hq,D], k/v [B,cap,Hkv,D] in the workload's dtypes, k_scale /
+    v_scale [B,cap,Hkv] fp32 (INT8 only, else None), total_len [B] int32.
+    """
+    g = torch.Generator().manual_seed(wl.seed if seed is None else seed)
+    B, S, cap = wl.batch, wl.q_len, wl.cap
+    qI = torch.randn(B, S, wl.idx_heads, wl.idx_dim, generator=g)
+    w = torch.rand(B, S, wl.idx_heads, generator=g)
+    kI = torch.randn(B, cap, wl.idx_dim, generator=g)
+    if wl.bias_frac > 0:
+        nb = int(wl.bias_frac * wl.total_len)
+        for b in range(B):
+            pos = torch.randperm(wl.total_len, generator=g)[:nb]
+            kI[b, pos] += 3.0
+    q = torch.randn(B, S, wl.num_q_heads, wl.head_dim, generator=g)
+    k = torch.randn(B, cap, wl.num_kv_heads, wl.head_dim, generator=g)
+    v = torch.randn(B, cap, wl.num_kv_heads, wl.head_dim, generator=g)
+    out = {
+        "qI": qI.to(torch.bfloat16).contiguous(),
+        "w": w.contiguous(),
+        "kI": kI.to(torch.bfloat16).contiguous(),
+        "q": q.to(DTYPES[wl.q_dtype]).contiguous(),
+        "total_len": torch.full((B,), wl.total_len, dtype=torch.int32),
+        "k_scale": None,
+        "v_scale": None,
+    }
+    if wl.kv_dtype == "int8":
+        out["k"], out["k_scale"] = quantize_int8(k)
+        out["v"], out["v_scale"] = quantize_int8(v)
+    else:
+        out["k"] = k.to(DTYPES[wl.kv_dtype]).contiguous()
+        out["v"] = v.to(DTYPES[wl.kv_dtype]).contiguous()
+    return out
+
+
+def small_workload(name="small", batch=2, q_len=3, total_len=1000, num_q_heads=8,
+                   num_kv_heads=2, top_k=64, q_dtype="bf16", kv_dtype="bf16",
+                   capacity=None, bias_frac=0.0, seed=7) -> Workload:
+    """A reduced-size workload of the same structure, for parity tests that the
+    oracle finishes in seconds."""
+    return Workload(name, batch, q_len, total_len, num_q_heads, num_kv_heads,
+                    top_k, q_dtype, kv_dtype, bias_frac=bias_frac,
+                    capacity=capacity, seed=seed)
+
+
+def to_f64(t: Optional[torch.Tensor]):
+    """Exact float64 numpy copy of a CPU tensor (bf16/fp16/int8/fp32 values are
+    all exactly representable in float64)."""
+    if t is None:
+        return None
+    return t.detach().to("cpu").to(torch.float64).numpy()

@@ -1,0 +1,196 @@
+"""CPU oracle for dynamic sparse attention (indexer -> top-k -> sparse GQA attention).
+
+TEST INFRASTRUCTURE ONLY. This module exists so that the tests, the smoke check
+and the benchmark's CPU-baseline leg can check the CUDA library against a
+plain, slow, obviously correct float64 restatement of what the method
+computes. The library never imports, links or calls it, and it shares no code
+with the library: it takes numpy arrays and returns numpy arrays.
+
+Sources (public pull-request pages of ONNX Runtime's CUDA contrib ops):
+
+* "[CUDA] Support FP16 KV cache and FP16 query/key in DynamicSparseAttention<
+  BFloat16> and FP32 rotary cache / FP16 output in RMSNormRotary" (PR #33997),
+  Description item 2: the op attends over a *selected* subset of the K/V cache
+  (prefill and grouped GQA decode), with BF16/FP16 query and BF16/FP16 cache.
+* "[CUDA] Optimize Qwen3.8-Flash-Next DSA, Indexer, HC, and QMoE kernels for
+  SM12x and 256K context" (PR #33802), Summary items 1-2: the indexer scores
+  every cached index key ("present_key_state") for each query token over 16
+  index heads, in 2,048-key chunks, and a radix top-k (per-chunk partial
+  histograms + one final merge-and-emit) picks the keys; INT8 KV cache with a
+  value scale.
+* Follow-up PR #33847 "... a large-value-scale accumulator", Description and
+  Changes table: the online-softmax rescale must not lose earlier tiles when
+  the running maximum rises by ~88 nats; worked example 2^120*e^-88/(1+e^-88).
+
+The pages print no formula. The readings taken here (each also listed in the
+design notes):
+
+R1  positions: the cache holds T rows and the S new query tokens are its last
+    S rows; query s sits at T-S+s and sees keys 0..T-S+s.
+R2  indexer score (the form fixed for this library):
+        score[t] = sum_h w[h] * max(0, qI[h] . kI[t])
+    one index key per token shared by all index heads; no 1/sqrt(d) factor.
+R3  top-k: k_eff = min(k, n) keys with the highest score; equal scores go to
+    the lower index; emitted in ascending index order, padded with -1.
+    -0.0 compares equal to +0.0.
+R4  attention: head h uses KV head g = h // (Hq/Hkv) (consecutive grouping);
+    logits = scale * q_h . K^[t,g] with scale = 1/sqrt(head_dim) unless given;
+    exact softmax over the selected keys; out_h = sum_t p_t V^[t,g].
+R5  INT8 cache: K^[t,g,:] = code[t,g,:] * k_scale[t,g] (same for V).
+
+Parity pins for every function live in tests/test_oracle_pins.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# positions (R1)
+# ---------------------------------------------------------------------------
+def visible_len(T: int, S: int, s: int) -> int:
+    """Number of keys visible to query s of a sequence whose cache holds T rows
+    with the S new tokens as its last rows: positions 0 .. T-S+s (R1)."""
+    n = T - S + s + 1
+    if n < 1:
+        raise ValueError("query position precedes the cache start")
+    return n
+
+
+# ---------------------------------------------------------------------------
+# indexer (R2) -- PR #33802 Summary item 2, PackedSparseAttentionIndexer
+# ---------------------------------------------------------------------------
+def index_scores_row(qI_s: np.ndarray, w_s: np.ndarray, kI_b: np.ndarray,
+                     n: int) -> np.ndarray:
+    """Scores of keys 0..n-1 for one query token.
+
+    qI_s [HI, DI], w_s [HI], kI_b [cap, DI] (float64 copies of the stored
+    values). Returns float64 [n]: sum_h w[h] * max(0, qI[h] . kI[t]).
+    """
+    dots = kI_b[:n] @ qI_s.T                      # [n, HI]: qI_h . kI_t
+    return np.maximum(dots, 0.0) @ w_s            # sum_h w_h * ReLU(.)
+
+
+def index_scores(qI, w, kI, total_len, rows=None) -> np.ndarray:
+    """Indexer scores for every query token.
+
+    qI [B,S,HI,DI], w [B,S,HI], kI [B,cap,DI], total_len [B] (T_b).
+    Returns float64 [B,S,cap]; entries past a query's visible length are NaN.
+    ``rows`` optionally restricts the work to a list of (b, s) pairs (the
+    others stay NaN) for workloads too large to score in full on a CPU.
+    """
+    B, S = qI.shape[:2]
+    cap = kI.shape[1]
+    out = np.full((B, S, cap), np.nan)
+    todo = rows if rows is not None else [(b, s) for b in range(B) for s in range(S)]
+    for b, s in todo:
+        n = visible_len(int(total_len[b]), S, s)
+        out[b, s, :n] = index_scores_row(qI[b, s], w[b, s], kI[b], n)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# top-k selection (R3) -- PR #33802 Summary item 2 (radix partial top-k over
+# 2,048-key chunks + final merge-and-emit); the chunking only changes speed,
+# not the selected set, so the oracle selects over the whole row at once.
+# ---------------------------------------------------------------------------
+def topk_select_row(scores: np.ndarray, k: int) -> np.ndarray:
+    """Select min(k, n) indices of the highest values of a 1-D array.
+
+    Values are compared exactly (pass fp32 values as float64 to compare fp32
+    numbers bit for bit); -0.0 equals +0.0; among equal values the lower index
+    wins. Returns int64 [k]: the selected indices ascending, then -1s.
+    """
+    v = np.asarray(scores, dtype=np.float64) + 0.0   # -0.0 + 0.0 == +0.0
+    n = v.shape[0]
+    if np.isnan(v).any():
+        raise ValueError("NaN scores have no defined order")
+    keff = min(k, n)
+    # sort by value descending, then index ascending
+    order = np.lexsort((np.arange(n), -v))
+    sel = np.sort(order[:keff])
+    out = np.full(k, -1, dtype=np.int64)
+    out[:keff] = sel
+    return out
+
+
+def topk(scores, total_len, k: int, rows=None) -> np.ndarray:
+    """Top-k for every query row of a [B,S,cap] score tensor (only the visible
+    prefix of each row takes part). Returns int64 [B,S,k]."""
+    B, S = scores.shape[:2]
+    out = np.full((B, S, k), -1, dtype=np.int64)
+    todo = rows if rows is not None else [(b, s) for b in range(B) for s in range(S)]
+    for b, s in todo:
+        n = visible_len(int(total_len[b]), S, s)
+        out[b, s] = topk_select_row(scores[b, s, :n], k)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# sparse GQA attention (R4, R5) -- PR #33997 Description item 2 (prefill and
+# grouped decode over the selected rows), PR #33802 Summary item 1 (INT8 cache)
+# ---------------------------------------------------------------------------
+def dequantize(codes: np.ndarray, scale) -> np.ndarray:
+    """K^ = code * scale per token and head (R5); scale None means the cache
+    already stores values (BF16/FP16)."""
+    if scale is None:
+        return codes
+    return codes * scale[..., None]
+
+
+def attend_row(q_h: np.ndarray, Kg: np.ndarray, Vg: np.ndarray,
+               scale: float) -> np.ndarray:
+    """Exact softmax attention of one query head over a set of rows.
+
+    q_h [D], Kg/Vg [m, D] (dequantised selected rows). Returns float64 [D].
+    """
+    logits = scale * (Kg @ q_h)
+    mx = logits.max()
+    p = np.exp(logits - mx)
+    p /= p.sum()
+    return p @ Vg
+
+
+def sparse_attention(q, k, v, idx, num_kv_heads: int, k_scale=None,
+                     v_scale=None, softmax_scale: float = 0.0,
+                     rows=None) -> np.ndarray:
+    """Softmax attention of each query head over its query token's selected
+    rows.
+
+    q [B,S,Hq,D]; k, v [B,cap,Hkv,D] (values, or INT8 codes with k_scale /
+    v_scale [B,cap,Hkv]); idx [B,S,k] (selected indices, -1 = unused).
+    Returns float64 [B,S,Hq,D] (rows not in ``rows`` stay NaN).
+    """
+    B, S, Hq, D = q.shape
+    G = Hq // num_kv_heads
+    scale = softmax_scale if softmax_scale else 1.0 / np.sqrt(D)
+    out = np.full(q.shape, np.nan)
+    todo = rows if rows is not None else [(b, s) for b in range(B) for s in range(S)]
+    for b, s in todo:
+        sel = idx[b, s]
+        sel = sel[sel >= 0]
+        Kb = dequantize(k[b, sel], None if k_scale is None else k_scale[b, sel])
+        Vb = dequantize(v[b, sel], None if v_scale is None else v_scale[b, sel])
+        for h in range(Hq):
+            g = h // G
+            out[b, s, h] = attend_row(q[b, s, h], Kb[:, g], Vb[:, g], scale)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the whole step
+# ---------------------------------------------------------------------------
+def sparse_attention_step(inp: dict, num_kv_heads: int, top_k: int,
+                          softmax_scale: float = 0.0, rows=None) -> dict:
+    """Indexer -> top-k -> sparse attention for one batch of query tokens.
+
+    ``inp`` holds float64 arrays qI, w, kI, q, k, v, k_scale, v_scale (None
+    unless INT8) and total_len. Returns dict(scores, idx, out).
+    """
+    T = inp["total_len"]
+    scores = index_scores(inp["qI"], inp["w"], inp["kI"], T, rows=rows)
+    idx = topk(scores, T, top_k, rows=rows)
+    out = sparse_attention(inp["q"], inp["k"], inp["v"], idx, num_kv_heads,
+                           inp.get("k_scale"), inp.get("v_scale"),
+                           softmax_scale, rows=rows)
+    return {"scores": scores, "idx": idx, "out": out}

@@ -1,0 +1,440 @@
+"""Pins for the CPU oracle: each check ties an oracle function to something
+other than itself -- values printed on the pages, hand-worked fixtures,
+closed forms, invariants, a library routine in a special case, or brute force
+on tiny inputs. The mutation tests at the end plant plausible mistakes in a
+copy of the oracle and assert that some pin catches each one.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.dsa_oracle as O
+from dsa_inputs import make_inputs, small_workload, to_f64
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _num(x):
+    return float(x) if not isinstance(x, str) else float(x)
+
+
+# ---------------------------------------------------------------------------
+# reusable checks (also driven by the mutation tests)
+# ---------------------------------------------------------------------------
+def check_topk_fixture(mod):
+    for case in _load("topk_tiny.json")["cases"]:
+        s = np.array([_num(x) for x in case["scores"]], dtype=np.float64)
+        got = mod.topk_select_row(s, case["k"])
+        assert got.tolist() == case["expected"], (case, got)
+
+
+def is_valid_topk(scores, k, sel):
+    """Definition of the selection, checked by properties only: right count,
+    ascending then -1 padding, every selected >= every unselected, and on the
+    threshold value the selected indices all precede the unselected ones."""
+    n = len(scores)
+    keff = min(k, n)
+    sel = np.asarray(sel)
+    if sel.shape != (k,) or (sel[keff:] != -1).any():
+        return False
+    chosen = sel[:keff]
+    if (chosen < 0).any() or (chosen >= n).any():
+        return False
+    if keff > 1 and not (np.diff(chosen) > 0).all():
+        return False
+    rest = np.setdiff1d(np.arange(n), chosen)
+    if len(rest) == 0 or keff == 0:
+        return True
+    vs = scores[chosen] + 0.0
+    vr = scores[rest] + 0.0
+    if vs.min() < vr.max():
+        return False
+    thr = vs.min()
+    if vr.max() == thr:
+        if chosen[vs == thr].max() > rest[vr == thr].min():
+            return False
+    return True
+
+
+def brute_force_topk(scores, k):
+    """k rounds of 'take the largest remaining value, lowest index first'."""
+    left = list(range(len(scores)))
+    picked = []
+    for _ in range(min(k, len(scores))):
+        best = left[0]
+        for i in left[1:]:
+            if scores[i] + 0.0 > scores[best] + 0.0:
+                best = i
+        picked.append(best)
+        left.remove(best)
+    out = sorted(picked) + [-1] * (k - len(picked))
+    return np.array(out)
+
+
+def check_topk_bruteforce(mod, trials=300):
+    rng = np.random.default_rng(0)
+    for _ in range(trials):
+        n = int(rng.integers(1, 10))
+        s = rng.integers(0, 4, size=n).astype(np.float64)
+        for k in (1, max(1, n // 2), n, n + 3):
+            got = mod.topk_select_row(s, k)
+            assert got.tolist() == brute_force_topk(s, k).tolist(), (s, k, got)
+
+
+def check_indexer_fixture(mod):
+    fx = _load("indexer_tiny.json")
+    got = mod.index_scores_row(np.array(fx["qI"]), np.array(fx["w"]),
+                               np.array(fx["kI"]), len(fx["kI"]))
+    assert np.array_equal(got, np.array(fx["expected"])), got
+
+
+def check_indexer_closed_form(mod):
+    """kI_t = c_t u and qI_h = a_h u give qI_h.kI_t = a_h c_t |u|^2, so
+    score_t = sum_h w_h max(0, a_h c_t |u|^2) -- with mixed signs of a_h and c_t
+    this separates ReLU-per-head from ReLU-after-the-sum and the head weights."""
+    rng = np.random.default_rng(1)
+    HI, DI, n = 16, 64, 40
+    u = rng.standard_normal(DI)
+    a = rng.standard_normal(HI)
+    c = rng.standard_normal(n)
+    w = rng.uniform(0, 1, HI)
+    qI = a[:, None] * u[None, :]
+    kI = c[:, None] * u[None, :]
+    uu = float(u @ u)
+    expect = np.array([sum(w[h] * max(0.0, a[h] * c[t] * uu) for h in range(HI))
+                       for t in range(n)])
+    got = mod.index_scores_row(qI, w, kI, n)
+    np.testing.assert_allclose(got, expect, rtol=1e-12, atol=1e-12)
+
+
+def check_indexer_loops(mod):
+    """Pure-Python loops on a tiny random case, including the causal limits of
+    S > 1 queries (R1) and a capacity larger than the live length."""
+    rng = np.random.default_rng(2)
+    B, S, HI, DI, cap = 2, 3, 3, 5, 9
+    T = np.array([7, 4])
+    qI = rng.standard_normal((B, S, HI, DI))
+    w = rng.uniform(0, 1, (B, S, HI))
+    kI = rng.standard_normal((B, cap, DI))
+    got = mod.index_scores(qI, w, kI, T)
+    for b in range(B):
+        for s in range(S):
+            n = T[b] - S + s + 1
+            for t in range(cap):
+                if t >= n:
+                    assert np.isnan(got[b, s, t])
+                    continue
+                tot = 0.0
+                for h in range(HI):
+                    d = 0.0
+                    for i in range(DI):
+                        d += qI[b, s, h, i] * kI[b, t, i]
+                    tot += w[b, s, h] * (d if d > 0 else 0.0)
+                assert abs(got[b, s, t] - tot) <= 1e-12 * (1 + abs(tot))
+
+
+def torch_dense_reference(q, k, v, T, softmax_scale=None):
+    """Dense causal GQA attention via torch's scaled_dot_product_attention in
+    float64 (the library routine the sparse method reduces to when every
+    visible key is selected)."""
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    out = np.zeros(q.shape)
+    for b in range(B):
+        n_all = int(T[b])
+        qt = torch.from_numpy(q[b]).permute(1, 0, 2)                 # [Hq,S,D]
+        kt = torch.from_numpy(k[b, :n_all]).permute(1, 0, 2)          # [Hkv,n,D]
+        vt = torch.from_numpy(v[b, :n_all]).permute(1, 0, 2)
+        kt = kt.repeat_interleave(G, dim=0)
+        vt = vt.repeat_interleave(G, dim=0)
+        pos = torch.arange(n_all - S, n_all)
+        mask = torch.arange(n_all)[None, :] <= pos[:, None]           # [S,n]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt, vt, attn_mask=mask, scale=softmax_scale)
+        out[b] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def check_dense_equivalence(mod):
+    wl = small_workload(batch=2, q_len=3, total_len=50, num_q_heads=6,
+                        num_kv_heads=2, top_k=64, seed=11)
+    inp = {k: to_f64(v) if isinstance(v, torch.Tensor) else v
+           for k, v in make_inputs(wl).items()}
+    res = mod.sparse_attention_step(inp, wl.num_kv_heads, wl.top_k)
+    ref = torch_dense_reference(inp["q"], inp["k"], inp["v"], inp["total_len"])
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-10, atol=1e-12)
+
+
+def check_worked_example(mod, spacing=0):
+    """PR #33847's case through the oracle's attention: q = 88 e_0, K codes
+    0 and e_0 (k_scale 1), V codes 1 and 0 with value scale 2^120, softmax
+    scale 1. ``spacing`` inserts keys with logit -1000 between the two
+    candidates (weights e^-1088 are exactly 0 in float64)."""
+    fx = _load("int8_rescale_worked_example.json")
+    D = 128
+    m = 2 + spacing
+    q = np.zeros((1, 1, 1, D))
+    q[0, 0, 0, 0] = 88.0
+    k = np.zeros((1, m, 1, D))
+    k[0, m - 1, 0, 0] = 1.0
+    k[0, 1:m - 1, 0, 0] = -1000.0 / 88.0
+    v = np.zeros((1, m, 1, D))
+    v[0, 0, 0, :] = fx["value_codes"][0]
+    v[0, m - 1, 0, :] = fx["value_codes"][1]
+    ks = np.ones((1, m, 1))
+    vs = np.full((1, m, 1), 2.0 ** fx["value_scale_log2"])
+    idx = np.arange(m)[None, None, :]
+    out = mod.sparse_attention(q, k, v, idx, 1, ks, vs, softmax_scale=1.0)
+    expect = 2.0 ** 120 * math.exp(-88) / (1 + math.exp(-88))
+    np.testing.assert_allclose(out[0, 0, 0], expect, rtol=1e-12)
+    assert round(out[0, 0, 0, 0], 4) == pytest.approx(fx["printed_value"], abs=5e-4)
+
+
+# ---------------------------------------------------------------------------
+# the pins
+# ---------------------------------------------------------------------------
+def test_topk_golden_fixture():
+    check_topk_fixture(O)
+
+
+def test_topk_bruteforce_tiny():
+    check_topk_bruteforce(O)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_topk_invariants_tie_heavy(seed):
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(40):
+        n = int(rng.integers(1, 300))
+        s = rng.integers(-3, 4, size=n).astype(np.float64)
+        if rng.random() < 0.3:
+            s[rng.integers(0, n, size=max(1, n // 5))] = -0.0
+        for k in (1, max(1, n // 3), n, n + 7):
+            assert is_valid_topk(s, k, O.topk_select_row(s, k))
+
+
+def test_topk_distinct_values_matches_argpartition():
+    rng = np.random.default_rng(3)
+    for n in (1, 17, 2048, 5000):
+        s = rng.permutation(n).astype(np.float64) * 0.5 - 7.0
+        for k in (1, min(n, 512), n):
+            expect = np.sort(np.argpartition(-s, k - 1)[:k])
+            assert O.topk_select_row(s, k)[:k].tolist() == expect.tolist()
+
+
+def test_indexer_golden_fixture():
+    check_indexer_fixture(O)
+
+
+def test_indexer_closed_form():
+    check_indexer_closed_form(O)
+
+
+def test_indexer_loops_causal():
+    check_indexer_loops(O)
+
+
+def test_visible_len_positions():
+    assert O.visible_len(4096, 1, 0) == 4096
+    assert [O.visible_len(40960, 8192, s) for s in (0, 8191)] == [32769, 40960]
+    with pytest.raises(ValueError):
+        O.visible_len(3, 5, 0)
+
+
+def test_dense_equivalence_when_topk_covers_all():
+    check_dense_equivalence(O)
+
+
+def test_worked_example_large_value_scale():
+    for spacing in (0, 1, 15, 40):
+        check_worked_example(O, spacing)
+
+
+def test_permutation_invariance():
+    wl = small_workload(batch=1, q_len=1, total_len=300, num_q_heads=8,
+                        num_kv_heads=2, top_k=37, seed=5)
+    inp = {k: to_f64(v) if isinstance(v, torch.Tensor) else v
+           for k, v in make_inputs(wl).items()}
+    base = O.sparse_attention_step(inp, 2, wl.top_k)
+    perm = np.random.default_rng(0).permutation(wl.total_len)
+    p = dict(inp)
+    for key in ("kI", "k", "v"):
+        p[key] = inp[key][:, perm]
+    got = O.sparse_attention_step(p, 2, wl.top_k)
+    np.testing.assert_allclose(got["out"], base["out"], rtol=1e-12, atol=1e-13)
+    # the selected rows are the same rows, renamed by the permutation
+    sel_b = set(base["idx"][0, 0].tolist())
+    sel_p = set(perm[got["idx"][0, 0]].tolist())
+    assert sel_b == sel_p
+
+
+def test_uniform_query_gives_mean_of_selected_values():
+    wl = small_workload(batch=2, q_len=2, total_len=200, num_q_heads=4,
+                        num_kv_heads=2, top_k=50, seed=6)
+    inp = {k: to_f64(v) if isinstance(v, torch.Tensor) else v
+           for k, v in make_inputs(wl).items()}
+    inp["q"] = np.zeros_like(inp["q"])
+    res = O.sparse_attention_step(inp, 2, wl.top_k)
+    for b in range(2):
+        for s in range(2):
+            sel = res["idx"][b, s]
+            sel = sel[sel >= 0]
+            for h in range(4):
+                g = h // 2
+                np.testing.assert_allclose(res["out"][b, s, h],
+                                           inp["v"][b, sel, g].mean(axis=0),
+                                           rtol=1e-12, atol=1e-14)
+
+
+def test_zero_index_keys_select_the_prefix():
+    wl = small_workload(batch=1, q_len=4, total_len=100, top_k=30, seed=8)
+    inp = {k: to_f64(v) if isinstance(v, torch.Tensor) else v
+           for k, v in make_inputs(wl).items()}
+    inp["kI"] = np.zeros_like(inp["kI"])
+    res = O.sparse_attention_step(inp, 2, 30)
+    assert (res["scores"][0, 0, :97] == 0).all()
+    for s in range(4):
+        assert res["idx"][0, s].tolist() == list(range(30))
+    # top_k beyond the visible length: everything, then -1
+    res = O.sparse_attention_step(inp, 2, 99)
+    assert res["idx"][0, 0].tolist() == list(range(97)) + [-1, -1]
+
+
+def test_int8_path_reduces_to_plain_values():
+    rng = np.random.default_rng(9)
+    B, S, Hq, Hkv, D, m = 1, 2, 4, 2, 128, 60
+    q = rng.standard_normal((B, S, Hq, D))
+    codes_k = rng.integers(-127, 128, (B, m, Hkv, D)).astype(np.float64)
+    codes_v = rng.integers(-127, 128, (B, m, Hkv, D)).astype(np.float64)
+    idx = np.tile(np.arange(0, m, 2), (B, S, 1))
+    ones = np.ones((B, m, Hkv))
+    a = O.sparse_attention(q, codes_k, codes_v, idx, Hkv, ones, ones)
+    b = O.sparse_attention(q, codes_k, codes_v, idx, Hkv)
+    np.testing.assert_array_equal(a, b)
+    # and a power-of-two scale scales the values exactly
+    a2 = O.sparse_attention(q, codes_k, codes_v, idx, Hkv, ones, 4 * ones)
+    np.testing.assert_array_equal(a2, 4 * b)
+
+
+def test_full_step_on_workload_shapes():
+    wl = small_workload(batch=2, q_len=3, total_len=700, top_k=100,
+                        kv_dtype="int8", seed=10)
+    inp = {k: to_f64(v) if isinstance(v, torch.Tensor) else v
+           for k, v in make_inputs(wl).items()}
+    res = O.sparse_attention_step(inp, 2, 100)
+    assert res["out"].shape == (2, 3, 8, 128)
+    for b in range(2):
+        for s in range(3):
+            n = 700 - 3 + s + 1
+            assert is_valid_topk(res["scores"][b, s, :n], 100, res["idx"][b, s])
+
+
+# ---------------------------------------------------------------------------
+# mutation tests: plant a mistake in a copy of the oracle, a pin must fail
+# ---------------------------------------------------------------------------
+class _Mutant:
+    """A namespace that forwards to the oracle except for replaced functions;
+    replaced functions are resolved through this namespace, so a mutant inner
+    helper reaches the outer functions that call it."""
+
+    def __init__(self, **repl):
+        g = dict(O.__dict__)
+        g.update(repl)
+        for name, f in O.__dict__.items():
+            if name in repl or not callable(f) or getattr(f, "__module__", "") != O.__name__:
+                continue
+            if hasattr(f, "__code__"):
+                g[name] = type(f)(f.__code__, g, f.__name__, f.__defaults__, f.__closure__)
+        self._ns = g
+
+    def __getattr__(self, name):
+        return self._ns[name]
+
+
+def _fails(check, mod):
+    try:
+        check(mod)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_mutant_relu_after_head_sum_is_caught():
+    def bad(qI_s, w_s, kI_b, n):
+        return np.maximum((kI_b[:n] @ qI_s.T) @ w_s, 0.0)
+    m = _Mutant(index_scores_row=bad)
+    assert _fails(check_indexer_fixture, m) and _fails(check_indexer_closed_form, m)
+
+
+def test_mutant_dropped_head_weight_is_caught():
+    def bad(qI_s, w_s, kI_b, n):
+        return np.maximum(kI_b[:n] @ qI_s.T, 0.0).sum(axis=1)
+    assert _fails(check_indexer_fixture, _Mutant(index_scores_row=bad))
+
+
+def test_mutant_transposed_operand_is_caught():
+    def bad(qI_s, w_s, kI_b, n):   # heads and dims mixed up where shapes allow
+        return np.maximum(kI_b[:n] @ qI_s.T[::-1], 0.0) @ w_s
+    assert _fails(check_indexer_fixture, _Mutant(index_scores_row=bad))
+
+
+def test_mutant_causal_off_by_one_is_caught():
+    def bad(T, S, s):
+        return T - S + s
+    assert _fails(check_indexer_loops, _Mutant(visible_len=bad))
+
+
+def test_mutant_tie_to_higher_index_is_caught():
+    def bad(scores, k):
+        v = np.asarray(scores, dtype=np.float64) + 0.0
+        n = v.shape[0]
+        keff = min(k, n)
+        order = np.lexsort((-np.arange(n), -v))
+        out = np.full(k, -1, dtype=np.int64)
+        out[:keff] = np.sort(order[:keff])
+        return out
+    m = _Mutant(topk_select_row=bad)
+    assert _fails(check_topk_fixture, m) and _fails(check_topk_bruteforce, m)
+
+
+def test_mutant_wrong_gqa_grouping_is_caught():
+    def bad(q, k, v, idx, num_kv_heads, k_scale=None, v_scale=None,
+            softmax_scale=0.0, rows=None):
+        B, S, Hq, D = q.shape
+        scale = softmax_scale if softmax_scale else 1.0 / np.sqrt(D)
+        out = np.full(q.shape, np.nan)
+        for b in range(B):
+            for s in range(S):
+                sel = idx[b, s][idx[b, s] >= 0]
+                Kb = O.dequantize(k[b, sel], None if k_scale is None else k_scale[b, sel])
+                Vb = O.dequantize(v[b, sel], None if v_scale is None else v_scale[b, sel])
+                for h in range(Hq):
+                    g = h % num_kv_heads          # interleaved instead of consecutive
+                    out[b, s, h] = O.attend_row(q[b, s, h], Kb[:, g], Vb[:, g], scale)
+        return out
+    assert _fails(check_dense_equivalence, _Mutant(sparse_attention=bad))
+
+
+def test_mutant_wrong_softmax_scale_is_caught():
+    def bad(q_h, Kg, Vg, scale):
+        logits = (Kg @ q_h) / Kg.shape[1]
+        p = np.exp(logits - logits.max())
+        return (p / p.sum()) @ Vg
+    assert _fails(check_dense_equivalence, _Mutant(attend_row=bad))
+
+
+def test_mutant_value_scale_dropped_is_caught():
+    def bad(codes, scale):
+        return codes
+    assert _fails(check_worked_example, _Mutant(dequantize=bad))

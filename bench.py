@@ -1,0 +1,378 @@
+"""Benchmark: decode query-tokens/s and achieved HBM GB/s of the dynamic
+sparse attention step (indexer -> radix top-k -> sparse GQA attention) at a
+131,072-token context with top_k = 2,048, on synthetic data.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libdsa|reference]
+                    [--workload NAME] [--no-graph]
+
+One JSON line on stdout (rank 0). A step is one call of the whole decode path
+(dsa_sparse_attn_decode) over one batch of query tokens with inputs resident
+in HBM; L2 is flushed (a 256 MiB write) before every timed step, and each
+step is timed with CUDA events on the stream the kernels run on. By default
+the step is replayed from a CUDA graph captured around the C-ABI call; `e2e`
+times the same call eagerly with the step's inputs copied from pinned host
+memory and its output copied back. Under torchrun every rank runs its own
+replica of the workload (the path shards by sequence with no exchange:
+weak scaling); the slowest rank's time is reported.
+
+--impl reference times the float64 CPU oracle on the same workload (rank 0
+only) -- a deliberately slow baseline, not the optimisation target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode query-tokens/s and achieved HBM GB/s (% of peak) at L=128K, top_k=2048"
+UNIT = "query-tokens/s"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic bytes
+def algorithmic_bytes(wl, idx_np=None):
+    """Bytes the method itself must move per step (DRAM), excluding work the
+    sparse method avoids: every visible index key once, the fp32 scores
+    written and read back, the unique selected K/V rows (with their scales),
+    q, qI, w, the index rows and the output."""
+    import numpy as np
+    B, S = wl.batch, wl.q_len
+    kv_elem = 1 if wl.kv_dtype == "int8" else 2
+    row_kv = wl.num_kv_heads * (128 * kv_elem + (4 if wl.kv_dtype == "int8" else 0))
+    n_vis = [[wl.total_len - S + s + 1 for s in range(S)] for _ in range(B)]
+    kI = B * wl.total_len * 64 * 2
+    scores = sum(sum(r) for r in n_vis) * 4 * 2
+    if idx_np is not None:
+        uniq = sum(len(np.unique(idx_np[b][idx_np[b] >= 0])) for b in range(B))
+    else:
+        uniq = B * min(wl.top_k, wl.total_len)
+    kv = uniq * row_kv * 2
+    small = B * S * (16 * 64 * 2 + 16 * 4 + wl.num_q_heads * 128 * 2 * 2 + wl.top_k * 4 * 2)
+    indexer = kI + scores // 2 + B * S * (16 * 64 * 2 + 16 * 4)
+    return {"step": kI + scores + kv + small, "indexer": indexer, "kv": kv}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if len(r) >= 8 and r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if len(r) >= 8 and r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) < 8:
+                continue
+            for i, n in enumerate(names):
+                if r[4 + i].lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_step_time(wl, cpu, budget_s=10.0, max_reps=50):
+    """Time the float64 oracle on full steps of the workload (bounded)."""
+    import numpy as np
+    import oracle.dsa_oracle as O
+    from dsa_inputs import to_f64
+    f = {k: to_f64(v) if hasattr(v, "numpy") else v for k, v in cpu.items()}
+    f["total_len"] = cpu["total_len"].numpy().astype(np.int64)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < max_reps and (not times or time.perf_counter() < t_end):
+        t0 = time.perf_counter()
+        O.sparse_attention_step(f, wl.num_kv_heads, wl.top_k)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from dsa_inputs import make_inputs
+    cpu = make_inputs(wl)
+    for _ in range(args.warmup):
+        oracle_step_time(wl, cpu, budget_s=0.0, max_reps=1)
+    times = []
+    for _ in range(args.steps):
+        times += oracle_step_time(wl, cpu, budget_s=0.0, max_reps=1)
+    ms = 1e3 * statistics.mean(times)
+    value = wl.query_tokens / (ms / 1e3)
+    sample = f"full {wl.name} step ({wl.query_tokens} query tokens) per timed step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, graph=False),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, graph):
+    return {"workload": wl.name, "batch": wl.batch, "q_len": wl.q_len,
+            "context": wl.total_len, "top_k": wl.top_k, "q_heads": wl.num_q_heads,
+            "kv_heads": wl.num_kv_heads, "head_dim": 128, "index_heads": 16, "index_dim": 64,
+            "q_dtype": wl.q_dtype, "kv_dtype": wl.kv_dtype,
+            "l2": "flushed before every timed step (256 MiB write)",
+            "cuda_graph": bool(graph)}
+
+
+# ------------------------------------------------------------------ libdsa arm
+def run_libdsa(args, wl):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from dsa_inputs import make_inputs
+    from top_sparse_attention_chunked_gb300 import build_lib
+    from top_sparse_attention_chunked_gb300 import dsa as D
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build_lib.build()
+    D.load_library()
+    dev_index = torch.cuda.current_device()
+
+    cpu = make_inputs(wl, seed=wl.seed + 7919 * rank)   # an independent replica per rank
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    p = D.problem_for(wl)
+    ws = D.alloc_workspace(p, D.DSA_OP_DECODE)
+    out = torch.empty(wl.batch, wl.q_len, wl.num_q_heads, 128, dtype=D._TORCH_DT[p.out_dtype],
+                      device="cuda")
+    idx = torch.empty(wl.batch, wl.q_len, wl.top_k, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        D.dsa_sparse_attn_decode(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"],
+                                 dev["v"], dev["k_scale"], dev["v_scale"], idx, out, ws)
+
+    D.dsa_timing_select(D.DSA_KERNEL_INDEXER)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert D.dsa_read_device_status(ws) == 0
+    graph = None
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def run_once():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    # ---------------- timed region: K steps, L2 flushed before each
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    idx_ms = []
+    clocks = ClockSampler(dev_index)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        run_once()
+        evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        idx_ms.append(D.dsa_timing_read())
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    D.dsa_timing_select(-1)
+    idx_np = idx.cpu().numpy()
+    ab = algorithmic_bytes(wl, idx_np)
+    hbm, bf16, peak_kind = peaks()
+    value = world * wl.query_tokens / (ms / 1e3)
+
+    # ---------------- per-kernel breakdown (separate short eager loop)
+    per_kernel = {}
+    for name, kind in (("indexer", D.DSA_KERNEL_INDEXER), ("topk_select", D.DSA_KERNEL_TOPK_SELECT),
+                       ("attention", D.DSA_KERNEL_ATTENTION)):
+        D.dsa_timing_select(kind)
+        vals = []
+        for _ in range(10):
+            flush.zero_()
+            step()
+            torch.cuda.synchronize()
+            vals.append(D.dsa_timing_read())
+        per_kernel[name] = round(1e3 * statistics.median(vals), 2)
+    D.dsa_timing_select(-1)
+
+    # ---------------- end to end through the C ABI with host buffers
+    pin = {k: cpu[k].pin_memory() for k in ("q", "qI", "w")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = out_h.numel() * out_h.element_size()
+    for _ in range(3):
+        for k2 in pin:
+            dev[k2].copy_(pin[k2], non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k2 in pin:
+            dev[k2].copy_(pin[k2], non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = world * wl.query_tokens / (statistics.mean(e2e_ms) / 1e3)
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only)
+    cpu_base = None
+    if rank == 0 and world == 1:
+        times = oracle_step_time(wl, cpu, budget_s=args.cpu_budget)
+        cpu_base = {"value": wl.query_tokens / statistics.mean(times), "unit": UNIT,
+                    "cores": cores(), "kind": "oracle",
+                    "sample": f"{len(times)} full {wl.name} steps ({wl.query_tokens} query "
+                              f"token(s) each) in float64 NumPy"}
+
+    idx_us = 1e3 * statistics.mean(idx_ms)
+    achieved = ab["indexer"] / (idx_us * 1e-6) / 1e9
+    step_gbs = ab["step"] / (ms * 1e-3) / 1e9
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) / U(0,1) tensors, see dsa_inputs.py)",
+            "config": config_of(wl, graph is not None),
+            "hbm_gbs_step": round(step_gbs, 1),
+            "hbm_frac_step": round(step_gbs / hbm, 4),
+            "hbm_frac_step_of_8tbs": round(step_gbs / 8000.0, 4),
+            "algorithmic_bytes_step": ab["step"],
+            "roofline": {"kernel": "indexer_tc_kernel", "bound": "hbm",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+                         "traffic": None, "algorithmic_bytes": ab["indexer"],
+                         "launch_us": round(idx_us, 2)},
+            "per_kernel_us": per_kernel,
+            "cpu_baseline": cpu_base,
+            "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="libdsa", choices=["libdsa", "reference"])
+    ap.add_argument("--workload", default="decode_128k")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from dsa_inputs import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_libdsa(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * libdsa -- dynamic sparse attention on one NVIDIA GB300 (sm_103a).
+ *
+ * For each query token the step does three things (pages: ONNX Runtime PR
+ * #33802 "[CUDA] Optimize Qwen3.8-Flash-Next DSA, Indexer, HC, and QMoE kernels
+ * for SM12x and 256K context", Summary items 1-2, and PR #33997 "[CUDA] Support
+ * FP16 KV cache and FP16 query/key in DynamicSparseAttention<BFloat16> ...",
+ * Description item 2):
+ *
+ *   1. indexer   score[t] = sum_h w[h] * max(0, qI[h] . kI[t])   (16 index
+ *                heads of dim 64 against one index key per cached token,
+ *                fp32 accumulation), streamed in 2,048-key chunks;
+ *   2. top-k     the top_k highest-scoring visible keys (ties -> lower index),
+ *                a radix select over per-chunk histograms with one final
+ *                merge-and-emit;
+ *   3. attention softmax GQA attention of every query head over only the
+ *                selected K/V rows (BF16, FP16 or INT8 with a per-token
+ *                per-head fp32 scale), split over the selected keys with an
+ *                online-softmax combine (follow-up PR #33847: the rescale never
+ *                flushes the earlier tiles).
+ *
+ * Conventions (all calls):
+ *  - Positions: a sequence's cache holds T_b = total_len[b] rows and its
+ *    q_len new query tokens are the LAST q_len rows, so query s sits at
+ *    position T_b - q_len + s and sees keys 0 .. T_b - q_len + s (causal,
+ *    itself included). Prefill and decode follow the same rule.
+ *  - Every tensor argument is a DEVICE pointer owned by the caller, dense
+ *    row-major in the layout stated beside it. The library allocates no
+ *    device memory and never synchronises the stream: every call enqueues
+ *    its kernels on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and returns. It can be captured in a CUDA graph.
+ *  - Arguments are validated on the host before anything is enqueued; on a
+ *    bad argument nothing is launched and the call returns the status, with
+ *    a message in dsa_last_error_string().
+ *  - The workspace is caller-owned device memory of at least
+ *    dsa_workspace_size() bytes, 256-byte aligned. Its contents are never
+ *    assumed: each call initialises what it uses. Calls that share a
+ *    workspace must be ordered on one stream.
+ *  - Problems a kernel detects (a bounded wait that ran out) are OR-ed into a
+ *    status word at the start of the workspace; read it with
+ *    dsa_read_device_status() after the call.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* shape, length or pointer is wrong          */
+  DSA_ERR_UNSUPPORTED = 2,   /* valid but not built (dims, dtype combo)     */
+  DSA_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small  */
+  DSA_ERR_MISALIGNED = 4,    /* a tensor pointer breaks its alignment rule  */
+  DSA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed           */
+  DSA_ERR_TIMEOUT = 6,       /* a kernel's bounded wait ran out (device)    */
+  DSA_ERR_NO_DEVICE = 7      /* no usable sm_100-class GPU is current       */
+} dsa_status;
+
+typedef enum dsa_dtype {
+  DSA_BF16 = 0,
+  DSA_FP16 = 1,
+  DSA_INT8 = 2,              /* KV cache only: codes + fp32 scale per token/head */
+  DSA_FP32 = 3               /* output only */
+} dsa_dtype;
+
+/* Which call a workspace is sized for. */
+typedef enum dsa_op {
+  DSA_OP_INDEX_SCORES = 0,
+  DSA_OP_TOPK = 1,
+  DSA_OP_DECODE = 2,
+  DSA_OP_PREFILL = 3
+} dsa_op;
+
+/* Built-in limits. */
+#define DSA_MAX_BATCH 64          /* sequences per call                          */
+#define DSA_HEAD_DIM 128          /* attention head dim                          */
+#define DSA_IDX_HEADS 16          /* index heads                                 */
+#define DSA_IDX_DIM 64            /* index head dim                              */
+#define DSA_CHUNK 2048            /* indexer / top-k chunk (keys)                */
+#define DSA_MAX_DECODE_Q_LEN 16   /* query tokens per sequence in decode         */
+#define DSA_MAX_CONTEXT (1 << 20) /* visible keys per query row                  */
+
+/*
+ * The problem, passed by pointer to every call (read on the host only, so it
+ * may live on the stack).
+ *
+ *   batch            B, 1 .. DSA_MAX_BATCH
+ *   q_len            S, new query tokens per sequence (>= 1; <= 16 in decode)
+ *   num_q_heads      Hq
+ *   num_kv_heads     Hkv, Hq % Hkv == 0; head h reads KV head h / (Hq/Hkv)
+ *   head_dim         D, must be 128
+ *   idx_heads        must be 16
+ *   idx_dim          must be 64
+ *   cache_capacity   cap: rows allocated per sequence in kI/K/V/scales; also
+ *                    the row stride of the score tensor
+ *   top_k            1 .. cap; a query with n < top_k visible keys selects
+ *                    all n and pads its index row with -1
+ *   total_len[b]     T_b, q_len .. cap (entries >= batch are ignored)
+ *   softmax_scale    logits = softmax_scale * q.K; 0 selects 1/sqrt(head_dim)
+ *   q_dtype          DSA_BF16 or DSA_FP16
+ *   kv_dtype         DSA_BF16, DSA_FP16 or DSA_INT8 (FP16 query with a BF16
+ *                    cache is not built)
+ *   out_dtype        DSA_BF16, DSA_FP16 or DSA_FP32
+ *   attn_split_keys  0 = automatic; otherwise selected keys per split-K
+ *                    attention block, a multiple of 16 (a tuning and testing
+ *                    knob: results agree for every value)
+ */
+typedef struct dsa_problem {
+  int32_t batch;
+  int32_t q_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t idx_heads;
+  int32_t idx_dim;
+  int32_t cache_capacity;
+  int32_t top_k;
+  int32_t total_len[DSA_MAX_BATCH];
+  float softmax_scale;
+  int32_t q_dtype;
+  int32_t kv_dtype;
+  int32_t out_dtype;
+  int32_t attn_split_keys;
+} dsa_problem;
+
+/*
+ * Bytes of workspace the call `op` needs for problem `p` (0 and a message in
+ * dsa_last_error_string() if `p` is invalid). Pure host computation.
+ */
+size_t dsa_workspace_size(const dsa_problem* p, int op);
+
+/*
+ * dsa_index_scores -- the indexer alone (step 1). PR #33802 Summary item 2
+ * (PackedSparseAttentionIndexer: per-query scoring of every cached index key).
+ *
+ *   qI      [B, S, 16, 64] bf16, 16-byte aligned
+ *   w       [B, S, 16] fp32 head weights
+ *   kI      [B, cap, 64] bf16 index keys, 16-byte aligned
+ *   scores  [B, S, cap] fp32 out: scores[b,s,t] for t <= T_b - S + s; entries
+ *           past a query's visible length are not written. 16-byte aligned.
+ * Runs on tcgen05 tensor cores (BF16 x BF16 -> FP32 in tensor memory).
+ */
+int dsa_index_scores(const dsa_problem* p, const void* qI, const float* w,
+                     const void* kI, float* scores, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_topk -- the selection alone (step 2) on a given fp32 score tensor.
+ * PR #33802 Summary item 2 (radix partial top-k per 2,048-key chunk with
+ * warp-aggregated histograms, one final merge-and-emit).
+ *
+ *   scores  [B, S, cap] fp32; only the visible prefix of each row is read.
+ *           Values are compared exactly; -0.0 equals +0.0; NaN is not allowed.
+ *   idx     [B, S, top_k] int32 out: the selected key indices in ascending
+ *           order, then -1 up to top_k.
+ * The result is exact (bit-identical to sorting by (-score, index)).
+ */
+int dsa_topk(const dsa_problem* p, const float* scores, int32_t* idx,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dsa_sparse_attn_decode -- the whole step for a few query tokens per
+ * sequence (S <= 16): indexer (with the chunk histograms fused in), top-k,
+ * then grouped split-K sparse attention. PR #33997 Description item 2
+ * (grouped decode over the selected rows), PR #33802 Summary item 1 (INT8
+ * cache, split-K decode), PR #33847 (rescale without flushing).
+ *
+ *   q        [B, S, Hq, 128] q_dtype, 16-byte aligned
+ *   qI, w, kI as for dsa_index_scores
+ *   k, v     [B, cap, Hkv, 128] kv_dtype (values, or INT8 codes), 16-byte aligned
+ *   k_scale, v_scale  [B, cap, Hkv] fp32, required iff kv_dtype == DSA_INT8
+ *            (else must be NULL): K^ = code * k_scale
+ *   idx_out  [B, S, top_k] int32 (optional, NULL allowed): receives the
+ *            selected indices as dsa_topk emits them
+ *   out      [B, S, Hq, 128] out_dtype
+ */
+int dsa_sparse_attn_decode(const dsa_problem* p, const void* q, const void* qI,
+                           const float* w, const void* kI, const void* k,
+                           const void* v, const float* k_scale,
+                           const float* v_scale, int32_t* idx_out, void* out,
+                           void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * dsa_sparse_attn_prefill -- the whole step for a chunk of many new tokens
+ * (any S >= 1): the indexer as a dense causal contraction on tcgen05 tensor
+ * cores, a per-row top-k held in shared memory, then sparse attention.
+ * Same arguments and layouts as dsa_sparse_attn_decode. PR #33997
+ * Description item 2 (sparse-attention prefill on tensor cores), PR #33802
+ * Summary item 2 (ragged prefill scoring).
+ */
+int dsa_sparse_attn_prefill(const dsa_problem* p, const void* q, const void* qI,
+                            const float* w, const void* kI, const void* k,
+                            const void* v, const float* k_scale,
+                            const float* v_scale, int32_t* idx_out, void* out,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * Synchronises `stream`, then copies the device status word from the
+ * workspace to *status_out (0 = no device-side problem; bit 0 = a bounded
+ * wait ran out). Returns DSA_ERR_TIMEOUT if that bit is set.
+ */
+int dsa_read_device_status(const void* workspace, size_t workspace_bytes,
+                           void* stream, uint32_t* status_out);
+
+/* Message for the last failed call on this host thread ("" if none). */
+const char* dsa_last_error_string(void);
+
+/* Name of a status code. */
+const char* dsa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+/*
+ * Kernel timing (diagnostics). dsa_timing_select(kind) makes the following
+ * calls on this host thread record a pair of CUDA events around every launch
+ * of one kernel kind (DSA_KERNEL_*) on the caller's stream (-1 turns it off;
+ * the events are recorded as external nodes under stream capture).
+ * dsa_timing_read() waits for the most recent pair and returns its elapsed
+ * milliseconds. Events are created on first use and kept for the thread.
+ */
+enum {
+  DSA_KERNEL_INDEXER = 0,       /* tcgen05 indexer (decode and prefill)      */
+  DSA_KERNEL_TOPK_HIST = 1,     /* chunk histograms (dsa_topk only)           */
+  DSA_KERNEL_TOPK_SELECT = 2,   /* chunk select + final merge-and-emit        */
+  DSA_KERNEL_TOPK_ROW = 3,      /* whole-row shared-memory select             */
+  DSA_KERNEL_ATTENTION = 4      /* sparse attention (+ split combine)         */
+};
+int dsa_timing_select(int kernel_kind);
+int dsa_timing_read(float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,124 @@
+"""Host-side checks of libdsa that need no GPU: the shared library builds for
+sm_103a, loads, exports every function include/dsa.h declares, sizes
+workspaces, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_sparse_attention_chunked_gb300 import build_lib, dsa
+    build_lib.build()
+    return dsa.load_library()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_functions_are_exported(lib):
+    names = header_functions()
+    assert "dsa_sparse_attn_decode" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in dsa.h but not exported"
+
+
+def test_binding_names_match_header():
+    from top_sparse_attention_chunked_gb300 import dsa
+    assert sorted(dsa.EXPORTED) == header_functions()
+
+
+def test_problem_struct_matches_header():
+    from top_sparse_attention_chunked_gb300.dsa import DsaProblem
+    # 9 ints, 64 lengths, 1 float, 4 ints
+    assert ctypes.sizeof(DsaProblem) == 4 * (9 + 64 + 1 + 4)
+
+
+def _prob(**kw):
+    from top_sparse_attention_chunked_gb300.dsa import make_problem
+    base = dict(batch=1, q_len=1, total_len=131072, top_k=2048, num_q_heads=24,
+                num_kv_heads=2, kv_dtype="fp16")
+    base.update(kw)
+    return make_problem(**base)
+
+
+def test_workspace_sizes(lib):
+    from top_sparse_attention_chunked_gb300.dsa import (DSA_OP_DECODE, DSA_OP_PREFILL,
+                                                        DSA_OP_TOPK, dsa_workspace_size)
+    n = dsa_workspace_size(_prob(), DSA_OP_DECODE)
+    # scores (512 KiB) + candidates (1 MiB) + bitmap + idx + histograms
+    assert 1_500_000 < n < 4_000_000
+    pre = _prob(q_len=8192, total_len=40960, kv_dtype="bf16")
+    m = dsa_workspace_size(pre, DSA_OP_PREFILL)
+    assert m >= 8192 * 40960 * 4            # the materialised scores
+    assert dsa_workspace_size(_prob(q_len=8, total_len=262144), DSA_OP_TOPK) > 8 * 262144 * 8
+
+
+@pytest.mark.parametrize("kw,frag", [
+    (dict(batch=0), "batch"),
+    (dict(batch=65), "batch"),
+    (dict(top_k=0), "top_k"),
+    (dict(top_k=200000), "top_k"),
+    (dict(total_len=[131073], cache_capacity=131072), "total_len"),
+    (dict(q_len=2, total_len=1, cache_capacity=16, top_k=1), "total_len"),
+    (dict(num_q_heads=25), "multiple"),
+    (dict(head_dim=64), "head_dim"),
+    (dict(idx_heads=8), "index heads"),
+    (dict(q_dtype="fp16", kv_dtype="bf16"), "FP16 query"),
+    (dict(q_len=17, total_len=4096), "decode takes"),
+    (dict(attn_split_keys=24), "attn_split_keys"),
+])
+def test_invalid_problems_rejected_on_host(lib, kw, frag):
+    from top_sparse_attention_chunked_gb300.dsa import DSA_OP_DECODE
+    p = _prob(**kw)
+    assert lib.dsa_workspace_size(ctypes.byref(p), DSA_OP_DECODE) == 0
+    assert frag in lib.dsa_last_error_string().decode()
+
+
+def _call_decode(lib, p, ws_bytes, ptrs=None, ws=0x10000):
+    a = ptrs or {}
+    vals = [a.get(n, 0x1000) for n in ("q", "qI", "w", "kI", "k", "v")]
+    return lib.dsa_sparse_attn_decode(ctypes.byref(p), *[ctypes.c_void_p(v) for v in vals],
+                                      ctypes.c_void_p(a.get("ks")), ctypes.c_void_p(a.get("vs")),
+                                      None, ctypes.c_void_p(a.get("out", 0x2000)),
+                                      ctypes.c_void_p(ws), ws_bytes, None)
+
+
+def test_bad_pointers_rejected_before_cuda(lib):
+    from top_sparse_attention_chunked_gb300.dsa import (DSA_ERR_INVALID_ARG, DSA_ERR_MISALIGNED,
+                                                        DSA_ERR_WORKSPACE, DSA_OP_DECODE)
+    p = _prob()
+    need = lib.dsa_workspace_size(ctypes.byref(p), DSA_OP_DECODE)
+    assert _call_decode(lib, p, need, {"q": 0}) == DSA_ERR_INVALID_ARG
+    assert _call_decode(lib, p, need, {"kI": 0x1008}) == DSA_ERR_MISALIGNED
+    assert _call_decode(lib, p, need - 1) == DSA_ERR_WORKSPACE
+    assert _call_decode(lib, p, need, ws=0x10010) == DSA_ERR_WORKSPACE
+    # scales only with an INT8 cache
+    assert _call_decode(lib, p, need, {"ks": 0x3000, "vs": 0x3000}) == DSA_ERR_INVALID_ARG
+    p8 = _prob(kv_dtype="int8")
+    need8 = lib.dsa_workspace_size(ctypes.byref(p8), DSA_OP_DECODE)
+    assert _call_decode(lib, p8, need8) == DSA_ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_NO_DEVICE, DSA_OP_DECODE
+    p = _prob()
+    need = lib.dsa_workspace_size(ctypes.byref(p), DSA_OP_DECODE)
+    assert _call_decode(lib, p, need) == DSA_ERR_NO_DEVICE
+
+
+def test_status_strings(lib):
+    assert lib.dsa_status_string(0) == b"DSA_OK"
+    assert lib.dsa_status_string(6) == b"DSA_ERR_TIMEOUT"
+    assert lib.dsa_version() >= 100

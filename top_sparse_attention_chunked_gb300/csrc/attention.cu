@@ -1,0 +1,470 @@
+// Sparse GQA attention over the selected K/V rows, split over the selected
+// keys, with an online-softmax combine.
+//
+// PR #33997 "[CUDA] Support FP16 KV cache and FP16 query/key in
+// DynamicSparseAttention<BFloat16> ...", Description item 2: a grouped decode
+// kernel processes the query heads of one KV head together over the selected
+// rows (the pages' test is a group ratio of 12) and a tensor-core prefill kernel
+// with FP16 operands (mma m16n8k16 f32.f16.f16.f32) for BF16 activations with
+// an FP16 cache. PR #33802 Summary item 1: INT8 cache with split-K decode.
+// Follow-up PR #33847: rescaling the PV accumulator by exp2(old_max - new_max)
+// must not flush the earlier tiles to zero when the max rises by ~88 nats.
+//
+// Layout of the work: one CTA per (split of the selected keys, KV head x group
+// of <= 16 query heads, query row). The group's query heads form the M = 16
+// rows of warp-level m16n8k16 MMAs; each warp gathers 16 selected rows of K
+// and V per tile with 16-byte cp.async into a swizzled double buffer, computes
+// S = Q K^T (16 heads x 16 keys), the online softmax in registers, and
+// O += P V. Warps, then splits, are merged with an LSE combine whose scaling
+// never forms a subnormal factor (mul_exp2).
+//
+// Precision: QK^T uses the cache's 16-bit type (a BF16 query is converted to
+// FP16 for an FP16 cache, as the pages' MmaFp16 path does); the probabilities
+// enter PV as FP16 for an FP16 cache and as a BF16 hi+lo pair otherwise, so
+// P keeps 16 significant bits. INT8 codes are exact in BF16/FP16; k_scale
+// multiplies the logit after the dot product and v_scale is folded into P.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dsa {
+
+constexpr int kAttnThreads = 128;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kTileKeys = 16;
+constexpr int kD = DSA_HEAD_DIM;
+constexpr int kTile16 = kTileKeys * kD * 2;      // 4 KB: one 16-key tile, 16-bit
+constexpr int kTile8 = kTileKeys * kD;           // 2 KB: one 16-key tile, INT8
+// Per-warp shared memory. 16-bit caches: K stage 0/1, V stage 0/1 (4 x 4 KB).
+// INT8: converted K and V tiles (2 x 4 KB), code staging K 0/1, V 0/1
+// (4 x 2 KB) and the k/v scales of both stages (256 B).
+constexpr int kWarpSmem = 4 * kTile16 + 2 * 4 * kTileKeys * 4;
+constexpr int kAttnSmem = kAttnWarps * kWarpSmem;
+
+enum { KV_BF16 = 0, KV_FP16 = 1, KV_INT8 = 2 };
+
+// byte offset of 16-byte chunk c of row r in a swizzled 16-bit tile
+__device__ __forceinline__ int swz(int r, int c) { return r * (kD * 2) + ((c ^ (r & 7)) << 4); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if constexpr (F16) return pack_f16(lo, hi);
+  else return pack_bf16(lo, hi);
+}
+
+// Load 2 consecutive query elements as the MMA operand type.
+template <bool Q_F16, bool OP_F16>
+__device__ __forceinline__ uint32_t load_q2(const void* q, size_t elem) {
+  const uint32_t raw = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(q) + elem);
+  if constexpr (Q_F16 == OP_F16) {
+    return raw;
+  } else if constexpr (Q_F16) {   // fp16 query, bf16 operand (INT8 cache only)
+    __half2 h = *reinterpret_cast<const __half2*>(&raw);
+    float2 f = __half22float2(h);
+    return pack_bf16(f.x, f.y);
+  } else {                        // bf16 query, fp16 operand
+    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float2 f = __bfloat1622float2(h);
+    return pack_f16(f.x, f.y);
+  }
+}
+
+// 16 INT8 codes -> 16 exact 16-bit values written as two swizzled chunks
+template <bool F16>
+__device__ __forceinline__ void convert_codes16(const uint4 src, uint8_t* tile, int row, int c0) {
+  const int8_t* b = reinterpret_cast<const int8_t*>(&src);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = pack16<F16>(static_cast<float>(b[2 * i]), static_cast<float>(b[2 * i + 1]));
+  *reinterpret_cast<uint4*>(tile + swz(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  *reinterpret_cast<uint4*>(tile + swz(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_out(void* out, size_t i, float v) {
+  if constexpr (OUT == DSA_BF16) static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+  else if constexpr (OUT == DSA_FP16) static_cast<__half*>(out)[i] = __float2half_rn(v);
+  else static_cast<float*>(out)[i] = v;
+}
+
+template <int KV, bool Q_F16, int OUT>
+__global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnParams p) {
+  constexpr bool QK_F16 = (KV == KV_FP16) || (KV == KV_INT8 && Q_F16);
+  constexpr bool PV_F16 = (KV == KV_FP16);
+  constexpr bool PV_SPLIT = !PV_F16;   // BF16 P as hi + lo
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates
+  const int r = blockIdx.z;                  // query row = b * S + s
+  const int b = r / p.S, s = r % p.S;
+  const int gh = blockIdx.y;                 // KV head x head group
+  const int g = gh / p.HG, hg = gh % p.HG;
+  const int h0 = g * p.G + hg * kAttnRows;
+  const int nh = min(kAttnRows, p.G - hg * kAttnRows);
+  const int T = p.lens.T[b];
+  const int keff = min(p.topk, visible_len(T, p.S, s));
+  const int split_begin = blockIdx.x * p.split_keys;
+  if (split_begin >= keff) return;
+  const int split_len = min(p.split_keys, keff - split_begin);
+  const int nreal = (keff + p.split_keys - 1) / p.split_keys;
+  const int ntiles = (split_len + kTileKeys - 1) / kTileKeys;
+
+  uint8_t* wsm = smem + warp * kWarpSmem;
+  uint8_t* sK[2] = {wsm, wsm + kTile16};
+  uint8_t* sV[2] = {wsm + 2 * kTile16, wsm + 3 * kTile16};
+  // INT8 only: converted tiles live in sK[0] / sK[1]'s space, staging after
+  uint8_t* sKc[2] = {wsm + 2 * kTile16, wsm + 2 * kTile16 + kTile8};
+  uint8_t* sVc[2] = {wsm + 3 * kTile16, wsm + 3 * kTile16 + kTile8};
+  float* sSc = reinterpret_cast<float*>(wsm + 4 * kTile16);   // [stage][k 16 | v 16]
+
+  // ---- query fragments (A operand of QK^T), resident for the whole CTA
+  uint32_t qa[kD / 16][4];
+  {
+    const size_t qrow0 = (static_cast<size_t>(r) * p.Hq + h0 + gq) * kD;
+    const size_t qrow1 = qrow0 + 8 * kD;
+    const bool ok0 = gq < nh, ok1 = gq + 8 < nh;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const int c = kk * 16 + 2 * tq;
+      qa[kk][0] = ok0 ? load_q2<Q_F16, QK_F16>(p.q, qrow0 + c) : 0u;
+      qa[kk][1] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c) : 0u;
+      qa[kk][2] = ok0 ? load_q2<Q_F16, QK_F16>(p.q, qrow0 + c + 8) : 0u;
+      qa[kk][3] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c + 8) : 0u;
+    }
+  }
+
+  const int32_t* idx_row = p.idx + static_cast<size_t>(r) * p.topk + split_begin;
+  const size_t kv_row_elems = static_cast<size_t>(p.Hkv) * kD;   // per cache token
+  const size_t kv_base = (static_cast<size_t>(b) * p.cap) * kv_row_elems + static_cast<size_t>(g) * kD;
+  const size_t sc_base = static_cast<size_t>(b) * p.cap * p.Hkv + g;
+
+  // gather the 16 selected rows of tile `it` (this warp's it-th tile) into stage st
+  auto issue_tile = [&](int it, int st) {
+    const int tile = warp + it * kAttnWarps;
+    const int o = tile * kTileKeys;
+    int key = -1;
+    if (lane < kTileKeys && o + lane < split_len) {
+      key = idx_row[o + lane];
+      if (key < 0 || key >= T) key = -1;
+    }
+    if constexpr (KV == KV_INT8) {
+      const int8_t* kb = static_cast<const int8_t*>(p.k);
+      const int8_t* vb = static_cast<const int8_t*>(p.v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = lane + 32 * i;            // 0..127: row j/8, chunk j%8
+        const int row = j >> 3, c = j & 7;
+        const int kr = __shfl_sync(0xffffffffu, key, row);
+        const size_t off = kv_base + static_cast<size_t>(kr < 0 ? 0 : kr) * kv_row_elems + c * 16;
+        cp_async16(sKc[st] + row * kD + c * 16, kb + off, kr >= 0);
+        cp_async16(sVc[st] + row * kD + c * 16, vb + off, kr >= 0);
+      }
+      const int kr = __shfl_sync(0xffffffffu, key, lane & 15);
+      const size_t so = sc_base + static_cast<size_t>(kr < 0 ? 0 : kr) * p.Hkv;
+      if (lane < 16) cp_async4(sSc + st * 32 + lane, p.k_scale + so, kr >= 0);
+      else cp_async4(sSc + st * 32 + lane, p.v_scale + so, kr >= 0);
+    } else {
+      const uint16_t* kb = static_cast<const uint16_t*>(p.k);
+      const uint16_t* vb = static_cast<const uint16_t*>(p.v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = lane + 32 * i;            // 0..255: row j/16, chunk j%16
+        const int row = j >> 4, c = j & 15;
+        const int kr = __shfl_sync(0xffffffffu, key, row);
+        const size_t off = kv_base + static_cast<size_t>(kr < 0 ? 0 : kr) * kv_row_elems + c * 8;
+        cp_async16(sK[st] + swz(row, c), kb + off, kr >= 0);
+        cp_async16(sV[st] + swz(row, c), vb + off, kr >= 0);
+      }
+    }
+  };
+
+  float o_acc[kD / 8][4];
+#pragma unroll
+  for (int i = 0; i < kD / 8; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.0f;
+  float m_run[2] = {-INFINITY, -INFINITY};   // rows gq, gq+8 (log2 units)
+  float l_run[2] = {0.0f, 0.0f};             // thread-partial sums
+
+  const int my_tiles = ntiles > warp ? (ntiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
+  if (my_tiles > 0) issue_tile(0, 0);
+  cp_async_commit();
+  for (int it = 0; it < my_tiles; ++it) {
+    const int st = it & 1;
+    if (it + 1 < my_tiles) issue_tile(it + 1, st ^ 1);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncwarp();
+    const int tile = warp + it * kAttnWarps;
+    const int nvalid = min(kTileKeys, split_len - tile * kTileKeys);
+
+    const uint8_t* tK = sK[st];
+    const uint8_t* tV = sV[st];
+    if constexpr (KV == KV_INT8) {
+      // codes -> exact 16-bit values in the swizzled layout ldmatrix expects
+      const int row = lane >> 1, half = lane & 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int c = half * 4 + i;             // 16-code chunk of the row
+        const uint4 kc = *reinterpret_cast<const uint4*>(sKc[st] + row * kD + c * 16);
+        const uint4 vc = *reinterpret_cast<const uint4*>(sVc[st] + row * kD + c * 16);
+        convert_codes16<QK_F16>(kc, sK[0], row, 2 * c);
+        convert_codes16<false>(vc, sK[1], row, 2 * c);
+      }
+      __syncwarp();
+      tK = sK[0];
+      tV = sK[1];
+    }
+
+    // ---- S = Q K^T : 16 heads x 16 keys
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3;
+      const int krow = ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        uint32_t bk[4];
+        ldmatrix_x4(bk, tK + swz(krow, 2 * kk + (mi & 1)));
+        mma_16816<QK_F16>(sc[0], qa[kk], bk);
+        mma_16816<QK_F16>(sc[1], qa[kk], bk + 2);
+      }
+    }
+
+    // ---- online softmax (log2 domain)
+    float kscale[2][2], vscale[2][2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kl = 8 * n + 2 * tq + e;
+        if constexpr (KV == KV_INT8) {
+          kscale[n][e] = sSc[st * 32 + kl];
+          vscale[n][e] = sSc[st * 32 + 16 + kl];
+        } else {
+          kscale[n][e] = 1.0f;
+          vscale[n][e] = 1.0f;
+        }
+      }
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kl = 8 * n + 2 * tq + (e & 1);
+        float v = sc[n][e] * kscale[n][e & 1] * p.scale_log2;
+        if (kl >= nvalid) v = -INFINITY;
+        sc[n][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+    float m_new[2], d_old[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+      m_new[i] = fmaxf(m_run[i], mx[i]);
+      d_old[i] = m_run[i] - m_new[i];   // <= 0; NaN/-inf when nothing was accumulated
+    }
+    float pt[2][4];
+    float tile_sum[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float dlt = sc[n][e] - m_new[e >> 1];
+        float pv = 0.0f, ptv = 0.0f;
+        if (sc[n][e] != -INFINITY) {
+          pv = exp2f(dlt);
+          if constexpr (KV == KV_INT8) ptv = mul_exp2(vscale[n][e & 1], dlt);
+          else ptv = pv;
+        }
+        tile_sum[e >> 1] += pv;
+        pt[n][e] = ptv;
+      }
+    // rescale the running state to the new max: l = l * 2^d_old + sum p
+    float alpha[2];
+    bool fast[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      fast[i] = d_old[i] >= -125.0f;
+      alpha[i] = fast[i] ? exp2f(d_old[i]) : 0.0f;
+      l_run[i] = mul_exp2(l_run[i], d_old[i]) + tile_sum[i];
+      m_run[i] = m_new[i];
+    }
+#pragma unroll
+    for (int nd = 0; nd < kD / 8; ++nd)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        o_acc[nd][e] = fast[e >> 1] ? o_acc[nd][e] * alpha[e >> 1]
+                                    : mul_exp2(o_acc[nd][e], d_old[e >> 1]);
+
+    // ---- O += P V
+    uint32_t pa[4], pl[4];
+    if constexpr (PV_F16) {
+      pa[0] = pack_f16(pt[0][0], pt[0][1]);
+      pa[1] = pack_f16(pt[0][2], pt[0][3]);
+      pa[2] = pack_f16(pt[1][0], pt[1][1]);
+      pa[3] = pack_f16(pt[1][2], pt[1][3]);
+    } else {
+      float hi[2][4], lo[2][4];
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[n][e] = __bfloat162float(__float2bfloat16_rn(pt[n][e]));
+          lo[n][e] = pt[n][e] - hi[n][e];
+        }
+      pa[0] = pack_bf16(hi[0][0], hi[0][1]);
+      pa[1] = pack_bf16(hi[0][2], hi[0][3]);
+      pa[2] = pack_bf16(hi[1][0], hi[1][1]);
+      pa[3] = pack_bf16(hi[1][2], hi[1][3]);
+      pl[0] = pack_bf16(lo[0][0], lo[0][1]);
+      pl[1] = pack_bf16(lo[0][2], lo[0][3]);
+      pl[2] = pack_bf16(lo[1][0], lo[1][1]);
+      pl[3] = pack_bf16(lo[1][2], lo[1][3]);
+    }
+    {
+      const int mi = lane >> 3;
+      const int vrow = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+      for (int nd = 0; nd < kD / 8; nd += 2) {
+        uint32_t bv[4];
+        ldmatrix_x4_trans(bv, tV + swz(vrow, nd + (mi >> 1)));
+        mma_16816<PV_F16>(o_acc[nd], pa, bv);
+        mma_16816<PV_F16>(o_acc[nd + 1], pa, bv + 2);
+        if constexpr (PV_SPLIT) {
+          mma_16816<PV_F16>(o_acc[nd], pl, bv);
+          mma_16816<PV_F16>(o_acc[nd + 1], pl, bv + 2);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  // ---- merge the warps of this CTA
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 1);
+    l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
+  }
+  __syncthreads();   // stage buffers become the merge area
+  float* ws = reinterpret_cast<float*>(smem);      // [warps][kPartialFloats]
+  float* mine = ws + warp * kPartialFloats;
+  if (tq == 0) {
+    mine[gq] = m_run[0];
+    mine[gq + 8] = m_run[1];
+    mine[kAttnRows + gq] = l_run[0];
+    mine[kAttnRows + gq + 8] = l_run[1];
+  }
+#pragma unroll
+  for (int nd = 0; nd < kD / 8; ++nd)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int row = gq + 8 * (e >> 1), col = nd * 8 + 2 * tq + (e & 1);
+      mine[2 * kAttnRows + row * kD + col] = o_acc[nd][e];
+    }
+  __syncthreads();
+
+  const int d = threadIdx.x;   // one output column per thread
+  const bool single = (p.nsplit == 1);
+  float* part = p.partial + ((static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit + blockIdx.x) *
+                                kPartialFloats;
+  const size_t out_row = static_cast<size_t>(r) * p.Hq + h0;
+  for (int row = 0; row < kAttnRows; ++row) {
+    float M = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, ws[w * kPartialFloats + row]);
+    float L = 0.0f, O = 0.0f;
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float dm = ws[w * kPartialFloats + row] - M;
+      L += mul_exp2(ws[w * kPartialFloats + kAttnRows + row], dm);
+      O += mul_exp2(ws[w * kPartialFloats + 2 * kAttnRows + row * kD + d], dm);
+    }
+    if (single) {
+      if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + d, O / L);
+    } else {
+      if (d == 0) {
+        part[row] = M;
+        part[kAttnRows + row] = L;
+      }
+      part[2 * kAttnRows + row * kD + d] = O;
+    }
+  }
+  if (single) return;
+
+  // ---- split combine by the last CTA of this (row, head group)
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t prev = atomicAdd(&p.ticket[static_cast<size_t>(r) * gridDim.y + gh], 1u);
+    s_last = (prev == static_cast<uint32_t>(nreal - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* parts = p.partial + (static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit * kPartialFloats;
+  for (int row = 0; row < nh; ++row) {
+    float M = -INFINITY;
+    for (int j = 0; j < nreal; ++j) M = fmaxf(M, __ldcg(parts + j * kPartialFloats + row));
+    float L = 0.0f, O = 0.0f;
+    for (int j = 0; j < nreal; ++j) {
+      const float* pj = parts + static_cast<size_t>(j) * kPartialFloats;
+      const float dm = __ldcg(pj + row) - M;
+      L += mul_exp2(__ldcg(pj + kAttnRows + row), dm);
+      O += mul_exp2(__ldcg(pj + 2 * kAttnRows + row * kD + d), dm);
+    }
+    store_out<OUT>(p.out, (out_row + row) * kD + d, O / L);
+  }
+}
+
+template <int KV, bool Q_F16, int OUT>
+static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
+  auto kern = sparse_attn_kernel<KV, Q_F16, OUT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
+  kern<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
+  return cudaPeekAtLastError();
+}
+
+template <int KV, bool Q_F16>
+static cudaError_t launch_out(const AttnParams& p, int out_dtype, cudaStream_t stream) {
+  switch (out_dtype) {
+    case DSA_BF16: return launch_t<KV, Q_F16, DSA_BF16>(p, stream);
+    case DSA_FP16: return launch_t<KV, Q_F16, DSA_FP16>(p, stream);
+    case DSA_FP32: return launch_t<KV, Q_F16, DSA_FP32>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
+                             cudaStream_t stream) {
+  const bool qf16 = (q_dtype == DSA_FP16);
+  switch (kv_dtype) {
+    case DSA_BF16:
+      if (qf16) return cudaErrorInvalidValue;
+      return launch_out<KV_BF16, false>(p, out_dtype, stream);
+    case DSA_FP16:
+      return qf16 ? launch_out<KV_FP16, true>(p, out_dtype, stream)
+                  : launch_out<KV_FP16, false>(p, out_dtype, stream);
+    case DSA_INT8:
+      return qf16 ? launch_out<KV_INT8, true>(p, out_dtype, stream)
+                  : launch_out<KV_INT8, false>(p, out_dtype, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsa

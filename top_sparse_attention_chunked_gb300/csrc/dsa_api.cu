@@ -1,0 +1,620 @@
+// Host side of libdsa: argument validation, workspace layout, TMA descriptors
+// and kernel dispatch behind the C ABI declared in include/dsa.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+thread_local std::string g_err;
+thread_local int g_timing_kind = -1;
+thread_local cudaEvent_t g_ev[2] = {nullptr, nullptr};
+thread_local bool g_ev_recorded = false;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// ------------------------------------------------------------------ device
+struct DeviceInfo {
+  int sms = 0;
+  size_t smem_optin = 0;
+  int major = 0, minor = 0;
+};
+
+int device_info(DeviceInfo* info) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DSA_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return fail(DSA_ERR_NO_DEVICE, "device ordinal %d out of range", dev);
+  if (!have[dev]) {
+    DeviceInfo d;
+    int v = 0;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(shared memory)");
+    d.smem_optin = static_cast<size_t>(v);
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *info = cache[dev];
+  if (info->major != 10)
+    return fail(DSA_ERR_NO_DEVICE, "libdsa is built for sm_103a (Blackwell); device is sm_%d%d",
+                info->major, info->minor);
+  return DSA_OK;
+}
+
+// ------------------------------------------------------------------ TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// rows x 64 bf16 matrix, box of box_rows x 64, 128-byte swizzle
+int make_map_rows64(CUtensorMap* m, const void* base, long long rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(DSA_IDX_DIM), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(DSA_IDX_DIM) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(DSA_IDX_DIM), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DSA_OK;
+}
+
+// ------------------------------------------------------------------ problem checks
+struct Derived {
+  int rows = 0;        // B * S
+  int max_n = 0;       // longest visible row
+  int kmax = 0;        // largest k_eff
+  int G = 0, HG = 0;   // group size, head groups per KV head
+  int bm_words = 0;    // bitmap words per row
+};
+
+int check_problem(const dsa_problem* p, int op, Derived* d) {
+  if (!p) return fail(DSA_ERR_INVALID_ARG, "problem is NULL");
+  if (p->batch < 1 || p->batch > DSA_MAX_BATCH)
+    return fail(DSA_ERR_INVALID_ARG, "batch %d outside 1..%d", p->batch, DSA_MAX_BATCH);
+  if (p->q_len < 1) return fail(DSA_ERR_INVALID_ARG, "q_len %d < 1", p->q_len);
+  if (p->cache_capacity < 1 || p->cache_capacity > (1 << 30))
+    return fail(DSA_ERR_INVALID_ARG, "cache_capacity %d invalid", p->cache_capacity);
+  if (p->idx_heads != DSA_IDX_HEADS || p->idx_dim != DSA_IDX_DIM)
+    return fail(DSA_ERR_UNSUPPORTED, "index heads x dim must be %dx%d (got %dx%d)",
+                DSA_IDX_HEADS, DSA_IDX_DIM, p->idx_heads, p->idx_dim);
+  if (p->top_k < 1 || p->top_k > p->cache_capacity)
+    return fail(DSA_ERR_INVALID_ARG, "top_k %d outside 1..cache_capacity (%d)", p->top_k,
+                p->cache_capacity);
+  d->rows = p->batch * p->q_len;
+  d->max_n = 0;
+  for (int b = 0; b < p->batch; ++b) {
+    const int T = p->total_len[b];
+    if (T < p->q_len || T > p->cache_capacity)
+      return fail(DSA_ERR_INVALID_ARG,
+                  "total_len[%d] = %d outside q_len..cache_capacity (%d..%d)", b, T, p->q_len,
+                  p->cache_capacity);
+    if (T > d->max_n) d->max_n = T;
+  }
+  if (d->max_n > DSA_MAX_CONTEXT)
+    return fail(DSA_ERR_UNSUPPORTED, "visible length %d above %d", d->max_n, DSA_MAX_CONTEXT);
+  d->kmax = p->top_k < d->max_n ? p->top_k : d->max_n;
+  d->bm_words = ceil_div(p->cache_capacity, 32);
+  if (op == DSA_OP_DECODE || op == DSA_OP_PREFILL) {
+    if (p->head_dim != DSA_HEAD_DIM)
+      return fail(DSA_ERR_UNSUPPORTED, "head_dim must be %d (got %d)", DSA_HEAD_DIM, p->head_dim);
+    if (p->num_q_heads < 1 || p->num_kv_heads < 1 || p->num_q_heads % p->num_kv_heads != 0)
+      return fail(DSA_ERR_INVALID_ARG, "num_q_heads %d must be a multiple of num_kv_heads %d",
+                  p->num_q_heads, p->num_kv_heads);
+    if (p->q_dtype != DSA_BF16 && p->q_dtype != DSA_FP16)
+      return fail(DSA_ERR_UNSUPPORTED, "q_dtype must be BF16 or FP16");
+    if (p->kv_dtype != DSA_BF16 && p->kv_dtype != DSA_FP16 && p->kv_dtype != DSA_INT8)
+      return fail(DSA_ERR_UNSUPPORTED, "kv_dtype must be BF16, FP16 or INT8");
+    if (p->q_dtype == DSA_FP16 && p->kv_dtype == DSA_BF16)
+      return fail(DSA_ERR_UNSUPPORTED, "FP16 query with a BF16 cache is not built");
+    if (p->out_dtype != DSA_BF16 && p->out_dtype != DSA_FP16 && p->out_dtype != DSA_FP32)
+      return fail(DSA_ERR_UNSUPPORTED, "out_dtype must be BF16, FP16 or FP32");
+    if (p->attn_split_keys < 0 || p->attn_split_keys % 16 != 0)
+      return fail(DSA_ERR_INVALID_ARG, "attn_split_keys %d must be 0 or a multiple of 16",
+                  p->attn_split_keys);
+    if (!(p->softmax_scale >= 0.0f) || std::isinf(p->softmax_scale))
+      return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    d->G = p->num_q_heads / p->num_kv_heads;
+    d->HG = ceil_div(d->G, kAttnRows);
+  }
+  if (op == DSA_OP_DECODE && p->q_len > DSA_MAX_DECODE_Q_LEN)
+    return fail(DSA_ERR_UNSUPPORTED, "decode takes at most %d query tokens per sequence (got %d)",
+                DSA_MAX_DECODE_Q_LEN, p->q_len);
+  return DSA_OK;
+}
+
+// Upper bound of the automatic split count (any GPU with <= 256 SMs).
+int splits_bound(const dsa_problem* p, const Derived& d) {
+  if (p->attn_split_keys > 0) return ceil_div(d.kmax, p->attn_split_keys);
+  const int units = d.rows * p->num_kv_heads * d.HG;
+  int s = ceil_div(2 * 256, units);
+  s = s < 16 ? s : 16;
+  const int cap = ceil_div(d.kmax, 64);
+  s = s < cap ? s : cap;
+  return s < 1 ? 1 : s;
+}
+
+// Actual split of the selected keys for the attention kernel.
+void choose_split(const dsa_problem* p, const Derived& d, int sms, int* split_keys, int* nsplit) {
+  int sk;
+  if (p->attn_split_keys > 0) {
+    sk = p->attn_split_keys;
+  } else {
+    const int units = d.rows * p->num_kv_heads * d.HG;
+    int s = ceil_div(2 * sms, units);
+    s = s < 16 ? s : 16;
+    const int cap = ceil_div(d.kmax, 64);
+    s = s < cap ? s : cap;
+    if (s < 1) s = 1;
+    sk = ceil_div(ceil_div(d.kmax, s), 16) * 16;
+  }
+  *split_keys = sk;
+  *nsplit = ceil_div(d.kmax, sk);
+}
+
+// ------------------------------------------------------------------ workspace
+constexpr int kPrefillTopkGroup = 128;   // rows per chunked top-k round in prefill
+
+struct Layout {
+  size_t status = 0;
+  size_t zero_begin = 0, zero_end = 0;
+  size_t hist = 0, topk_ticket = 0, cand_count = 0, topk_zero_end = 0, attn_ticket = 0;
+  size_t scores = 0, cands = 0, bitmap = 0, idx = 0, partial = 0;
+  long long cand_stride = 0;
+  int topk_rows = 0;   // rows the top-k scratch covers
+  size_t total = 0;
+};
+
+Layout layout(const dsa_problem* p, int op, const Derived& d) {
+  Layout L;
+  size_t o = 256;   // status word
+  const bool attn = (op == DSA_OP_DECODE || op == DSA_OP_PREFILL);
+  const bool topk = (op != DSA_OP_INDEX_SCORES);
+  L.topk_rows = (op == DSA_OP_PREFILL && d.rows > kPrefillTopkGroup) ? kPrefillTopkGroup : d.rows;
+  const int units = attn ? d.rows * p->num_kv_heads * d.HG : 0;
+  L.zero_begin = o;
+  if (topk) {
+    L.hist = o;        o = up256(o + static_cast<size_t>(L.topk_rows) * kHistBins * 4);
+    L.topk_ticket = o; o = up256(o + static_cast<size_t>(L.topk_rows) * 4);
+    L.cand_count = o;  o = up256(o + static_cast<size_t>(L.topk_rows) * 4);
+    L.topk_zero_end = o;
+  }
+  if (attn) {
+    L.attn_ticket = o; o = up256(o + static_cast<size_t>(units) * 4);
+  }
+  L.zero_end = o;
+  if (attn) {
+    L.scores = o; o = up256(o + static_cast<size_t>(d.rows) * p->cache_capacity * 4);
+  }
+  if (topk) {
+    L.cand_stride = d.max_n;
+    L.cands = o;  o = up256(o + static_cast<size_t>(L.topk_rows) * d.max_n * 8);
+    L.bitmap = o; o = up256(o + static_cast<size_t>(L.topk_rows) * d.bm_words * 4);
+  }
+  if (attn) {
+    L.idx = o;     o = up256(o + static_cast<size_t>(d.rows) * p->top_k * 4);
+    const int ns = splits_bound(p, d);
+    if (ns > 1) {
+      L.partial = o;
+      o = up256(o + static_cast<size_t>(units) * ns * kPartialFloats * 4);
+    }
+  }
+  L.total = o;
+  return L;
+}
+
+int check_ws(void* ws, size_t bytes, const Layout& L) {
+  if (!ws) return fail(DSA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(ws, 256)) return fail(DSA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (bytes < L.total)
+    return fail(DSA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", bytes, L.total);
+  return DSA_OK;
+}
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+SeqLens lens_of(const dsa_problem* p) {
+  SeqLens s;
+  memset(&s, 0, sizeof(s));
+  for (int b = 0; b < p->batch; ++b) s.T[b] = p->total_len[b];
+  return s;
+}
+
+int pow2_at_least(int x) {
+  int v = 1;
+  while (v < x) v <<= 1;
+  return v;
+}
+
+// ------------------------------------------------------------------ stages
+int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const void* qI,
+                const float* w, const void* kI, float* scores, uint32_t* hist, uint32_t* status,
+                cudaStream_t st) {
+  IndexerParams ip;
+  ip.w = w;
+  ip.scores = scores;
+  ip.hist = hist;
+  ip.status = status;
+  ip.B = p->batch;
+  ip.S = p->q_len;
+  ip.cap = p->cache_capacity;
+  ip.QB = p->q_len <= 16 ? pow2_at_least(p->q_len) : 16;
+  ip.nqb = ceil_div(p->q_len, ip.QB);
+  ip.lens = lens_of(p);
+  long long total = 0;
+  long long per_seq_max = 0;
+  for (int b = 0; b < p->batch; ++b) {
+    long long nb = 0;
+    for (int qb = 0; qb < ip.nqb; ++qb) {
+      const int last_s = std::min(p->q_len, (qb + 1) * ip.QB) - 1;
+      const int n = p->total_len[b] - p->q_len + last_s + 1;
+      nb += ceil_div(n, kKeyTile);
+    }
+    total += nb;
+    if (nb > per_seq_max) per_seq_max = nb;
+  }
+  ip.total_units = total;
+  CUtensorMap tm_kI, tm_qI;
+  int rc = make_map_rows64(&tm_kI, kI, static_cast<long long>(p->batch) * p->cache_capacity, kKeyTile);
+  if (rc) return rc;
+  rc = make_map_rows64(&tm_qI, qI, static_cast<long long>(d.rows) * DSA_IDX_HEADS, ip.QB * 16);
+  if (rc) return rc;
+  int stages = 0;
+  const size_t smem = indexer_smem_bytes(ip.QB, hist != nullptr, &stages, di.smem_optin);
+  if (smem > di.smem_optin) return fail(DSA_ERR_UNSUPPORTED, "indexer needs %zu B of shared memory", smem);
+  dim3 grid;
+  if (hist) {
+    // CTAs per sequence, so each CTA's histograms belong to one sequence
+    long long per = ceil_div(di.sms, p->batch);
+    if (per > per_seq_max) per = per_seq_max;
+    if (per < 1) per = 1;
+    grid = dim3(static_cast<unsigned>(per), static_cast<unsigned>(p->batch));
+    if (p->batch == 1) grid.y = 1;   // one sequence: the flat split is the same
+  } else {
+    grid = dim3(static_cast<unsigned>(total < di.sms ? total : di.sms));
+  }
+  timing_before(DSA_KERNEL_INDEXER, st);
+  cudaError_t e = launch_indexer(ip, tm_kI, tm_qI, grid, smem, stages, st);
+  timing_after(DSA_KERNEL_INDEXER, st);
+  if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+  return DSA_OK;
+}
+
+int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
+             const float* scores, int32_t* idx, void* ws, bool hist_ready, bool prefer_rows,
+             cudaStream_t st) {
+  TopkParams tp;
+  tp.scores = scores;
+  tp.idx = idx;
+  tp.hist = at<uint32_t>(ws, L.hist);
+  tp.ticket = at<uint32_t>(ws, L.topk_ticket);
+  tp.cand_count = at<uint32_t>(ws, L.cand_count);
+  tp.cands = at<unsigned long long>(ws, L.cands);
+  tp.bitmap = at<uint32_t>(ws, L.bitmap);
+  tp.cand_stride = L.cand_stride;
+  tp.bitmap_stride = d.bm_words;
+  tp.B = p->batch;
+  tp.S = p->q_len;
+  tp.cap = p->cache_capacity;
+  tp.k = p->top_k;
+  tp.nchunks = ceil_div(d.max_n, kChunk);
+  tp.lens = lens_of(p);
+  tp.row0 = 0;
+  tp.nrows = d.rows;
+  cudaError_t e;
+  const int row_max = topk_row_max_len(di.smem_optin);
+  if (!hist_ready && prefer_rows && d.max_n <= row_max) {
+    timing_before(DSA_KERNEL_TOPK_ROW, st);
+    e = launch_topk_row(tp, d.max_n, di.smem_optin, st);
+    timing_after(DSA_KERNEL_TOPK_ROW, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k row launch");
+    return DSA_OK;
+  }
+  // chunked path, in rounds of at most L.topk_rows rows
+  for (int r0 = 0; r0 < d.rows; r0 += L.topk_rows) {
+    tp.row0 = r0;
+    tp.nrows = std::min(L.topk_rows, d.rows - r0);
+    if (!hist_ready) {
+      e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.hist, 0, L.topk_zero_end - L.hist, st);
+      if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+      timing_before(DSA_KERNEL_TOPK_HIST, st);
+      e = launch_topk_hist(tp, st);
+      timing_after(DSA_KERNEL_TOPK_HIST, st);
+      if (e != cudaSuccess) return cuda_fail(e, "top-k histogram launch");
+    }
+    timing_before(DSA_KERNEL_TOPK_SELECT, st);
+    e = launch_topk_chunk_select(tp, st);
+    timing_after(DSA_KERNEL_TOPK_SELECT, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k select launch");
+  }
+  return DSA_OK;
+}
+
+int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
+                  const void* q, const void* k, const void* v, const float* ks, const float* vs,
+                  const int32_t* idx, void* out, void* ws, cudaStream_t st) {
+  AttnParams ap;
+  ap.q = q;
+  ap.k = k;
+  ap.v = v;
+  ap.k_scale = ks;
+  ap.v_scale = vs;
+  ap.idx = idx;
+  ap.out = out;
+  ap.partial = L.partial ? at<float>(ws, L.partial) : nullptr;
+  ap.ticket = at<uint32_t>(ws, L.attn_ticket);
+  ap.B = p->batch;
+  ap.S = p->q_len;
+  ap.Hq = p->num_q_heads;
+  ap.Hkv = p->num_kv_heads;
+  ap.G = d.G;
+  ap.HG = d.HG;
+  ap.cap = p->cache_capacity;
+  ap.topk = p->top_k;
+  choose_split(p, d, di.sms, &ap.split_keys, &ap.nsplit);
+  if (ap.nsplit > splits_bound(p, d))
+    return fail(DSA_ERR_UNSUPPORTED, "device has more SMs than the workspace bound assumes");
+  const float scale = p->softmax_scale > 0.0f ? p->softmax_scale
+                                              : 1.0f / std::sqrt(static_cast<float>(p->head_dim));
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.lens = lens_of(p);
+  timing_before(DSA_KERNEL_ATTENTION, st);
+  cudaError_t e = launch_attention(ap, p->q_dtype, p->kv_dtype, p->out_dtype, st);
+  timing_after(DSA_KERNEL_ATTENTION, st);
+  if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+  return DSA_OK;
+}
+
+int check_attn_ptrs(const dsa_problem* p, const void* q, const void* qI, const float* w,
+                    const void* kI, const void* k, const void* v, const float* ks,
+                    const float* vs, const int32_t* idx_out, const void* out) {
+  if (!q || !qI || !w || !kI || !k || !v || !out)
+    return fail(DSA_ERR_INVALID_ARG, "a required tensor pointer is NULL");
+  if (p->kv_dtype == DSA_INT8) {
+    if (!ks || !vs) return fail(DSA_ERR_INVALID_ARG, "INT8 cache needs k_scale and v_scale");
+    if (!aligned(ks, 4) || !aligned(vs, 4)) return fail(DSA_ERR_MISALIGNED, "scales must be 4-byte aligned");
+  } else if (ks || vs) {
+    return fail(DSA_ERR_INVALID_ARG, "k_scale/v_scale must be NULL unless the cache is INT8");
+  }
+  if (!aligned(q, 16) || !aligned(qI, 16) || !aligned(kI, 16) || !aligned(k, 16) ||
+      !aligned(v, 16))
+    return fail(DSA_ERR_MISALIGNED, "q, qI, kI, k and v must be 16-byte aligned");
+  if (!aligned(w, 4) || !aligned(out, 4) || (idx_out && !aligned(idx_out, 4)))
+    return fail(DSA_ERR_MISALIGNED, "w, out and idx_out must be 4-byte aligned");
+  return DSA_OK;
+}
+
+int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const float* w,
+              const void* kI, const void* k, const void* v, const float* ks, const float* vs,
+              int32_t* idx_out, void* out, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  int rc = check_problem(p, op, &d);
+  if (rc) return rc;
+  rc = check_attn_ptrs(p, q, qI, w, kI, k, v, ks, vs, idx_out, out);
+  if (rc) return rc;
+  const Layout L = layout(p, op, d);
+  rc = check_ws(ws, ws_bytes, L);
+  if (rc) return rc;
+  DeviceInfo di;
+  rc = device_info(&di);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.zero_begin - 256, 0,
+                                  L.zero_end - L.zero_begin + 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  float* scores = at<float>(ws, L.scores);
+  int32_t* idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
+  uint32_t* status = at<uint32_t>(ws, 0);
+  const bool decode = (op == DSA_OP_DECODE);
+  rc = run_indexer(p, d, di, qI, w, kI, scores, decode ? at<uint32_t>(ws, L.hist) : nullptr, status, st);
+  if (rc) return rc;
+  rc = run_topk(p, d, di, L, scores, idx, ws, decode, !decode, st);
+  if (rc) return rc;
+  return run_attention(p, d, di, L, q, k, v, ks, vs, idx, out, ws, st);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ timing hook
+void timing_before(int kind, cudaStream_t st) {
+  if (kind != g_timing_kind) return;
+  if (!g_ev[0]) {
+    cudaEventCreate(&g_ev[0]);
+    cudaEventCreate(&g_ev[1]);
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_ev[0], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_ev[0], st);
+}
+
+void timing_after(int kind, cudaStream_t st) {
+  if (kind != g_timing_kind || !g_ev[1]) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_ev[1], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_ev[1], st);
+  g_ev_recorded = true;
+}
+
+}  // namespace dsa
+
+// ====================================================================== C ABI
+using namespace dsa;
+
+extern "C" {
+
+size_t dsa_workspace_size(const dsa_problem* p, int op) {
+  if (op < DSA_OP_INDEX_SCORES || op > DSA_OP_PREFILL) {
+    fail(DSA_ERR_INVALID_ARG, "unknown op %d", op);
+    return 0;
+  }
+  Derived d;
+  if (check_problem(p, op, &d)) return 0;
+  return layout(p, op, d).total;
+}
+
+int dsa_index_scores(const dsa_problem* p, const void* qI, const float* w, const void* kI,
+                     float* scores, void* ws, size_t ws_bytes, void* stream) {
+  Derived d;
+  int rc = check_problem(p, DSA_OP_INDEX_SCORES, &d);
+  if (rc) return rc;
+  if (!qI || !w || !kI || !scores) return fail(DSA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned(qI, 16) || !aligned(kI, 16) || !aligned(scores, 16) || !aligned(w, 4))
+    return fail(DSA_ERR_MISALIGNED, "qI, kI and scores must be 16-byte aligned, w 4-byte");
+  const Layout L = layout(p, DSA_OP_INDEX_SCORES, d);
+  rc = check_ws(ws, ws_bytes, L);
+  if (rc) return rc;
+  DeviceInfo di;
+  rc = device_info(&di);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  return run_indexer(p, d, di, qI, w, kI, scores, nullptr, at<uint32_t>(ws, 0), st);
+}
+
+int dsa_topk(const dsa_problem* p, const float* scores, int32_t* idx, void* ws, size_t ws_bytes,
+             void* stream) {
+  Derived d;
+  int rc = check_problem(p, DSA_OP_TOPK, &d);
+  if (rc) return rc;
+  if (!scores || !idx) return fail(DSA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned(scores, 4) || !aligned(idx, 4))
+    return fail(DSA_ERR_MISALIGNED, "scores and idx must be 4-byte aligned");
+  const Layout L = layout(p, DSA_OP_TOPK, d);
+  rc = check_ws(ws, ws_bytes, L);
+  if (rc) return rc;
+  DeviceInfo di;
+  rc = device_info(&di);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  // few rows: spread each row over its chunks; many short rows: one CTA per row
+  const bool prefer_rows = d.rows >= 2 * di.sms;
+  return run_topk(p, d, di, L, scores, idx, ws, false, prefer_rows, st);
+}
+
+int dsa_sparse_attn_decode(const dsa_problem* p, const void* q, const void* qI, const float* w,
+                           const void* kI, const void* k, const void* v, const float* k_scale,
+                           const float* v_scale, int32_t* idx_out, void* out, void* ws,
+                           size_t ws_bytes, void* stream) {
+  return attn_call(p, DSA_OP_DECODE, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
+                   ws_bytes, stream);
+}
+
+int dsa_sparse_attn_prefill(const dsa_problem* p, const void* q, const void* qI, const float* w,
+                            const void* kI, const void* k, const void* v, const float* k_scale,
+                            const float* v_scale, int32_t* idx_out, void* out, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return attn_call(p, DSA_OP_PREFILL, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
+                   ws_bytes, stream);
+}
+
+int dsa_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* status_out) {
+  if (!ws || ws_bytes < 256 || !status_out)
+    return fail(DSA_ERR_INVALID_ARG, "workspace or status_out invalid");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *status_out = v;
+  if (v & kDevTimeout) return fail(DSA_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+  return DSA_OK;
+}
+
+const char* dsa_last_error_string(void) { return g_err.c_str(); }
+
+const char* dsa_status_string(int s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_NO_DEVICE: return "DSA_ERR_NO_DEVICE";
+    default: return "unknown status";
+  }
+}
+
+int dsa_version(void) { return 100; }
+
+int dsa_timing_select(int kind) {
+  if (kind < -1 || kind > DSA_KERNEL_ATTENTION) return fail(DSA_ERR_INVALID_ARG, "unknown kernel kind %d", kind);
+  g_timing_kind = kind;
+  g_ev_recorded = false;
+  return DSA_OK;
+}
+
+int dsa_timing_read(float* ms) {
+  if (!ms) return fail(DSA_ERR_INVALID_ARG, "ms is NULL");
+  if (!g_ev_recorded || !g_ev[1]) return fail(DSA_ERR_INVALID_ARG, "no timed launch recorded");
+  cudaError_t e = cudaEventSynchronize(g_ev[1]);
+  if (e != cudaSuccess) return cuda_fail(e, "event synchronize");
+  e = cudaEventElapsedTime(ms, g_ev[0], g_ev[1]);
+  if (e != cudaSuccess) return cuda_fail(e, "event elapsed time");
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Internal parameter blocks and launcher entry points shared by the library's
+// translation units (host API <-> kernels). Not part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kChunk = DSA_CHUNK;          // 2,048-key chunks (indexer + top-k)
+constexpr int kHistBits = 11;              // first radix digit: top 11 key bits
+constexpr int kHistBins = 1 << kHistBits;  // 2,048 bins per query row
+constexpr int kKeyTile = 128;              // keys per tcgen05 indexer tile (M)
+constexpr uint32_t kDevTimeout = 1u;       // status bit: a bounded wait ran out
+
+struct SeqLens {
+  int32_t T[DSA_MAX_BATCH];
+};
+
+// ---------------------------------------------------------------- indexer
+struct IndexerParams {
+  const float* w;        // [B, S, 16]
+  float* scores;         // [B, S, cap]
+  uint32_t* hist;        // [B*S, 2048] radix histograms (decode) or nullptr
+  uint32_t* status;      // device status word
+  int B, S, cap;
+  int QB;                // query tokens per block (N = 16 * QB)
+  int nqb;               // query blocks per sequence, ceil(S / QB)
+  long long total_units; // (sequence, query block, key tile) triples
+  SeqLens lens;
+};
+
+// Kernel kinds for the timing hook (mirror DSA_KERNEL_*).
+void timing_before(int kind, cudaStream_t stream);
+void timing_after(int kind, cudaStream_t stream);
+
+// grid.y > 1 gives each sequence its own CTAs (required with histograms).
+cudaError_t launch_indexer(const IndexerParams& p, const CUtensorMap& tm_kI,
+                           const CUtensorMap& tm_qI, dim3 grid, size_t smem_bytes,
+                           int stages, cudaStream_t stream);
+size_t indexer_smem_bytes(int QB, bool with_hist, int* stages_out, size_t smem_limit);
+
+// ---------------------------------------------------------------- top-k
+struct TopkParams {
+  const float* scores;          // [B*S, cap]
+  int32_t* idx;                 // [B*S, k]
+  uint32_t* hist;               // [B*S, 2048]     zeroed before the first kernel
+  uint32_t* ticket;             // [B*S]           zeroed
+  uint32_t* cand_count;         // [B*S]           zeroed
+  unsigned long long* cands;    // [B*S, cand_stride] candidate composites
+  uint32_t* bitmap;             // [B*S, bitmap_stride] selection bits
+  long long cand_stride;
+  int bitmap_stride;            // words per row
+  int B, S, cap, k;
+  int nchunks;                  // chunks of the longest row
+  int row0, nrows;              // rows handled by this launch (workspace rows are local)
+  SeqLens lens;
+};
+
+cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream);
+cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit,
+                            cudaStream_t stream);
+// Longest row the shared-memory whole-row select handles.
+int topk_row_max_len(size_t smem_limit);
+
+// ---------------------------------------------------------------- attention
+struct AttnParams {
+  const void* q;           // [B, S, Hq, 128]
+  const void* k;           // [B, cap, Hkv, 128]
+  const void* v;
+  const float* k_scale;    // [B, cap, Hkv] (INT8 only)
+  const float* v_scale;
+  const int32_t* idx;      // [B*S, topk]
+  void* out;               // [B, S, Hq, 128]
+  float* partial;          // split-K partial states
+  uint32_t* ticket;        // [B*S*Hkv*HG] zeroed when nsplit > 1
+  int B, S, Hq, Hkv, G, HG, cap, topk;
+  int split_keys, nsplit;
+  float scale_log2;        // softmax_scale * log2(e)
+  SeqLens lens;
+};
+
+constexpr int kAttnRows = 16;                                   // heads per MMA tile
+constexpr int kPartialFloats = 2 * kAttnRows + kAttnRows * DSA_HEAD_DIM;  // m, l, o
+
+cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
+                             cudaStream_t stream);
+
+}  // namespace dsa

@@ -1,0 +1,388 @@
+// Indexer on tcgen05 tensor cores.
+//
+//   score[b,s,t] = sum_h w[b,s,h] * max(0, qI[b,s,h,:] . kI[b,t,:])
+//
+// (PR #33802 "... DSA, Indexer, HC, and QMoE kernels for SM12x and 256K
+// context", Summary item 2: every cached index key is scored against each
+// query token's 16 index heads; the pages' SM12x kernel tiles 8 query tokens
+// per CTA and reduces the 16 heads with a shuffle butterfly.)
+//
+// GB300 design. The contraction is laid out "keys as M": one 128-key tile of
+// kI (128 rows x 64 bf16 = 16 KB, streamed from HBM by TMA) is the A operand,
+// the query block's index queries (QB tokens x 16 heads = N rows x 64) are the
+// B operand, and tcgen05.mma accumulates D[128 keys x N] in fp32 tensor
+// memory. After tcgen05.ld every epilogue thread owns one key and holds all
+// 16 head dot-products of a query in registers, so the ReLU, the head weights
+// and the head sum are plain per-thread FMAs -- no shuffles, no shared-memory
+// reduction. The same kernel serves decode (QB = S, all queries of a sequence
+// in one block, the radix histograms of the top-k fused into the epilogue)
+// and prefill (QB = 16, N = 256, causal: tile ranges stop at each block's
+// last visible key).
+//
+// Warp roles (192 threads): warp 0 issues TMA loads into a ring of shared
+// stages, warp 1 owns tensor memory and issues the MMAs, warps 2-5 are the
+// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31). Accumulators are
+// double-buffered in TMEM so the MMA of tile i+1 overlaps the epilogue of
+// tile i. Work is a flat list of (sequence, query block, key tile) units split
+// evenly over a persistent grid of one CTA per SM.
+#include <cstdio>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dsa {
+
+constexpr int kIdxThreads = 192;
+constexpr int kIdxMaxStages = 8;
+constexpr uint32_t kATileBytes = kKeyTile * DSA_IDX_DIM * 2;   // 16 KB
+
+struct UnitCursor {
+  int b, qb, kt, ntiles;
+};
+
+__device__ __forceinline__ int block_tiles(const IndexerParams& p, int b, int qb) {
+  const int last_s = min(p.S, (qb + 1) * p.QB) - 1;
+  const int n = visible_len(p.lens.T[b], p.S, last_s);
+  return (n + kKeyTile - 1) / kKeyTile;
+}
+
+__device__ __forceinline__ UnitCursor locate_unit(const IndexerParams& p, long long u) {
+  UnitCursor c{p.B, 0, 0, 0};
+  for (int b = 0; b < p.B; ++b)
+    for (int qb = 0; qb < p.nqb; ++qb) {
+      const int nt = block_tiles(p, b, qb);
+      if (u < nt) {
+        c.b = b; c.qb = qb; c.kt = static_cast<int>(u); c.ntiles = nt;
+        return c;
+      }
+      u -= nt;
+    }
+  return c;
+}
+
+__device__ __forceinline__ void advance_unit(const IndexerParams& p, UnitCursor& c) {
+  if (++c.kt < c.ntiles) return;
+  c.kt = 0;
+  do {
+    if (++c.qb >= p.nqb) { c.qb = 0; ++c.b; }
+    if (c.b >= p.B) return;
+    c.ntiles = block_tiles(p, c.b, c.qb);
+  } while (c.ntiles == 0);
+}
+
+// Bounded wait used on the unwinding path: ignores the abort flag.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitBudgetCycles) return;
+  }
+}
+
+template <int N>
+struct IdxCfg {
+  static constexpr int QB = N / 16;
+  static constexpr uint32_t kBBytes = N * DSA_IDX_DIM * 2;
+  static constexpr uint32_t kTmemCols = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128
+                                      : (2 * N <= 256) ? 256 : 512;
+  // queries whose accumulator columns are read per tcgen05.ld batch
+  static constexpr int QG = QB < 4 ? QB : 4;
+};
+
+struct IdxBarriers {
+  uint64_t full[kIdxMaxStages];
+  uint64_t empty[kIdxMaxStages];
+  uint64_t bfull[2], bempty[2];
+  uint64_t accfull[2], accempty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__host__ __device__ inline size_t indexer_smem_layout(int N, bool with_hist, int stages,
+                                                     size_t* off_b, size_t* off_w,
+                                                     size_t* off_hist, size_t* off_bar) {
+  const int QB = N / 16;
+  size_t o = static_cast<size_t>(stages) * kATileBytes;
+  *off_b = o;
+  o += 2ull * N * DSA_IDX_DIM * 2;
+  *off_w = o;   // one copy of the block's head weights per epilogue warp
+  o += 4ull * QB * 16 * sizeof(float);
+  o = (o + 15) & ~size_t(15);
+  *off_hist = o;
+  if (with_hist) o += static_cast<size_t>(QB) * kHistBins * sizeof(uint32_t);
+  o = (o + 15) & ~size_t(15);
+  *off_bar = o;
+  o += sizeof(IdxBarriers);
+  return o + 1024;   // slack to align the dynamic base to 1024 bytes
+}
+
+template <int N, bool HIST>
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_kI,
+                      const __grid_constant__ CUtensorMap tm_qI, const IndexerParams p,
+                      int stages) {
+  using C = IdxCfg<N>;
+  constexpr int QB = C::QB;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  size_t off_b, off_w, off_hist, off_bar;
+  indexer_smem_layout(N, HIST, stages, &off_b, &off_w, &off_hist, &off_bar);
+  uint8_t* sA = base;
+  uint8_t* sB = base + off_b;
+  float* sW = reinterpret_cast<float*>(base + off_w);
+  uint32_t* sHist = reinterpret_cast<uint32_t*>(base + off_hist);
+  IdxBarriers* bars = reinterpret_cast<IdxBarriers*>(base + off_bar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Unit range of this CTA. A 2-D grid (decode) gives every sequence its own
+  // CTAs (gridDim.y == B, one query block per sequence), so a CTA never
+  // changes query block and its histograms are flushed once at the end.
+  long long u0, u1;
+  if (gridDim.y > 1) {
+    long long start = 0;
+    for (int b = 0; b < static_cast<int>(blockIdx.y); ++b)
+      for (int qb = 0; qb < p.nqb; ++qb) start += block_tiles(p, b, qb);
+    long long nb = 0;
+    for (int qb = 0; qb < p.nqb; ++qb) nb += block_tiles(p, blockIdx.y, qb);
+    u0 = start + nb * blockIdx.x / gridDim.x;
+    u1 = start + nb * (blockIdx.x + 1) / gridDim.x;
+  } else {
+    u0 = p.total_units * blockIdx.x / gridDim.x;
+    u1 = p.total_units * (blockIdx.x + 1) / gridDim.x;
+  }
+  const long long count = u1 - u0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->bfull[i], 1);
+      mbar_init(&bars->bempty[i], 1);
+      mbar_init(&bars->accfull[i], 1);
+      mbar_init(&bars->accempty[i], 4);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_base, C::kTmemCols);
+  if constexpr (HIST) {
+    for (int i = threadIdx.x; i < QB * kHistBins; i += kIdxThreads) sHist[i] = 0u;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && count > 0) {
+      tma_prefetch_desc(&tm_kI);
+      tma_prefetch_desc(&tm_qI);
+      UnitCursor c = locate_unit(p, u0);
+      int pb = -1, pqb = -1, nblk = 0;
+      long long issued = 0;
+      for (long long i = 0; i < count; ++i) {
+        if (c.b != pb || c.qb != pqb) {
+          const int bi = nblk & 1;
+          if (nblk >= 2 && !mbar_wait_bounded(&bars->bempty[bi], ((nblk >> 1) - 1) & 1, abort_flag))
+            break;
+          mbar_arrive_expect_tx(&bars->bfull[bi], C::kBBytes);
+          tma_load_2d(sB + bi * C::kBBytes, &tm_qI, &bars->bfull[bi], 0,
+                      (c.b * p.S + c.qb * QB) * DSA_IDX_HEADS);
+          ++nblk;
+          pb = c.b;
+          pqb = c.qb;
+        }
+        const int s = static_cast<int>(i % stages);
+        const long long r = i / stages;
+        if (i >= stages && !mbar_wait_bounded(&bars->empty[s], static_cast<uint32_t>((r - 1) & 1), abort_flag))
+          break;
+        mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
+        tma_load_2d(sA + s * kATileBytes, &tm_kI, &bars->full[s], 0,
+                    c.b * p.cap + c.kt * kKeyTile);
+        ++issued;
+        advance_unit(p, c);
+      }
+      if (*abort_flag) {
+        // let the copies still in flight land before the CTA can exit
+        const long long first = issued > stages ? issued - stages : 0;
+        for (long long i = first; i < issued; ++i)
+          mbar_drain(&bars->full[i % stages], static_cast<uint32_t>((i / stages) & 1));
+        for (int k = 0; k < nblk && k < 2; ++k) {
+          const int blk = nblk - 1 - k;
+          mbar_drain(&bars->bfull[blk & 1], (blk >> 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && count > 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kKeyTile, N);
+      UnitCursor c = locate_unit(p, u0);
+      int pb = -1, pqb = -1, nblk = 0, bi = 0;
+      for (long long i = 0; i < count; ++i) {
+        if (c.b != pb || c.qb != pqb) {
+          if (nblk > 0) tc_commit(&bars->bempty[bi]);
+          bi = nblk & 1;
+          if (!mbar_wait_bounded(&bars->bfull[bi], (nblk >> 1) & 1, abort_flag)) break;
+          ++nblk;
+          pb = c.b;
+          pqb = c.qb;
+        }
+        const int s = static_cast<int>(i % stages);
+        if (!mbar_wait_bounded(&bars->full[s], static_cast<uint32_t>((i / stages) & 1), abort_flag))
+          break;
+        const int a = static_cast<int>(i & 1);
+        if (i >= 2 && !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i >> 1) - 1) & 1), abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + a * N;
+        const uint32_t a_addr = smem_u32(sA + s * kATileBytes);
+        const uint32_t b_addr = smem_u32(sB + bi * C::kBBytes);
+#pragma unroll
+        for (int k = 0; k < DSA_IDX_DIM / 16; ++k)
+          tc_mma_f16(d, desc_kmajor_sw128(a_addr + 32 * k), desc_kmajor_sw128(b_addr + 32 * k),
+                     idesc, k > 0 ? 1u : 0u);
+        tc_commit(&bars->empty[s]);
+        tc_commit(&bars->accfull[a]);
+        advance_unit(p, c);
+      }
+      // every MMA this CTA issued must finish before tensor memory is freed
+      tc_commit(&bars->done);
+      mbar_drain(&bars->done, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int et = threadIdx.x - 64;            // 0 .. 127
+    const int quarter = warp & 3;               // TMEM lanes 32*quarter ..
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    float* wv_warp = sW + (warp - 2) * QB * DSA_IDX_HEADS;
+    UnitCursor c = count > 0 ? locate_unit(p, u0) : UnitCursor{p.B, 0, 0, 0};
+    const int hist_b = c.b;
+    int pb = -1, pqb = -1;
+
+    // No CTA-wide barrier inside this loop: a bounded wait that gives up
+    // leaves the loop early, and every epilogue thread still reaches the
+    // single named barrier after it exactly once.
+    for (long long i = 0; i < count; ++i) {
+      if (c.b != pb || c.qb != pqb) {
+        __syncwarp();
+        for (int j = lane; j < QB * DSA_IDX_HEADS; j += 32) {
+          const int s = c.qb * QB + j / DSA_IDX_HEADS;
+          wv_warp[j] = s < p.S
+              ? p.w[(static_cast<size_t>(c.b) * p.S + s) * DSA_IDX_HEADS + (j % DSA_IDX_HEADS)]
+              : 0.0f;
+        }
+        __syncwarp();
+        pb = c.b;
+        pqb = c.qb;
+      }
+      const int a = static_cast<int>(i & 1);
+      if (!mbar_wait_bounded(&bars->accfull[a], static_cast<uint32_t>((i >> 1) & 1), abort_flag)) break;
+      tc_fence_after();
+      const int t = c.kt * kKeyTile + quarter * 32 + lane;
+      const int T = p.lens.T[c.b];
+#pragma unroll 1
+      for (int jq = 0; jq < QB; jq += C::QG) {
+        float v[C::QG][16];
+#pragma unroll
+        for (int g = 0; g < C::QG; ++g)
+          tmem_ld16(tmem_base + lane_addr + a * N + (jq + g) * 16, v[g]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < C::QG; ++g) {
+          const int s = c.qb * QB + jq + g;
+          if (s >= p.S) break;
+          const float* wv = wv_warp + (jq + g) * DSA_IDX_HEADS;
+          float acc = 0.0f;
+#pragma unroll
+          for (int h = 0; h < DSA_IDX_HEADS; ++h) acc = fmaf(wv[h], fmaxf(v[g][h], 0.0f), acc);
+          const bool valid = t < visible_len(T, p.S, s);
+          if (valid) p.scores[(static_cast<size_t>(c.b) * p.S + s) * p.cap + t] = acc;
+          if constexpr (HIST) {
+            const uint32_t bin = valid ? (float_key(acc) >> (32 - kHistBits)) : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (valid && lane == __ffs(peers) - 1)
+              atomicAdd(&sHist[(jq + g) * kHistBins + bin], static_cast<uint32_t>(__popc(peers)));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->accempty[a]);
+      advance_unit(p, c);
+    }
+    if constexpr (HIST) {
+      // one query block per CTA here (see the unit ranges above)
+      named_bar_sync(1, 128);
+      if (count > 0) {
+        for (int j = 0; j < QB; ++j) {
+          const int s = j;
+          if (s >= p.S) break;
+          uint32_t* g = p.hist + static_cast<size_t>(hist_b * p.S + s) * kHistBins;
+          for (int bin = et; bin < kHistBins; bin += 128) {
+            const uint32_t v = sHist[j * kHistBins + bin];
+            if (v) atomicAdd(g + bin, v);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (threadIdx.x == 0 && bars->abort_flag) atomicOr(p.status, kDevTimeout);
+}
+
+size_t indexer_smem_bytes(int QB, bool with_hist, int* stages_out, size_t smem_limit) {
+  const int N = QB * 16;
+  size_t ob, ow, oh, obar;
+  int stages = kIdxMaxStages;
+  if (with_hist && QB >= 8) stages = 6;
+  while (stages > 2 && indexer_smem_layout(N, with_hist, stages, &ob, &ow, &oh, &obar) > smem_limit)
+    --stages;
+  *stages_out = stages;
+  return indexer_smem_layout(N, with_hist, stages, &ob, &ow, &oh, &obar);
+}
+
+template <int N, bool HIST>
+static cudaError_t launch_n(const IndexerParams& p, const CUtensorMap& tm_kI,
+                            const CUtensorMap& tm_qI, dim3 grid, size_t smem, int stages,
+                            cudaStream_t stream) {
+  auto kern = indexer_tc_kernel<N, HIST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kIdxThreads, smem, stream>>>(tm_kI, tm_qI, p, stages);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_indexer(const IndexerParams& p, const CUtensorMap& tm_kI,
+                           const CUtensorMap& tm_qI, dim3 grid, size_t smem, int stages,
+                           cudaStream_t stream) {
+  const bool hist = p.hist != nullptr;
+  switch (p.QB) {
+#define DSA_IDX_CASE(QBV)                                                                  \
+  case QBV:                                                                                \
+    return hist ? launch_n<QBV * 16, true>(p, tm_kI, tm_qI, grid, smem, stages, stream)   \
+                : launch_n<QBV * 16, false>(p, tm_kI, tm_qI, grid, smem, stages, stream);
+    DSA_IDX_CASE(1)
+    DSA_IDX_CASE(2)
+    DSA_IDX_CASE(4)
+    DSA_IDX_CASE(8)
+    DSA_IDX_CASE(16)
+#undef DSA_IDX_CASE
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,363 @@
+// Exact radix top-k over fp32 scores.
+//
+// PR #33802 "... for SM12x and 256K context", Summary item 2: the pages'
+// selection is a radix-histogram partial top-k per 2,048-key chunk (histogram
+// updates aggregated per warp with __match_any_sync) followed by one
+// single-launch final merge-and-emit kernel. With top_k = 2,048 equal to the
+// chunk size a per-chunk top-k prunes nothing, so here the chunks build ONE
+// global radix histogram per query row and the selection is a global radix
+// select:
+//
+//   1. histogram of the top 11 bits of every visible key (fused into the
+//      indexer epilogue in decode; topk_hist_kernel for dsa_topk);
+//   2. topk_chunk_select_kernel, one CTA per (chunk, row): every CTA finds the
+//      threshold bin from the row histogram, writes its chunk's "certainly
+//      selected" bits into a selection bitmap and appends the threshold-bin
+//      candidates to a list; the last CTA of the row to finish (an atomic
+//      ticket, no waiting) resolves the candidates exactly (radix select over
+//      64-bit (key, ~index) composites, so equal scores go to the lower index)
+//      and emits the selected indices in ascending order from the bitmap;
+//   3. topk_row_kernel: when there are many rows and each fits in shared
+//      memory (prefill), one CTA per row runs the whole radix select in
+//      shared memory and emits with block scans.
+//
+// Keys: float_key() maps fp32 to an order-preserving uint32 (-0.0 == +0.0).
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dsa {
+
+constexpr int kHistThreads = 256;
+constexpr int kSelThreads = 512;
+constexpr int kRowThreads = 1024;
+constexpr int kCandSmem = 6144;   // candidates resolved from shared memory up to this many
+
+struct RowInfo {
+  int n, keff;
+};
+
+__device__ __forceinline__ RowInfo row_info(const TopkParams& p, int r) {
+  const int b = r / p.S, s = r % p.S;
+  RowInfo ri;
+  ri.n = visible_len(p.lens.T[b], p.S, s);
+  ri.keff = min(p.k, ri.n);
+  return ri;
+}
+
+// Warp-aggregated shared-memory histogram increment (lanes with equal bins
+// add once); bin == 0xFFFFFFFF marks an inactive lane. All lanes call.
+__device__ __forceinline__ void hist_add_warp(uint32_t* h, uint32_t bin) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  if (bin != 0xFFFFFFFFu && (threadIdx.x & 31) == __ffs(peers) - 1)
+    atomicAdd(&h[bin], static_cast<uint32_t>(__popc(peers)));
+}
+
+// ---------------------------------------------------------------------------
+// 1. chunk histograms -> one histogram per row (top 11 key bits)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const TopkParams p) {
+  __shared__ uint32_t h[kHistBins];
+  const int rl = blockIdx.y, r = p.row0 + rl, c = blockIdx.x;
+  const RowInfo ri = row_info(p, r);
+  const int t0 = c * kChunk;
+  if (t0 >= ri.n) return;
+  for (int i = threadIdx.x; i < kHistBins; i += kHistThreads) h[i] = 0u;
+  __syncthreads();
+  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
+  for (int j = threadIdx.x; j < kChunk; j += kHistThreads) {
+    const int t = t0 + j;
+    const uint32_t bin = t < ri.n ? (float_key(row[t]) >> (32 - kHistBits)) : 0xFFFFFFFFu;
+    hist_add_warp(h, bin);
+  }
+  __syncthreads();
+  uint32_t* g = p.hist + static_cast<size_t>(rl) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kHistThreads)
+    if (h[i]) atomicAdd(g + i, h[i]);
+}
+
+// ---------------------------------------------------------------------------
+// Exact select among candidate composites (key << 32 | ~index), all sharing
+// the top 11 key bits `bin`: marks the `need` largest in the row bitmap.
+// `cands` may point to shared or global memory.
+// ---------------------------------------------------------------------------
+__device__ void resolve_candidates(const unsigned long long* cands, int count, uint32_t bin,
+                                   uint32_t need, uint32_t* bitmap_row, uint32_t* hist,
+                                   uint32_t* warp_tot, int* sd, uint32_t* sabove,
+                                   uint32_t* scnt) {
+  unsigned long long prefix = static_cast<unsigned long long>(bin) << 53;
+  unsigned long long mask = ~0ull << 53;
+  int hi = 52;
+  while (hi >= 0) {
+    const int w = hi + 1 < 11 ? hi + 1 : 11;
+    const int sh = hi - w + 1;
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < (1 << w); i += kSelThreads) hist[i] = 0u;
+    __syncthreads();
+    const int cround = ((count + 31) / 32) * 32;   // whole warps take part
+    for (int i = threadIdx.x; i < cround; i += kSelThreads) {
+      uint32_t d = 0xFFFFFFFFu;
+      if (i < count) {
+        const unsigned long long cc = cands[i];
+        if ((cc & mask) == prefix) d = static_cast<uint32_t>(cc >> sh) & dm;
+      }
+      hist_add_warp(hist, d);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
+    __syncthreads();
+    find_threshold_digit<kSelThreads>(hist, 1 << w, need, warp_tot, sd, sabove, scnt);
+    const uint32_t d = static_cast<uint32_t>(*sd);
+    need -= *sabove;
+    prefix |= static_cast<unsigned long long>(d) << sh;
+    mask |= static_cast<unsigned long long>(dm) << sh;
+    const bool all = (*scnt == need);
+    __syncthreads();
+    if (all) break;
+    hi -= w;
+  }
+  // selected: determined bits >= the threshold prefix
+  for (int i = threadIdx.x; i < count; i += kSelThreads) {
+    const unsigned long long cc = cands[i];
+    if ((cc & mask) >= prefix) {
+      const uint32_t t = 0xFFFFFFFFu - static_cast<uint32_t>(cc & 0xFFFFFFFFull);
+      atomicOr(&bitmap_row[t >> 5], 1u << (t & 31));
+    }
+  }
+}
+
+// Emit the set bits of bitmap words [0, nwords) as ascending indices into
+// out[0 ..), then -1 up to k.
+__device__ void emit_bitmap(const uint32_t* bitmap_row, int nwords, int32_t* out, int keff,
+                            int k, uint32_t* warp_tot) {
+  const int per = (nwords + kSelThreads - 1) / kSelThreads;
+  const int w0 = threadIdx.x * per;
+  uint32_t cnt = 0;
+  for (int j = 0; j < per; ++j) {
+    const int wi = w0 + j;
+    if (wi < nwords) cnt += __popc(__ldcg(bitmap_row + wi));
+  }
+  uint32_t total;
+  uint32_t pos = block_exclusive_scan<kSelThreads>(cnt, warp_tot, &total);
+  for (int j = 0; j < per; ++j) {
+    const int wi = w0 + j;
+    if (wi >= nwords) break;
+    uint32_t bits = __ldcg(bitmap_row + wi);
+    while (bits) {
+      const int bpos = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < static_cast<uint32_t>(keff)) out[pos] = wi * 32 + bpos;
+      ++pos;
+    }
+  }
+  for (int i = keff + threadIdx.x; i < k; i += kSelThreads) out[i] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// 2. per-chunk select + last-CTA merge-and-emit
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSelThreads) topk_chunk_select_kernel(const TopkParams p) {
+  extern __shared__ unsigned long long s_cands[];   // kCandSmem entries
+  __shared__ uint32_t h[kHistBins];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ int s_d;
+  __shared__ uint32_t s_above, s_cnt;
+  __shared__ int s_last;
+
+  const int rl = blockIdx.y, r = p.row0 + rl, c = blockIdx.x;
+  const RowInfo ri = row_info(p, r);
+  const int nch = (ri.n + kChunk - 1) / kChunk;
+  if (c >= nch) return;
+
+  // threshold bin of the row from its histogram
+  const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h[i] = __ldcg(gh + i);
+  if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+  __syncthreads();
+  find_threshold_digit<kSelThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
+                                    &s_above, &s_cnt);
+  const uint32_t bin = static_cast<uint32_t>(s_d);
+  const uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
+  const bool take_all = (need == s_cnt);
+
+  // scan the chunk: bitmap words for sure keys, candidates for the threshold bin
+  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
+  uint32_t* bm = p.bitmap + static_cast<size_t>(rl) * p.bitmap_stride;
+  unsigned long long* cl = p.cands + static_cast<size_t>(rl) * p.cand_stride;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t_end = min(ri.n, (c + 1) * kChunk);
+  for (int base = c * kChunk + warp * 32; base < (c + 1) * kChunk; base += kSelThreads) {
+    const int t = base + lane;
+    bool sel = false, cand = false;
+    uint32_t key = 0;
+    if (t < t_end) {
+      key = float_key(row[t]);
+      const uint32_t kb = key >> (32 - kHistBits);
+      sel = kb > bin || (take_all && kb == bin);
+      cand = !take_all && kb == bin;
+    }
+    const uint32_t word = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0 && base < ri.n) bm[base >> 5] = word;
+    const uint32_t cm = __ballot_sync(0xffffffffu, cand);
+    if (cm) {
+      uint32_t wbase = 0;
+      if (lane == 0) wbase = atomicAdd(&p.cand_count[rl], static_cast<uint32_t>(__popc(cm)));
+      wbase = __shfl_sync(0xffffffffu, wbase, 0);
+      if (cand) {
+        const uint32_t rank = __popc(cm & ((1u << lane) - 1u));
+        cl[wbase + rank] = (static_cast<unsigned long long>(key) << 32) |
+                           static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(t));
+      }
+    }
+  }
+
+  // ticket: the last CTA of the row finishes the selection
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t prev = atomicAdd(&p.ticket[rl], 1u);
+    s_last = (prev == static_cast<uint32_t>(nch - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  if (!take_all) {
+    const int count = static_cast<int>(__ldcg(&p.cand_count[rl]));
+    const unsigned long long* src = cl;
+    if (count <= kCandSmem) {
+      for (int i = threadIdx.x; i < count; i += kSelThreads) s_cands[i] = __ldcg(cl + i);
+      __syncthreads();
+      src = s_cands;
+    }
+    resolve_candidates(src, count, bin, need, bm, h, warp_tot, &s_d, &s_above, &s_cnt);
+    __threadfence();
+    __syncthreads();
+  }
+  emit_bitmap(bm, (ri.n + 31) / 32, p.idx + static_cast<size_t>(r) * p.k, ri.keff, p.k,
+              warp_tot);
+}
+
+// ---------------------------------------------------------------------------
+// 3. whole-row select in shared memory (one CTA per row)
+// ---------------------------------------------------------------------------
+int topk_row_max_len(size_t smem_limit) {
+  const size_t fixed = (kHistBins + 64) * sizeof(uint32_t) + 1024;
+  if (smem_limit <= fixed) return 0;
+  return static_cast<int>(((smem_limit - fixed) / sizeof(uint32_t)) & ~size_t(3));
+}
+
+__global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams p) {
+  extern __shared__ uint32_t skeys[];          // n keys, then the histogram
+  __shared__ uint32_t warp_tot[32];
+  __shared__ int s_d;
+  __shared__ uint32_t s_above, s_cnt;
+
+  const int r = blockIdx.x;
+  const RowInfo ri = row_info(p, r);
+  const int n = ri.n;
+  uint32_t* h = skeys + ((n + 3) & ~3);
+  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
+  for (int i = threadIdx.x; i < n; i += kRowThreads) skeys[i] = float_key(row[i]);
+  const int nround = ((n + 31) / 32) * 32;
+
+  uint32_t prefix = 0, mask = 0, need = static_cast<uint32_t>(ri.keff);
+  bool all = false;
+  const int shifts[3] = {21, 10, 0};
+  const int widths[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3 && !all; ++pass) {
+    const int sh = shifts[pass], w = widths[pass];
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < (1 << w); i += kRowThreads) h[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nround; i += kRowThreads) {
+      uint32_t d = 0xFFFFFFFFu;
+      if (i < n) {
+        const uint32_t key = skeys[i];
+        if ((key & mask) == prefix) d = (key >> sh) & dm;
+      }
+      hist_add_warp(h, d);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+    __syncthreads();
+    find_threshold_digit<kRowThreads>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
+    need -= s_above;
+    prefix |= static_cast<uint32_t>(s_d) << sh;
+    mask |= dm << sh;
+    all = (s_cnt == need);
+    __syncthreads();
+  }
+  // keys above the threshold are selected; keys equal to it are selected in
+  // index order until `need` of them are taken (all of them when `all`)
+  const uint32_t eq_limit = all ? 0xFFFFFFFFu : need;
+  int32_t* out = p.idx + static_cast<size_t>(r) * p.k;
+  uint32_t eq_run = 0, sel_run = 0;
+  for (int tile = 0; tile < n; tile += 4 * kRowThreads) {
+    const int i0 = tile + 4 * threadIdx.x;
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j;
+      if (i < n) {
+        const uint32_t km = skeys[i] & mask;
+        if (km > prefix) gt |= 1u << j;
+        else if (km == prefix) eq |= 1u << j;
+      }
+    }
+    uint32_t eq_tot;
+    uint32_t eq_before = eq_run + block_exclusive_scan<kRowThreads>(__popc(eq), warp_tot, &eq_tot);
+    uint32_t sel = gt;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((eq >> j) & 1u) {
+        if (eq_before < eq_limit) sel |= 1u << j;
+        ++eq_before;
+      }
+    uint32_t sel_tot;
+    uint32_t pos = sel_run + block_exclusive_scan<kRowThreads>(__popc(sel), warp_tot, &sel_tot);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((sel >> j) & 1u) {
+        if (pos < static_cast<uint32_t>(ri.keff)) out[pos] = i0 + j;
+        ++pos;
+      }
+    eq_run += eq_tot;
+    sel_run += sel_tot;
+  }
+  for (int i = ri.keff + threadIdx.x; i < p.k; i += kRowThreads) out[i] = -1;
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream) {
+  dim3 grid(p.nchunks, p.nrows);
+  topk_hist_kernel<<<grid, kHistThreads, 0, stream>>>(p);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
+  const size_t smem = kCandSmem * sizeof(unsigned long long);
+  cudaError_t e = cudaFuncSetAttribute(topk_chunk_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.nchunks, p.nrows);
+  topk_chunk_select_kernel<<<grid, kSelThreads, smem, stream>>>(p);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit,
+                            cudaStream_t stream) {
+  const size_t smem = (static_cast<size_t>((max_n + 3) & ~3) + kHistBins) * sizeof(uint32_t);
+  if (smem + 1024 > smem_limit) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(topk_row_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  topk_row_kernel<<<p.B * p.S, kRowThreads, smem, stream>>>(p);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,252 @@
+"""Python binding of libdsa (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks that the tensors it is handed are contiguous
+CUDA tensors of the dtype and shape the problem implies, passes their device
+pointers and PyTorch's current stream to the C ABI, and raises DsaError on a
+non-zero status. There is no fallback: if libdsa.so is missing the first call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+# mirrors include/dsa.h
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE = 0, 1, 2, 3
+DSA_ERR_MISALIGNED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT, DSA_ERR_NO_DEVICE = 4, 5, 6, 7
+DSA_BF16, DSA_FP16, DSA_INT8, DSA_FP32 = 0, 1, 2, 3
+DSA_OP_INDEX_SCORES, DSA_OP_TOPK, DSA_OP_DECODE, DSA_OP_PREFILL = 0, 1, 2, 3
+DSA_MAX_BATCH = 64
+DSA_KERNEL_INDEXER, DSA_KERNEL_TOPK_HIST, DSA_KERNEL_TOPK_SELECT = 0, 1, 2
+DSA_KERNEL_TOPK_ROW, DSA_KERNEL_ATTENTION = 3, 4
+
+EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
+            "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill",
+            "dsa_read_device_status", "dsa_last_error_string", "dsa_status_string",
+            "dsa_version", "dsa_timing_select", "dsa_timing_read"]
+
+_DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
+_TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
+             DSA_FP32: torch.float32}
+
+
+class DsaProblem(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("idx_heads", ctypes.c_int32),
+        ("idx_dim", ctypes.c_int32),
+        ("cache_capacity", ctypes.c_int32),
+        ("top_k", ctypes.c_int32),
+        ("total_len", ctypes.c_int32 * DSA_MAX_BATCH),
+        ("softmax_scale", ctypes.c_float),
+        ("q_dtype", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
+        ("attn_split_keys", ctypes.c_int32),
+    ]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libdsa.so (built in-tree by build_lib.build()); raise if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"libdsa.so not found at {p}: build it with "
+                           "top_sparse_attention_chunked_gb300.build_lib.build()")
+    lib = ctypes.CDLL(p)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    P = ctypes.POINTER(DsaProblem)
+    sig = {
+        "dsa_workspace_size": (sz, [P, i32]),
+        "dsa_index_scores": (i32, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "dsa_topk": (i32, [P, vp, vp, vp, sz, vp]),
+        "dsa_sparse_attn_decode": (i32, [P] + [vp] * 11 + [sz, vp]),
+        "dsa_sparse_attn_prefill": (i32, [P] + [vp] * 11 + [sz, vp]),
+        "dsa_read_device_status": (i32, [vp, sz, vp, ctypes.POINTER(ctypes.c_uint32)]),
+        "dsa_last_error_string": (ctypes.c_char_p, []),
+        "dsa_status_string": (ctypes.c_char_p, [i32]),
+        "dsa_version": (i32, []),
+        "dsa_timing_select": (i32, [i32]),
+        "dsa_timing_read": (i32, [ctypes.POINTER(ctypes.c_float)]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != DSA_OK:
+        lib = load_library()
+        raise DsaError(status, lib.dsa_last_error_string().decode())
+
+
+def make_problem(batch: int, q_len: int, total_len: Sequence[int] | int, top_k: int,
+                 num_q_heads: int = 24, num_kv_heads: int = 2, cache_capacity: Optional[int] = None,
+                 q_dtype="bf16", kv_dtype="bf16", out_dtype=None, softmax_scale: float = 0.0,
+                 head_dim: int = 128, idx_heads: int = 16, idx_dim: int = 64,
+                 attn_split_keys: int = 0) -> DsaProblem:
+    """Fill a DsaProblem; dtypes by name ('bf16', 'fp16', 'int8', 'fp32')."""
+    if isinstance(total_len, int):
+        total_len = [total_len] * max(1, min(batch, DSA_MAX_BATCH))
+    p = DsaProblem()
+    p.batch, p.q_len = batch, q_len
+    p.num_q_heads, p.num_kv_heads, p.head_dim = num_q_heads, num_kv_heads, head_dim
+    p.idx_heads, p.idx_dim = idx_heads, idx_dim
+    p.cache_capacity = cache_capacity if cache_capacity is not None else max(total_len)
+    p.top_k = top_k
+    for b, t in enumerate(list(total_len)[:DSA_MAX_BATCH]):
+        p.total_len[b] = int(t)
+    p.softmax_scale = softmax_scale
+    p.q_dtype = _DT[q_dtype]
+    p.kv_dtype = _DT[kv_dtype]
+    p.out_dtype = _DT[out_dtype if out_dtype is not None else q_dtype]
+    p.attn_split_keys = attn_split_keys
+    return p
+
+
+def problem_for(wl, **overrides) -> DsaProblem:
+    """DsaProblem of a dsa_inputs.Workload."""
+    kw = dict(batch=wl.batch, q_len=wl.q_len, total_len=wl.total_len, top_k=wl.top_k,
+              num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+              cache_capacity=wl.cap, q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype,
+              head_dim=wl.head_dim, idx_heads=wl.idx_heads, idx_dim=wl.idx_dim)
+    kw.update(overrides)
+    return make_problem(**kw)
+
+
+def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def dsa_workspace_size(p: DsaProblem, op: int) -> int:
+    lib = load_library()
+    n = lib.dsa_workspace_size(ctypes.byref(p), op)
+    if n == 0:
+        raise DsaError(DSA_ERR_INVALID_ARG, lib.dsa_last_error_string().decode())
+    return n
+
+
+def alloc_workspace(p: DsaProblem, op: int, device="cuda") -> torch.Tensor:
+    """Caller-owned workspace (torch allocations are 256-byte aligned)."""
+    return torch.empty(dsa_workspace_size(p, op), dtype=torch.uint8, device=device)
+
+
+def _ws(ws: torch.Tensor):
+    return _ptr(ws, "workspace", torch.uint8), ws.numel()
+
+
+def dsa_index_scores(p: DsaProblem, qI, w, kI, scores, workspace, stream=None):
+    B, S, cap = p.batch, p.q_len, p.cache_capacity
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check(lib.dsa_index_scores(
+        ctypes.byref(p), _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
+        _ptr(w, "w", torch.float32, (B, S, 16)), _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)),
+        _ptr(scores, "scores", torch.float32, (B, S, cap)), wp, wn, _stream(stream)))
+
+
+def dsa_topk(p: DsaProblem, scores, idx, workspace, stream=None):
+    B, S, cap = p.batch, p.q_len, p.cache_capacity
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    _check(lib.dsa_topk(ctypes.byref(p), _ptr(scores, "scores", torch.float32, (B, S, cap)),
+                        _ptr(idx, "idx", torch.int32, (B, S, p.top_k)), wp, wn, _stream(stream)))
+
+
+def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream):
+    B, S, cap, Hq, Hkv = p.batch, p.q_len, p.cache_capacity, p.num_q_heads, p.num_kv_heads
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    kvdt = _TORCH_DT[p.kv_dtype]
+    args = [
+        ctypes.byref(p),
+        _ptr(q, "q", _TORCH_DT[p.q_dtype], (B, S, Hq, 128)),
+        _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
+        _ptr(w, "w", torch.float32, (B, S, 16)),
+        _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)),
+        _ptr(k, "k", kvdt, (B, cap, Hkv, 128)),
+        _ptr(v, "v", kvdt, (B, cap, Hkv, 128)),
+        _ptr(k_scale, "k_scale", torch.float32, (B, cap, Hkv)),
+        _ptr(v_scale, "v_scale", torch.float32, (B, cap, Hkv)),
+        _ptr(idx_out, "idx_out", torch.int32, (B, S, p.top_k)),
+        _ptr(out, "out", _TORCH_DT[p.out_dtype], (B, S, Hq, 128)),
+        wp, wn, _stream(stream),
+    ]
+    _check(getattr(lib, fn_name)(*args))
+
+
+def dsa_sparse_attn_decode(p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace,
+                           stream=None):
+    _attn("dsa_sparse_attn_decode", p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
+          workspace, stream)
+
+
+def dsa_sparse_attn_prefill(p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace,
+                            stream=None):
+    _attn("dsa_sparse_attn_prefill", p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
+          workspace, stream)
+
+
+def dsa_read_device_status(workspace, stream=None) -> int:
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    st = ctypes.c_uint32(0)
+    _check(lib.dsa_read_device_status(wp, wn, _stream(stream), ctypes.byref(st)))
+    return st.value
+
+
+def dsa_timing_select(kind: int):
+    _check(load_library().dsa_timing_select(kind))
+
+
+def dsa_timing_read() -> float:
+    ms = ctypes.c_float(0.0)
+    _check(load_library().dsa_timing_read(ctypes.byref(ms)))
+    return ms.value
+
+
+def dsa_version() -> int:
+    return load_library().dsa_version()

@@ -69,6 +69,13 @@ def algorithmic_bytes(wl, idx_np=None):
     return {"step": kI + scores + kv + small, "indexer": indexer, "kv": kv}
 
 
+def indexer_flops(wl):
+    """2 * 16 heads * 64 dims per (query token, visible key)."""
+    S, T = wl.q_len, wl.total_len
+    vis = sum(T - S + s + 1 for s in range(S))
+    return wl.batch * vis * 2 * 16 * 64
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -124,20 +131,34 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle leg
+def oracle_rows(wl, max_rows=32):
+    """Query rows the oracle leg times: all of them for decode-sized batches, a
+    seeded sample (first and last included) when there are many."""
+    import numpy as np
+    rows = [(b, s) for b in range(wl.batch) for s in range(wl.q_len)]
+    if len(rows) <= max_rows:
+        return None, len(rows)
+    rng = np.random.default_rng(0)
+    pick = sorted({0, len(rows) - 1, *rng.choice(len(rows), max_rows - 2, replace=False).tolist()})
+    return [rows[i] for i in pick], len(pick)
+
+
 def oracle_step_time(wl, cpu, budget_s=10.0, max_reps=50):
-    """Time the float64 oracle on full steps of the workload (bounded)."""
+    """Time the float64 oracle on steps of the workload (bounded). Returns
+    (seconds per step, query tokens per step)."""
     import numpy as np
     import oracle.dsa_oracle as O
     from dsa_inputs import to_f64
     f = {k: to_f64(v) if hasattr(v, "numpy") else v for k, v in cpu.items()}
     f["total_len"] = cpu["total_len"].numpy().astype(np.int64)
+    rows, ntok = oracle_rows(wl)
     times = []
     t_end = time.perf_counter() + budget_s
     while len(times) < max_reps and (not times or time.perf_counter() < t_end):
         t0 = time.perf_counter()
-        O.sparse_attention_step(f, wl.num_kv_heads, wl.top_k)
+        O.sparse_attention_step(f, wl.num_kv_heads, wl.top_k, rows=rows)
         times.append(time.perf_counter() - t0)
-    return times
+    return times, ntok
 
 
 def cores():
@@ -158,10 +179,13 @@ def run_reference(args, wl):
         oracle_step_time(wl, cpu, budget_s=0.0, max_reps=1)
     times = []
     for _ in range(args.steps):
-        times += oracle_step_time(wl, cpu, budget_s=0.0, max_reps=1)
+        t, ntok = oracle_step_time(wl, cpu, budget_s=0.0, max_reps=1)
+        times += t
     ms = 1e3 * statistics.mean(times)
-    value = wl.query_tokens / (ms / 1e3)
-    sample = f"full {wl.name} step ({wl.query_tokens} query tokens) per timed step"
+    value = ntok / (ms / 1e3)
+    sample = (f"{ntok} of {wl.query_tokens} query tokens of {wl.name} per timed step"
+              if ntok < wl.query_tokens else
+              f"full {wl.name} step ({wl.query_tokens} query tokens) per timed step")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -206,16 +230,19 @@ def run_libdsa(args, wl):
     cpu = make_inputs(wl, seed=wl.seed + 7919 * rank)   # an independent replica per rank
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
     p = D.problem_for(wl)
-    ws = D.alloc_workspace(p, D.DSA_OP_DECODE)
+    ws = D.alloc_workspace(p, D.DSA_OP_PREFILL if wl.q_len > 16 else D.DSA_OP_DECODE)
     out = torch.empty(wl.batch, wl.q_len, wl.num_q_heads, 128, dtype=D._TORCH_DT[p.out_dtype],
                       device="cuda")
     idx = torch.empty(wl.batch, wl.q_len, wl.top_k, dtype=torch.int32, device="cuda")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
+    prefill = wl.q_len > 16
+    call = D.dsa_sparse_attn_prefill if prefill else D.dsa_sparse_attn_decode
+
     def step():
-        D.dsa_sparse_attn_decode(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"],
-                                 dev["v"], dev["k_scale"], dev["v_scale"], idx, out, ws)
+        call(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"], dev["k_scale"],
+             dev["v_scale"], idx, out, ws)
 
     D.dsa_timing_select(D.DSA_KERNEL_INDEXER)
     for _ in range(max(3, args.warmup)):
@@ -277,8 +304,10 @@ def run_libdsa(args, wl):
 
     # ---------------- per-kernel breakdown (separate short eager loop)
     per_kernel = {}
-    for name, kind in (("indexer", D.DSA_KERNEL_INDEXER), ("topk_select", D.DSA_KERNEL_TOPK_SELECT),
-                       ("attention", D.DSA_KERNEL_ATTENTION)):
+    kinds = [("indexer", D.DSA_KERNEL_INDEXER),
+             ("topk_row", D.DSA_KERNEL_TOPK_ROW) if prefill else ("topk_select", D.DSA_KERNEL_TOPK_SELECT),
+             ("attention", D.DSA_KERNEL_ATTENTION)]
+    for name, kind in kinds:
         D.dsa_timing_select(kind)
         vals = []
         for _ in range(10):
@@ -317,15 +346,29 @@ def run_libdsa(args, wl):
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu_base = None
     if rank == 0 and world == 1:
-        times = oracle_step_time(wl, cpu, budget_s=args.cpu_budget)
-        cpu_base = {"value": wl.query_tokens / statistics.mean(times), "unit": UNIT,
+        times, ntok = oracle_step_time(wl, cpu, budget_s=args.cpu_budget)
+        what = (f"{ntok} sampled query rows of" if ntok < wl.query_tokens else "full")
+        cpu_base = {"value": ntok / statistics.mean(times), "unit": UNIT,
                     "cores": cores(), "kind": "oracle",
-                    "sample": f"{len(times)} full {wl.name} steps ({wl.query_tokens} query "
+                    "sample": f"{len(times)} x {what} {wl.name} step ({ntok} query "
                               f"token(s) each) in float64 NumPy"}
 
     idx_us = 1e3 * statistics.mean(idx_ms)
-    achieved = ab["indexer"] / (idx_us * 1e-6) / 1e9
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
+    if prefill:
+        # the dense causal indexer contraction is tensor-bound
+        flops = indexer_flops(wl)
+        achieved = flops / (idx_us * 1e-6) / 1e12
+        roof = {"kernel": "indexer_tc_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": bf16, "unit": "TFLOP/s", "frac": round(achieved / bf16, 4),
+                "peak_kind": peak_kind, "traffic": None, "algorithmic_flops": flops,
+                "launch_us": round(idx_us, 2)}
+    else:
+        achieved = ab["indexer"] / (idx_us * 1e-6) / 1e9
+        roof = {"kernel": "indexer_tc_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes": ab["indexer"],
+                "launch_us": round(idx_us, 2)}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -337,16 +380,15 @@ def run_libdsa(args, wl):
             "hbm_frac_step": round(step_gbs / hbm, 4),
             "hbm_frac_step_of_8tbs": round(step_gbs / 8000.0, 4),
             "algorithmic_bytes_step": ab["step"],
-            "roofline": {"kernel": "indexer_tc_kernel", "bound": "hbm",
-                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-                         "traffic": None, "algorithmic_bytes": ab["indexer"],
-                         "launch_us": round(idx_us, 2)},
+            "roofline": roof,
             "per_kernel_us": per_kernel,
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
             "gpu_launches": 3 * args.steps,
+            "kernels_per_step": ["indexer_tc_kernel",
+                                 "topk_row_kernel" if prefill else "topk_chunk_select_kernel",
+                                 "sparse_attn_prefill_tc_kernel" if prefill else "sparse_attn_kernel"],
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)

@@ -211,13 +211,36 @@ def test_decode_fp32_output_and_ragged_lengths(dsa):
     assert err < 2e-4   # no output rounding: only the attention arithmetic
 
 
-@pytest.mark.parametrize("B,S,T,cap,k", [(2, 40, 300, 320, 64), (1, 130, 2500, 2500, 2048),
-                                         (1, 33, 33, 33, 8)])
-def test_prefill_parity_small(dsa, B, S, T, cap, k):
-    wl = small_workload(batch=B, q_len=S, total_len=T, capacity=cap, num_q_heads=24,
-                        num_kv_heads=2, top_k=k, seed=S)
+@pytest.mark.parametrize("kv", ["bf16", "fp16", "int8"])
+@pytest.mark.parametrize("B,S,T,cap,Hq,Hkv,k", [
+    (2, 40, 300, 320, 24, 2, 64), (1, 130, 2500, 2500, 24, 2, 2048), (1, 33, 33, 33, 8, 2, 8),
+    (2, 17, 1000, 1100, 32, 1, 200), (1, 50, 4000, 4000, 4, 4, 3000),
+])
+def test_prefill_parity_small(dsa, kv, B, S, T, cap, Hq, Hkv, k):
+    wl = small_workload(batch=B, q_len=S, total_len=T, capacity=cap, num_q_heads=Hq,
+                        num_kv_heads=Hkv, top_k=k, kv_dtype=kv, seed=S + Hq)
     cpu, idx, out = run_step(dsa, wl, prefill=True)
     check_step(wl, cpu, idx, out)
+
+
+def test_prefill_fp16_query_fp16_cache(dsa):
+    wl = small_workload(batch=1, q_len=64, total_len=900, top_k=300, q_dtype="fp16",
+                        kv_dtype="fp16", seed=41)
+    cpu, idx, out = run_step(dsa, wl, prefill=True)
+    check_step(wl, cpu, idx, out)
+
+
+def test_prefill_and_decode_agree(dsa):
+    """The same 8 query tokens through the decode path and the prefill path."""
+    wl = small_workload(batch=2, q_len=8, total_len=6000, num_q_heads=24, num_kv_heads=2,
+                        top_k=2048, kv_dtype="bf16", seed=43)
+    cpu = make_inputs(wl)
+    _, idx_d, out_d = run_step(dsa, wl, cpu=cpu, out_dtype="fp32")
+    _, idx_p, out_p = run_step(dsa, wl, cpu=cpu, prefill=True, out_dtype="fp32")
+    check_step(wl, cpu, idx_d, out_d)
+    check_step(wl, cpu, idx_p, out_p)
+    if np.array_equal(idx_d, idx_p):
+        assert rel_l2(out_p, out_d) < 1e-5
 
 
 def test_prefill_parity_8k_on_32k_sampled(dsa):
@@ -294,8 +317,8 @@ def test_int8_large_value_scale_worked_example(dsa, spacing, split):
 
 def test_workspace_reuse_across_shapes(dsa):
     big = WORKLOADS["decode_4k"]
-    small = small_workload(batch=1, q_len=1, total_len=300, num_q_heads=8, num_kv_heads=2,
-                           top_k=512, seed=12)
+    small = small_workload(batch=1, q_len=1, total_len=300, capacity=4096, num_q_heads=8,
+                           num_kv_heads=2, top_k=512, seed=12)
     pb, ps = dsa.problem_for(big), dsa.problem_for(small)
     ws = dsa.alloc_workspace(pb, dsa.DSA_OP_DECODE)
     assert ws.numel() >= dsa.dsa_workspace_size(ps, dsa.DSA_OP_DECODE)

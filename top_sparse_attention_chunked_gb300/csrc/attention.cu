@@ -42,7 +42,11 @@ constexpr int kTile8 = kTileKeys * kD;           // 2 KB: one 16-key tile, INT8
 // INT8: converted K and V tiles (2 x 4 KB), code staging K 0/1, V 0/1
 // (4 x 2 KB) and the k/v scales of both stages (256 B).
 constexpr int kWarpSmem = 4 * kTile16 + 2 * 4 * kTileKeys * 4;
-constexpr int kAttnSmem = kAttnWarps * kWarpSmem;
+// the split combine merges up to kAttnMaxSplits partial states
+constexpr int kMaxCombine = kAttnMaxSplits;
+constexpr int kMergeFloats = kAttnWarps * kPartialFloats + 2 * kMaxCombine * kAttnRows + 2 * kAttnRows;
+constexpr int kAttnSmem = (kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnWarps * kWarpSmem
+                                                                       : kMergeFloats * 4;
 
 enum { KV_BF16 = 0, KV_FP16 = 1, KV_INT8 = 2 };
 
@@ -100,6 +104,40 @@ __device__ __forceinline__ void store_out(void* out, size_t i, float v) {
   else static_cast<float*>(out)[i] = v;
 }
 
+// x * 2^e == (x * f1) * f2 with both factors formed without underflow where
+// it matters: f1 = 2^max(e, -120) is normal, f2 = 2^(e - max(e, -120)) is 1
+// unless e < -120. A state that saw no keys (m = -inf) gets weight 0.
+__device__ __forceinline__ void exp2_pair(float e, float* f1, float* f2) {
+  if (!(e > -1.0e30f)) {
+    *f1 = 0.0f;
+    *f2 = 0.0f;
+    return;
+  }
+  const float a = fmaxf(e, -120.0f);
+  *f1 = exp2f(a);
+  *f2 = exp2f(e - a);
+}
+
+// Thread `row` (< 16) merges `n` online-softmax states whose m / l live at
+// st[j * stride + row] / st[j * stride + 16 + row]: writes the factors that
+// bring state j to the common max and the merged M, L.
+__device__ __forceinline__ void combine_factors(const float* st, int stride, int n, float* fac1,
+                                                float* fac2, float* sML) {
+  const int row = threadIdx.x;
+  float M = -INFINITY;
+  for (int j = 0; j < n; ++j) M = fmaxf(M, st[j * stride + row]);
+  float L = 0.0f;
+  for (int j = 0; j < n; ++j) {
+    float f1, f2;
+    exp2_pair(st[j * stride + row] - M, &f1, &f2);
+    fac1[j * kAttnRows + row] = f1;
+    fac2[j * kAttnRows + row] = f2;
+    L += st[j * stride + kAttnRows + row] * f1 * f2;
+  }
+  sML[row] = M;
+  sML[kAttnRows + row] = L;
+}
+
 template <int KV, bool Q_F16, int OUT>
 __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnParams p) {
   constexpr bool QK_F16 = (KV == KV_FP16) || (KV == KV_INT8 && Q_F16);
@@ -131,22 +169,6 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   uint8_t* sKc[2] = {wsm + 2 * kTile16, wsm + 2 * kTile16 + kTile8};
   uint8_t* sVc[2] = {wsm + 3 * kTile16, wsm + 3 * kTile16 + kTile8};
   float* sSc = reinterpret_cast<float*>(wsm + 4 * kTile16);   // [stage][k 16 | v 16]
-
-  // ---- query fragments (A operand of QK^T), resident for the whole CTA
-  uint32_t qa[kD / 16][4];
-  {
-    const size_t qrow0 = (static_cast<size_t>(r) * p.Hq + h0 + gq) * kD;
-    const size_t qrow1 = qrow0 + 8 * kD;
-    const bool ok0 = gq < nh, ok1 = gq + 8 < nh;
-#pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const int c = kk * 16 + 2 * tq;
-      qa[kk][0] = ok0 ? load_q2<Q_F16, QK_F16>(p.q, qrow0 + c) : 0u;
-      qa[kk][1] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c) : 0u;
-      qa[kk][2] = ok0 ? load_q2<Q_F16, QK_F16>(p.q, qrow0 + c + 8) : 0u;
-      qa[kk][3] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c + 8) : 0u;
-    }
-  }
 
   const int32_t* idx_row = p.idx + static_cast<size_t>(r) * p.topk + split_begin;
   const size_t kv_row_elems = static_cast<size_t>(p.Hkv) * kD;   // per cache token
@@ -202,6 +224,22 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   const int my_tiles = ntiles > warp ? (ntiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
   if (my_tiles > 0) issue_tile(0, 0);
   cp_async_commit();
+  // ---- query fragments (A operand of QK^T), resident for the whole CTA
+  uint32_t qa[kD / 16][4];
+  {
+    const size_t qrow0 = (static_cast<size_t>(r) * p.Hq + h0 + gq) * kD;
+    const size_t qrow1 = qrow0 + 8 * kD;
+    const bool ok0 = gq < nh, ok1 = gq + 8 < nh;
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const int c = kk * 16 + 2 * tq;
+      qa[kk][0] = ok0 ? load_q2<Q_F16, QK_F16>(p.q, qrow0 + c) : 0u;
+      qa[kk][1] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c) : 0u;
+      qa[kk][2] = ok0 ? load_q2<Q_F16, QK_F16>(p.q, qrow0 + c + 8) : 0u;
+      qa[kk][3] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c + 8) : 0u;
+    }
+  }
+
   for (int it = 0; it < my_tiles; ++it) {
     const int st = it & 1;
     if (it + 1 < my_tiles) issue_tile(it + 1, st ^ 1);
@@ -362,6 +400,9 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   }
   __syncthreads();   // stage buffers become the merge area
   float* ws = reinterpret_cast<float*>(smem);      // [warps][kPartialFloats]
+  float* fac1 = ws + kAttnWarps * kPartialFloats;  // [max(warps, splits)][16]
+  float* fac2 = fac1 + kMaxCombine * kAttnRows;
+  float* sML = fac2 + kMaxCombine * kAttnRows;     // M[16], L[16]
   float* mine = ws + warp * kPartialFloats;
   if (tq == 0) {
     mine[gq] = m_run[0];
@@ -377,32 +418,36 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       mine[2 * kAttnRows + row * kD + col] = o_acc[nd][e];
     }
   __syncthreads();
+  if (threadIdx.x < kAttnRows)
+    combine_factors(ws, kPartialFloats, kAttnWarps, fac1, fac2, sML);
+  __syncthreads();
 
   const int d = threadIdx.x;   // one output column per thread
   const bool single = (p.nsplit == 1);
+  const size_t out_row = static_cast<size_t>(r) * p.Hq + h0;
+  float acc[kAttnRows];
+#pragma unroll
+  for (int row = 0; row < kAttnRows; ++row) acc[row] = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kAttnWarps; ++w)
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row)
+      acc[row] += ws[w * kPartialFloats + 2 * kAttnRows + row * kD + d] *
+                  fac1[w * kAttnRows + row] * fac2[w * kAttnRows + row];
+  if (single) {
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row)
+      if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + d, acc[row] / sML[kAttnRows + row]);
+    return;
+  }
   float* part = p.partial + ((static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit + blockIdx.x) *
                                 kPartialFloats;
-  const size_t out_row = static_cast<size_t>(r) * p.Hq + h0;
-  for (int row = 0; row < kAttnRows; ++row) {
-    float M = -INFINITY;
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, ws[w * kPartialFloats + row]);
-    float L = 0.0f, O = 0.0f;
-    for (int w = 0; w < kAttnWarps; ++w) {
-      const float dm = ws[w * kPartialFloats + row] - M;
-      L += mul_exp2(ws[w * kPartialFloats + kAttnRows + row], dm);
-      O += mul_exp2(ws[w * kPartialFloats + 2 * kAttnRows + row * kD + d], dm);
-    }
-    if (single) {
-      if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + d, O / L);
-    } else {
-      if (d == 0) {
-        part[row] = M;
-        part[kAttnRows + row] = L;
-      }
-      part[2 * kAttnRows + row * kD + d] = O;
-    }
+  if (d < kAttnRows) {
+    part[d] = sML[d];
+    part[kAttnRows + d] = sML[kAttnRows + d];
   }
-  if (single) return;
+#pragma unroll
+  for (int row = 0; row < kAttnRows; ++row) part[2 * kAttnRows + row * kD + d] = acc[row];
 
   // ---- split combine by the last CTA of this (row, head group)
   __threadfence();
@@ -415,18 +460,31 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   if (!s_last) return;
   __threadfence();
   const float* parts = p.partial + (static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit * kPartialFloats;
-  for (int row = 0; row < nh; ++row) {
-    float M = -INFINITY;
-    for (int j = 0; j < nreal; ++j) M = fmaxf(M, __ldcg(parts + j * kPartialFloats + row));
-    float L = 0.0f, O = 0.0f;
-    for (int j = 0; j < nreal; ++j) {
-      const float* pj = parts + static_cast<size_t>(j) * kPartialFloats;
-      const float dm = __ldcg(pj + row) - M;
-      L += mul_exp2(__ldcg(pj + kAttnRows + row), dm);
-      O += mul_exp2(__ldcg(pj + 2 * kAttnRows + row * kD + d), dm);
-    }
-    store_out<OUT>(p.out, (out_row + row) * kD + d, O / L);
+  // m and l of every split into shared memory, then the per-split factors
+  float* sm = ws;   // [nreal][2 * 16] (m, l)
+  for (int i = threadIdx.x; i < nreal * 2 * kAttnRows; i += kAttnThreads) {
+    const int j = i / (2 * kAttnRows), o = i % (2 * kAttnRows);
+    sm[j * 2 * kAttnRows + o] = __ldcg(parts + static_cast<size_t>(j) * kPartialFloats + o);
   }
+  __syncthreads();
+  if (threadIdx.x < kAttnRows)
+    combine_factors(sm, 2 * kAttnRows, nreal, fac1, fac2, sML);
+  __syncthreads();
+#pragma unroll
+  for (int row = 0; row < kAttnRows; ++row) acc[row] = 0.0f;
+#pragma unroll 2
+  for (int j = 0; j < nreal; ++j) {
+    const float* oj = parts + static_cast<size_t>(j) * kPartialFloats + 2 * kAttnRows + d;
+    float v[kAttnRows];
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row) v[row] = __ldcg(oj + row * kD);
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row)
+      acc[row] += v[row] * fac1[j * kAttnRows + row] * fac2[j * kAttnRows + row];
+  }
+#pragma unroll
+  for (int row = 0; row < kAttnRows; ++row)
+    if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + d, acc[row] / sML[kAttnRows + row]);
 }
 
 template <int KV, bool Q_F16, int OUT>

@@ -175,6 +175,7 @@ int check_problem(const dsa_problem* p, int op, Derived* d) {
 // Upper bound of the automatic split count (any GPU with <= 256 SMs).
 int splits_bound(const dsa_problem* p, const Derived& d) {
   if (p->attn_split_keys > 0) return ceil_div(d.kmax, p->attn_split_keys);
+  if (ceil_div(d.kmax, 64) > kAttnMaxSplits) return kAttnMaxSplits;
   const int units = d.rows * p->num_kv_heads * d.HG;
   int s = ceil_div(2 * 256, units);
   s = s < 16 ? s : 16;
@@ -196,6 +197,8 @@ void choose_split(const dsa_problem* p, const Derived& d, int sms, int* split_ke
     s = s < cap ? s : cap;
     if (s < 1) s = 1;
     sk = ceil_div(ceil_div(d.kmax, s), 16) * 16;
+    const int sk_min = ceil_div(ceil_div(d.kmax, kAttnMaxSplits), 16) * 16;
+    if (sk < sk_min) sk = sk_min;
   }
   *split_keys = sk;
   *nsplit = ceil_div(d.kmax, sk);
@@ -384,7 +387,7 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
 
 int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
                   const void* q, const void* k, const void* v, const float* ks, const float* vs,
-                  const int32_t* idx, void* out, void* ws, cudaStream_t st) {
+                  const int32_t* idx, void* out, void* ws, bool prefill, cudaStream_t st) {
   AttnParams ap;
   ap.q = q;
   ap.k = k;
@@ -404,14 +407,23 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.cap = p->cache_capacity;
   ap.topk = p->top_k;
   choose_split(p, d, di.sms, &ap.split_keys, &ap.nsplit);
+  if (ap.nsplit > kAttnMaxSplits)
+    return fail(DSA_ERR_UNSUPPORTED, "attn_split_keys %d gives %d splits (max %d)",
+                p->attn_split_keys, ap.nsplit, kAttnMaxSplits);
   if (ap.nsplit > splits_bound(p, d))
     return fail(DSA_ERR_UNSUPPORTED, "device has more SMs than the workspace bound assumes");
   const float scale = p->softmax_scale > 0.0f ? p->softmax_scale
                                               : 1.0f / std::sqrt(static_cast<float>(p->head_dim));
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.lens = lens_of(p);
+  ap.q_dtype = p->q_dtype;
+  ap.out_dtype = p->out_dtype;
+  cudaError_t e;
   timing_before(DSA_KERNEL_ATTENTION, st);
-  cudaError_t e = launch_attention(ap, p->q_dtype, p->kv_dtype, p->out_dtype, st);
+  if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin))
+    e = launch_prefill_tc(ap, p->kv_dtype, di.sms, at<uint32_t>(ws, 0), st);
+  else
+    e = launch_attention(ap, p->q_dtype, p->kv_dtype, p->out_dtype, st);
   timing_after(DSA_KERNEL_ATTENTION, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return DSA_OK;
@@ -462,7 +474,7 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
   if (rc) return rc;
   rc = run_topk(p, d, di, L, scores, idx, ws, decode, !decode, st);
   if (rc) return rc;
-  return run_attention(p, d, di, L, q, k, v, ks, vs, idx, out, ws, st);
+  return run_attention(p, d, di, L, q, k, v, ks, vs, idx, out, ws, !decode, st);
 }
 
 }  // namespace

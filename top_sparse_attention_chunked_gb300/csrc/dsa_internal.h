@@ -80,14 +80,21 @@ struct AttnParams {
   uint32_t* ticket;        // [B*S*Hkv*HG] zeroed when nsplit > 1
   int B, S, Hq, Hkv, G, HG, cap, topk;
   int split_keys, nsplit;
+  int q_dtype, out_dtype;
   float scale_log2;        // softmax_scale * log2(e)
   SeqLens lens;
 };
 
 constexpr int kAttnRows = 16;                                   // heads per MMA tile
+constexpr int kAttnMaxSplits = 128;                             // split-K partial states per row
 constexpr int kPartialFloats = 2 * kAttnRows + kAttnRows * DSA_HEAD_DIM;  // m, l, o
 
 cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
                              cudaStream_t stream);
+
+// tcgen05 prefill attention (BF16 / FP16 cache, top_k <= 2048)
+bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin);
+cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, uint32_t* status,
+                              cudaStream_t stream);
 
 }  // namespace dsa

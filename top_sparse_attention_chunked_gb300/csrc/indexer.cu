@@ -105,7 +105,9 @@ __host__ __device__ inline size_t indexer_smem_layout(int N, bool with_hist, int
   const int QB = N / 16;
   size_t o = static_cast<size_t>(stages) * kATileBytes;
   *off_b = o;
-  o += 2ull * N * DSA_IDX_DIM * 2;
+  // two query-block buffers when a CTA may move to a new block (prefill);
+  // with histograms a CTA owns one sequence's single block
+  o += (with_hist ? 1ull : 2ull) * N * DSA_IDX_DIM * 2;
   *off_w = o;   // one copy of the block's head weights per epilogue warp
   o += 4ull * QB * 16 * sizeof(float);
   o = (o + 15) & ~size_t(15);

@@ -1,0 +1,455 @@
+// Sparse GQA attention for prefill on tcgen05 tensor cores.
+//
+// PR #33997 "[CUDA] Support FP16 KV cache and FP16 query/key in
+// DynamicSparseAttention<BFloat16> ...", Description item 2: the pages run the
+// sparse-attention prefill on tensor cores (mma.sync m16n8k16 f32.f16.f16.f32)
+// over each query token's selected K/V rows. Here the dense tiles run on the
+// 5th-generation tensor cores with tensor-memory accumulators.
+//
+// One work item = (query token, KV head, group of <= 16 query heads) with up to
+// 2,048 selected keys (16 tiles of 128). Per item:
+//   1. QK^T, "swap-AB": for each tile of 128 gathered K rows (A, K-major, 128-byte
+//      swizzle) against the 16 head queries (B), tcgen05.mma writes a 128 x 16
+//      fp32 block of logits into tensor memory; all 16 blocks stay resident
+//      (256 TMEM columns), so the softmax needs no online rescaling at all;
+//   2. the epilogue warps (one TMEM lane = one key each) take the exact per-head
+//      maximum over every selected key, then form P = exp2(s - max) tile by
+//      tile and write it to shared memory as a K-major [16 heads x 128 keys]
+//      operand (BF16 hi + lo pair for a BF16 cache, FP16 for an FP16 cache);
+//   3. PV^T: for each tile of 128 gathered V rows, read MN-major (head dim
+//      contiguous) as the A operand, tcgen05.mma accumulates O^T[128 dims x 16
+//      heads] in tensor memory; the epilogue divides by the row sums and stores.
+// Four loader warps gather the selected rows with 16-byte cp.async straight
+// into the swizzled operand layout and signal a ring of shared stages; one
+// warp issues the MMAs and owns tensor memory. A persistent grid of one CTA per
+// SM walks the work items.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace dsa {
+
+namespace pf {
+constexpr int kThreads = 320;          // warp 0 MMA, warp 1 idle, 2-5 softmax, 6-9 loaders
+constexpr int kKeys = 128;             // keys per tile (MMA M for QK^T, K for PV^T)
+constexpr int kMaxTiles = 16;          // 2,048 selected keys
+constexpr int kStages = 5;
+constexpr uint32_t kTileBytes = kKeys * DSA_HEAD_DIM * 2;   // 32 KB: 2 column blocks of 16 KB
+constexpr uint32_t kBlockBytes = kKeys * 128;               // one 64-wide column block
+constexpr uint32_t kQBytes = 16 * DSA_HEAD_DIM * 2;         // 4 KB
+constexpr uint32_t kPBytes = 16 * kKeys * 2;                // 4 KB: [16 heads x 128 keys]
+constexpr int kLogitCols = kMaxTiles * 16;                  // 256
+constexpr int kOCol = kLogitCols;                           // O^T after the logits
+constexpr uint32_t kTmemCols = 512;
+
+struct Bars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t q_ready, logits_ready, o_ready, tmem_free;
+  uint64_t p_ready[2], p_free[2];
+  uint64_t done;
+  uint64_t grp;          // barrier of the 128 softmax threads
+  uint32_t tmem_base;
+  int abort_flag;
+  float red[2][4][16];   // cross-warp max / sum scratch
+};
+
+constexpr size_t kSmemBytes = 1024 + kStages * kTileBytes + kQBytes + 4 * kPBytes + sizeof(Bars);
+}  // namespace pf
+
+// Shared-memory descriptor with explicit leading/stride byte offsets and
+// 128-byte swizzle (K-major: stride = 8-row group pitch; MN-major: leading =
+// pitch of 64-element MN blocks, stride = 8-row K group pitch).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// kind::f16 instruction descriptor: f32 accumulate, A/B both BF16 (F16 = false)
+// or both FP16, A K-major or MN-major, B K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool f16, bool a_mn_major) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier of a thread group on an mbarrier whose count is the group size, with
+// the bounded wait (a named barrier could strand threads that gave up).
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t* phase, volatile int* abort_flag) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait_bounded(bar, *phase, abort_flag);
+  *phase ^= 1u;
+  return ok;
+}
+
+// Byte offset of element (row, col) in a K-major SW128 operand whose rows hold
+// `cols` 16-bit elements split in 64-element column blocks of `rows` * 128 B.
+__device__ __forceinline__ uint32_t sw128_off(int row, int col, int rows) {
+  const int blk = col >> 6, c = col & 63;
+  return static_cast<uint32_t>(blk * rows * 128 + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) +
+                               (c & 7) * 2);
+}
+
+struct PfItem {
+  int r, g, hg, keff, ntiles;
+};
+
+__device__ __forceinline__ PfItem pf_item(const AttnParams& p, long long it) {
+  PfItem w;
+  const int per_row = p.Hkv * p.HG;
+  w.r = static_cast<int>(it / per_row);
+  const int gh = static_cast<int>(it % per_row);
+  w.g = gh / p.HG;
+  w.hg = gh % p.HG;
+  const int b = w.r / p.S, s = w.r % p.S;
+  w.keff = min(p.topk, visible_len(p.lens.T[b], p.S, s));
+  w.ntiles = (w.keff + pf::kKeys - 1) / pf::kKeys;
+  return w;
+}
+
+template <bool F16>
+__global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel(const AttnParams p,
+                                                                                  long long n_items,
+                                                                                  uint32_t* status) {
+  using namespace pf;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sKV = base;                                 // kStages x 32 KB
+  uint8_t* sQ = sKV + kStages * kTileBytes;            // 4 KB
+  uint8_t* sP = sQ + kQBytes;                          // [2 buffers][hi, lo] x 4 KB
+  Bars* bars = reinterpret_cast<Bars*>(sP + 4 * kPBytes);
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars->full[i], 128);
+      mbar_init(&bars->empty[i], 1);
+    }
+    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->logits_ready, 1);
+    mbar_init(&bars->o_ready, 1);
+    mbar_init(&bars->tmem_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->p_ready[i], 128);
+      mbar_init(&bars->p_free[i], 1);
+    }
+    mbar_init(&bars->done, 1);
+    mbar_init(&bars->grp, 128);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&bars->tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const long long my_first = blockIdx.x;
+  const long long stride = gridDim.x;
+
+  if (warp >= 6) {
+    // ------------------------------------------------------------ loaders
+    const int lt = threadIdx.x - 192;    // 0..127: one key row per thread
+    long long seq = 0;                   // position in the ring (tiles issued)
+    long long arrived = 0;
+    const size_t kv_tok = static_cast<size_t>(p.Hkv) * DSA_HEAD_DIM;
+    const uint16_t* Kb = static_cast<const uint16_t*>(p.k);
+    const uint16_t* Vb = static_cast<const uint16_t*>(p.v);
+    bool ok = true;
+    for (long long it = my_first; it < n_items && ok; it += stride) {
+      const PfItem w = pf_item(p, it);
+      const int b = w.r / p.S;
+      const int32_t* idx_row = p.idx + static_cast<size_t>(w.r) * p.topk;
+      for (int pass = 0; pass < 2 && ok; ++pass) {            // K tiles, then V tiles
+        const uint16_t* src = pass == 0 ? Kb : Vb;
+        for (int t = 0; t < w.ntiles; ++t) {
+          const int st = static_cast<int>(seq % kStages);
+          if (seq >= kStages &&
+              !mbar_wait_bounded(&bars->empty[st], static_cast<uint32_t>(((seq / kStages) - 1) & 1),
+                                 abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int j = t * kKeys + lt;
+          int key = j < w.keff ? idx_row[j] : -1;
+          if (key >= p.lens.T[b]) key = -1;
+          const uint16_t* row = src + (static_cast<size_t>(b) * p.cap + (key < 0 ? 0 : key)) * kv_tok +
+                                static_cast<size_t>(w.g) * DSA_HEAD_DIM;
+          uint8_t* dst = sKV + st * kTileBytes;
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            cp_async16(dst + sw128_off(lt, c * 8, kKeys), row + c * 8, key >= 0);
+          cp_async_commit();
+          ++seq;
+          // signal the tile issued two groups ago
+          if (seq - arrived > 2) {
+            cp_async_wait<2>();
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->full[arrived % kStages]);
+            ++arrived;
+          }
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    while (arrived < seq) {
+      mbar_arrive(&bars->full[arrived % kStages]);
+      ++arrived;
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_f16(kKeys, 16, F16, false);
+      constexpr uint32_t id_pv = idesc_f16(DSA_HEAD_DIM, 16, F16, true);
+      long long seq = 0;
+      long long n = 0;   // items handled by this CTA
+      long long ptile = 0;
+      for (long long it = my_first; it < n_items; it += stride, ++n) {
+        const PfItem w = pf_item(p, it);
+        // the softmax warps must be done with the previous item's tensor memory
+        if (n > 0 && !mbar_wait_bounded(&bars->tmem_free, static_cast<uint32_t>((n - 1) & 1), abort_flag))
+          break;
+        if (!mbar_wait_bounded(&bars->q_ready, static_cast<uint32_t>(n & 1), abort_flag)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int t = 0; t < w.ntiles; ++t, ++seq) {
+          const int st = static_cast<int>(seq % kStages);
+          if (!mbar_wait_bounded(&bars->full[st], static_cast<uint32_t>((seq / kStages) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sKV + st * kTileBytes);
+          const uint32_t b0 = smem_u32(sQ);
+#pragma unroll
+          for (int kk = 0; kk < DSA_HEAD_DIM / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (16 * 128) + (kk & 3) * 32;
+            tc_mma_f16(tmem + t * 16, desc_sw128(a0 + koff, 16, 1024), desc_sw128(b0 + qoff, 16, 1024),
+                       id_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&bars->empty[st]);
+        }
+        if (!ok) break;
+        tc_commit(&bars->logits_ready);
+        for (int t = 0; t < w.ntiles; ++t, ++seq, ++ptile) {
+          const int st = static_cast<int>(seq % kStages);
+          if (!mbar_wait_bounded(&bars->full[st], static_cast<uint32_t>((seq / kStages) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int pb = static_cast<int>(ptile & 1);
+          if (!mbar_wait_bounded(&bars->p_ready[pb], static_cast<uint32_t>((ptile >> 1) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t v0 = smem_u32(sKV + st * kTileBytes);
+          const uint32_t ph = smem_u32(sP + (2 * pb) * kPBytes);
+          const uint32_t pl = ph + kPBytes;
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint32_t voff = kk * 16 * 128;                       // 16 keys of both blocks
+            const uint32_t poff = (kk >> 2) * (16 * 128) + (kk & 3) * 32;
+            const uint64_t adesc = desc_sw128(v0 + voff, kBlockBytes, 1024);
+            tc_mma_f16(tmem + kOCol, adesc, desc_sw128(ph + poff, 16, 1024), id_pv,
+                       (t > 0 || kk > 0) ? 1u : 0u);
+            if constexpr (!F16)
+              tc_mma_f16(tmem + kOCol, adesc, desc_sw128(pl + poff, 16, 1024), id_pv, 1u);
+          }
+          tc_commit(&bars->empty[st]);
+          tc_commit(&bars->p_free[pb]);
+        }
+        if (!ok) break;
+        tc_commit(&bars->o_ready);
+      }
+      tc_commit(&bars->done);
+      long long t0 = clock64();
+      while (!mbar_try_wait(&bars->done, 0) && clock64() - t0 < kWaitBudgetCycles) {
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int et = threadIdx.x - 64;          // 0..127
+    const int quarter = warp & 3;
+    const int key_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = p.scale_log2;
+    long long n = 0, ptile = 0;
+    uint32_t gphase = 0;
+
+    auto load_q = [&](const PfItem& w) {
+      // [16 heads x 128 dims] K-major SW128; heads past the group are zero
+      const int h0 = w.g * p.G + w.hg * 16;
+      const int nh = min(16, p.G - w.hg * 16);
+      for (int i = et; i < 16 * 16; i += 128) {
+        const int h = i >> 4, ch = i & 15;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (h < nh) {
+          const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
+                                 (static_cast<size_t>(w.r) * p.Hq + h0 + h) * DSA_HEAD_DIM + ch * 8;
+          v = *reinterpret_cast<const uint4*>(qrow);
+          if (F16 && p.q_dtype == DSA_BF16) {
+            const __nv_bfloat16* bsrc = reinterpret_cast<const __nv_bfloat16*>(&v);
+            __half hv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hv[e] = __float2half_rn(__bfloat162float(bsrc[e]));
+            v = *reinterpret_cast<const uint4*>(hv);
+          }
+        }
+        *reinterpret_cast<uint4*>(sQ + sw128_off(h, ch * 8, 16)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->q_ready);
+    };
+
+    long long it = my_first;
+    if (it < n_items) load_q(pf_item(p, it));
+    for (; it < n_items; it += stride, ++n) {
+      const PfItem w = pf_item(p, it);
+      if (!mbar_wait_bounded(&bars->logits_ready, static_cast<uint32_t>(n & 1), abort_flag)) break;
+      tc_fence_after();
+      // the query buffer is free once the logits are in: stage the next item's
+      if (it + stride < n_items) load_q(pf_item(p, it + stride));
+
+      // ---- exact per-head max over all selected keys
+      float mx[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) mx[h] = -INFINITY;
+      for (int t = 0; t < w.ntiles; ++t) {
+        float v[16];
+        tmem_ld16(tmem + lane_addr + t * 16, v);
+        tmem_ld_wait();
+        if (t * kKeys + key_in_tile < w.keff) {
+#pragma unroll
+          for (int h = 0; h < 16; ++h) mx[h] = fmaxf(mx[h], v[h]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) bars->red[0][warp - 2][h] = mx[h];
+      }
+      if (!group_sync(&bars->grp, &gphase, abort_flag)) break;
+      float M[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        M[h] = fmaxf(fmaxf(bars->red[0][0][h], bars->red[0][1][h]),
+                     fmaxf(bars->red[0][2][h], bars->red[0][3][h])) * c;
+
+      // ---- P tiles
+      float lsum[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) lsum[h] = 0.0f;
+      for (int t = 0; t < w.ntiles; ++t, ++ptile) {
+        const int pb = static_cast<int>(ptile & 1);
+        if (ptile >= 2 &&
+            !mbar_wait_bounded(&bars->p_free[pb], static_cast<uint32_t>(((ptile >> 1) - 1) & 1), abort_flag))
+          break;
+        float v[16];
+        tmem_ld16(tmem + lane_addr + t * 16, v);
+        tmem_ld_wait();
+        const bool valid = t * kKeys + key_in_tile < w.keff;
+        uint8_t* ph = sP + (2 * pb) * kPBytes;
+        uint8_t* pl = ph + kPBytes;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float pv = valid ? exp2f(fmaf(v[h], c, -M[h])) : 0.0f;
+          lsum[h] += pv;
+          const uint32_t off = sw128_off(h, key_in_tile, 16);
+          if constexpr (F16) {
+            *reinterpret_cast<__half*>(ph + off) = __float2half_rn(pv);
+          } else {
+            const __nv_bfloat16 hi = __float2bfloat16_rn(pv);
+            *reinterpret_cast<__nv_bfloat16*>(ph + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(pl + off) = __float2bfloat16_rn(pv - __bfloat162float(hi));
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->p_ready[pb]);
+      }
+      // ---- row sums
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) bars->red[1][warp - 2][h] = lsum[h];
+      }
+      if (!group_sync(&bars->grp, &gphase, abort_flag)) break;
+      // ---- O^T: TMEM lane = head dim, columns = heads
+      if (!mbar_wait_bounded(&bars->o_ready, static_cast<uint32_t>(n & 1), abort_flag)) break;
+      tc_fence_after();
+      float o[16];
+      tmem_ld16(tmem + lane_addr + kOCol, o);
+      tmem_ld_wait();
+      const int h0 = w.g * p.G + w.hg * 16;
+      const int nh = min(16, p.G - w.hg * 16);
+      const int d = key_in_tile;   // lane of the O^T accumulator
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        if (h >= nh) break;
+        const float L = bars->red[1][0][h] + bars->red[1][1][h] + bars->red[1][2][h] + bars->red[1][3][h];
+        const size_t oi = (static_cast<size_t>(w.r) * p.Hq + h0 + h) * DSA_HEAD_DIM + d;
+        const float val = o[h] / L;
+        if (p.out_dtype == DSA_BF16) static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(val);
+        else if (p.out_dtype == DSA_FP16) static_cast<__half*>(p.out)[oi] = __float2half_rn(val);
+        else static_cast<float*>(p.out)[oi] = val;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->tmem_free);
+      // red[] reads done before the next item reuses it
+      if (!group_sync(&bars->grp, &gphase, abort_flag)) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && bars->abort_flag) atomicOr(status, kDevTimeout);
+}
+
+bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin) {
+  return (kv_dtype == DSA_BF16 || kv_dtype == DSA_FP16) && p.topk <= pf::kMaxTiles * pf::kKeys &&
+         pf::kSmemBytes <= smem_optin;
+}
+
+cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, uint32_t* status,
+                              cudaStream_t stream) {
+  const long long n_items = static_cast<long long>(p.B) * p.S * p.Hkv * p.HG;
+  const int grid = static_cast<int>(n_items < sms ? n_items : sms);
+  if (kv_dtype == DSA_FP16) {
+    auto k = sparse_attn_prefill_tc_kernel<true>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(pf::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    k<<<grid, pf::kThreads, pf::kSmemBytes, stream>>>(p, n_items, status);
+  } else {
+    auto k = sparse_attn_prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(pf::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    k<<<grid, pf::kThreads, pf::kSmemBytes, stream>>>(p, n_items, status);
+  }
+  return cudaPeekAtLastError();
+}
+
+}  // namespace dsa

@@ -222,8 +222,6 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   float l_run[2] = {0.0f, 0.0f};             // thread-partial sums
 
   const int my_tiles = ntiles > warp ? (ntiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
-  if (my_tiles > 0) issue_tile(0, 0);
-  cp_async_commit();
   // ---- query fragments (A operand of QK^T), resident for the whole CTA
   uint32_t qa[kD / 16][4];
   {
@@ -239,6 +237,10 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       qa[kk][3] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c + 8) : 0u;
     }
   }
+  pdl_wait();       // the selected indices come from the previous kernel
+  pdl_trigger();
+  if (my_tiles > 0) issue_tile(0, 0);
+  cp_async_commit();
 
   for (int it = 0; it < my_tiles; ++it) {
     const int st = it & 1;
@@ -492,9 +494,8 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
   auto kern = sparse_attn_kernel<KV, Q_F16, OUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
-  kern<<<grid, kAttnThreads, kAttnSmem, stream>>>(p);
-  return cudaPeekAtLastError();
+  return launch_kernel(kern, dim3(p.nsplit, p.Hkv * p.HG, p.B * p.S), dim3(kAttnThreads), kAttnSmem,
+                       stream, true, p);
 }
 
 template <int KV, bool Q_F16>

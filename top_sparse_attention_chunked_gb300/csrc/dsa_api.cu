@@ -337,7 +337,7 @@ int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, co
 
 int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
              const float* scores, int32_t* idx, void* ws, bool hist_ready, bool prefer_rows,
-             cudaStream_t st) {
+             bool after_kernel, cudaStream_t st) {
   TopkParams tp;
   tp.scores = scores;
   tp.idx = idx;
@@ -360,7 +360,7 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
   const int row_max = topk_row_max_len(di.smem_optin);
   if (!hist_ready && prefer_rows && d.max_n <= row_max) {
     timing_before(DSA_KERNEL_TOPK_ROW, st);
-    e = launch_topk_row(tp, d.max_n, di.smem_optin, st);
+    e = launch_topk_row(tp, d.max_n, di.smem_optin, after_kernel, st);
     timing_after(DSA_KERNEL_TOPK_ROW, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-k row launch");
     return DSA_OK;
@@ -472,7 +472,7 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
   const bool decode = (op == DSA_OP_DECODE);
   rc = run_indexer(p, d, di, qI, w, kI, scores, decode ? at<uint32_t>(ws, L.hist) : nullptr, status, st);
   if (rc) return rc;
-  rc = run_topk(p, d, di, L, scores, idx, ws, decode, !decode, st);
+  rc = run_topk(p, d, di, L, scores, idx, ws, decode, !decode, true, st);
   if (rc) return rc;
   return run_attention(p, d, di, L, q, k, v, ks, vs, idx, out, ws, !decode, st);
 }
@@ -561,7 +561,7 @@ int dsa_topk(const dsa_problem* p, const float* scores, int32_t* idx, void* ws, 
   if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
   // few rows: spread each row over its chunks; many short rows: one CTA per row
   const bool prefer_rows = d.rows >= 2 * di.sms;
-  return run_topk(p, d, di, L, scores, idx, ws, false, prefer_rows, st);
+  return run_topk(p, d, di, L, scores, idx, ws, false, prefer_rows, false, st);
 }
 
 int dsa_sparse_attn_decode(const dsa_problem* p, const void* q, const void* qI, const float* w,

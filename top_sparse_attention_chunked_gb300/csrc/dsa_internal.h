@@ -10,6 +10,25 @@
 
 namespace dsa {
 
+// Launch `kern` on `stream`; with `pdl` the launch may overlap the tail of the
+// previous kernel in the stream (the kernel calls pdl_wait() before reading
+// what that kernel wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kChunk = DSA_CHUNK;          // 2,048-key chunks (indexer + top-k)
 constexpr int kHistBits = 11;              // first radix digit: top 11 key bits
 constexpr int kHistBins = 1 << kHistBits;  // 2,048 bins per query row
@@ -62,7 +81,8 @@ struct TopkParams {
 
 cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream);
 cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream);
-cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit,
+// `pdl`: launched right after another kernel of the same call
+cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,
                             cudaStream_t stream);
 // Longest row the shared-memory whole-row select handles.
 int topk_row_max_len(size_t smem_limit);

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -363,8 +364,7 @@ static cudaError_t launch_n(const IndexerParams& p, const CUtensorMap& tm_kI,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kIdxThreads, smem, stream>>>(tm_kI, tm_qI, p, stages);
-  return cudaPeekAtLastError();
+  return launch_kernel(kern, grid, dim3(kIdxThreads), smem, stream, false, tm_kI, tm_qI, p, stages);
 }
 
 cudaError_t launch_indexer(const IndexerParams& p, const CUtensorMap& tm_kI,

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
 
   if (warp >= 6) {
     // ------------------------------------------------------------ loaders
+    pdl_wait();      // the selected indices come from the previous kernel
     const int lt = threadIdx.x - 192;    // 0..127: one key row per thread
     long long seq = 0;                   // position in the ring (tiles issued)
     long long arrived = 0;
@@ -441,15 +442,16 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, uint32
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::kSmemBytes));
     if (e != cudaSuccess) return e;
-    k<<<grid, pf::kThreads, pf::kSmemBytes, stream>>>(p, n_items, status);
+    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, p, n_items,
+                         status);
   } else {
     auto k = sparse_attn_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::kSmemBytes));
     if (e != cudaSuccess) return e;
-    k<<<grid, pf::kThreads, pf::kSmemBytes, stream>>>(p, n_items, status);
+    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, p, n_items,
+                         status);
   }
-  return cudaPeekAtLastError();
 }
 
 }  // namespace dsa

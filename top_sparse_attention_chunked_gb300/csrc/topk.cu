@@ -59,6 +59,7 @@ __device__ __forceinline__ void hist_add_warp(uint32_t* h, uint32_t bin) {
 __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const TopkParams p) {
   __shared__ uint32_t h[kHistBins];
   const int rl = blockIdx.y, r = p.row0 + rl, c = blockIdx.x;
+  pdl_trigger();
   const RowInfo ri = row_info(p, r);
   const int t0 = c * kChunk;
   if (t0 >= ri.n) return;
@@ -163,8 +164,11 @@ __global__ void __launch_bounds__(kSelThreads) topk_chunk_select_kernel(const To
   __shared__ int s_d;
   __shared__ uint32_t s_above, s_cnt;
   __shared__ int s_last;
+  __shared__ uint32_t s_cbase;
 
   const int rl = blockIdx.y, r = p.row0 + rl, c = blockIdx.x;
+  pdl_wait();      // scores and histograms come from the previous kernel
+  pdl_trigger();
   const RowInfo ri = row_info(p, r);
   const int nch = (ri.n + kChunk - 1) / kChunk;
   if (c >= nch) return;
@@ -180,13 +184,20 @@ __global__ void __launch_bounds__(kSelThreads) topk_chunk_select_kernel(const To
   const uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
   const bool take_all = (need == s_cnt);
 
-  // scan the chunk: bitmap words for sure keys, candidates for the threshold bin
+  // scan the chunk: bitmap words for sure keys, candidates for the threshold
+  // bin. Each warp covers kChunk / 16 = 128 keys in 4 groups of 32; the
+  // candidate slots of the whole CTA are reserved with one atomic.
   const float* row = p.scores + static_cast<size_t>(r) * p.cap;
   uint32_t* bm = p.bitmap + static_cast<size_t>(rl) * p.bitmap_stride;
   unsigned long long* cl = p.cands + static_cast<size_t>(rl) * p.cand_stride;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t_end = min(ri.n, (c + 1) * kChunk);
-  for (int base = c * kChunk + warp * 32; base < (c + 1) * kChunk; base += kSelThreads) {
+  constexpr int kGroups = kChunk / kSelThreads;   // 4
+  uint32_t keys[kGroups], cmask[kGroups];
+  uint32_t wcount = 0;
+#pragma unroll
+  for (int gi = 0; gi < kGroups; ++gi) {
+    const int base = c * kChunk + gi * kSelThreads + warp * 32;
     const int t = base + lane;
     bool sel = false, cand = false;
     uint32_t key = 0;
@@ -198,16 +209,27 @@ __global__ void __launch_bounds__(kSelThreads) topk_chunk_select_kernel(const To
     }
     const uint32_t word = __ballot_sync(0xffffffffu, sel);
     if (lane == 0 && base < ri.n) bm[base >> 5] = word;
-    const uint32_t cm = __ballot_sync(0xffffffffu, cand);
-    if (cm) {
-      uint32_t wbase = 0;
-      if (lane == 0) wbase = atomicAdd(&p.cand_count[rl], static_cast<uint32_t>(__popc(cm)));
-      wbase = __shfl_sync(0xffffffffu, wbase, 0);
-      if (cand) {
-        const uint32_t rank = __popc(cm & ((1u << lane) - 1u));
-        cl[wbase + rank] = (static_cast<unsigned long long>(key) << 32) |
-                           static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(t));
+    keys[gi] = key;
+    cmask[gi] = __ballot_sync(0xffffffffu, cand);
+    wcount += __popc(cmask[gi]);
+  }
+  uint32_t ctotal;
+  const uint32_t wbefore =
+      block_exclusive_scan<kSelThreads>(lane == 0 ? wcount : 0u, warp_tot, &ctotal);
+  if (threadIdx.x == 0 && ctotal) s_cbase = atomicAdd(&p.cand_count[rl], ctotal);
+  __syncthreads();
+  if (ctotal) {
+    uint32_t pos = s_cbase + __shfl_sync(0xffffffffu, wbefore, 0);
+#pragma unroll
+    for (int gi = 0; gi < kGroups; ++gi) {
+      const uint32_t cm = cmask[gi];
+      if ((cm >> lane) & 1u) {
+        const int t = c * kChunk + gi * kSelThreads + warp * 32 + lane;
+        cl[pos + __popc(cm & ((1u << lane) - 1u))] =
+            (static_cast<unsigned long long>(keys[gi]) << 32) |
+            static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(t));
       }
+      pos += __popc(cm);
     }
   }
 
@@ -254,6 +276,8 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
   __shared__ uint32_t s_above, s_cnt;
 
   const int r = blockIdx.x;
+  pdl_wait();      // scores come from the previous kernel
+  pdl_trigger();
   const RowInfo ri = row_info(p, r);
   const int n = ri.n;
   uint32_t* h = skeys + ((n + 3) & ~3);
@@ -332,9 +356,8 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream) {
-  dim3 grid(p.nchunks, p.nrows);
-  topk_hist_kernel<<<grid, kHistThreads, 0, stream>>>(p);
-  return cudaPeekAtLastError();
+  return launch_kernel(topk_hist_kernel, dim3(p.nchunks, p.nrows), dim3(kHistThreads), 0, stream,
+                       false, p);
 }
 
 cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
@@ -343,12 +366,11 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(p.nchunks, p.nrows);
-  topk_chunk_select_kernel<<<grid, kSelThreads, smem, stream>>>(p);
-  return cudaPeekAtLastError();
+  return launch_kernel(topk_chunk_select_kernel, dim3(p.nchunks, p.nrows), dim3(kSelThreads), smem,
+                       stream, true, p);
 }
 
-cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit,
+cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,
                             cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>((max_n + 3) & ~3) + kHistBins) * sizeof(uint32_t);
   if (smem + 1024 > smem_limit) return cudaErrorInvalidValue;
@@ -356,8 +378,7 @@ cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  topk_row_kernel<<<p.B * p.S, kRowThreads, smem, stream>>>(p);
-  return cudaPeekAtLastError();
+  return launch_kernel(topk_row_kernel, dim3(p.B * p.S), dim3(kRowThreads), smem, stream, pdl, p);
 }
 
 }  // namespace dsa

@@ -135,6 +135,7 @@ def _topk_case(dsa, B, S, T, cap, k, kind, seed):
 @pytest.mark.parametrize("B,S,T,cap,k", [
     (2, 3, [5000, 3000], 5000, 100), (1, 1, 4096, 4096, 512), (2, 2, [2049, 2], 4100, 2048),
     (1, 4, 70, 80, 64), (1, 1, 1, 1, 1), (1, 2, 9000, 9000, 8999),
+    (1, 1, 600000, 600000, 2048),   # longer than the cluster select: global merge path
 ])
 def test_topk_bitexact_chunked(dsa, kind, B, S, T, cap, k):
     _topk_case(dsa, B, S, T, cap, k, kind, seed=hash((kind, B, S, k)) & 0xFFFF)

@@ -23,6 +23,7 @@
 // enter PV as FP16 for an FP16 cache and as a BF16 hi+lo pair otherwise, so
 // P keeps 16 significant bits. INT8 codes are exact in BF16/FP16; k_scale
 // multiplies the logit after the dot product and v_scale is folded into P.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -157,8 +158,9 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   const int T = p.lens.T[b];
   const int keff = min(p.topk, visible_len(T, p.S, s));
   const int split_begin = blockIdx.x * p.split_keys;
-  if (split_begin >= keff) return;
-  const int split_len = min(p.split_keys, keff - split_begin);
+  // in a cluster every split takes part in the combine, empty or not
+  if (split_begin >= keff && !p.cluster) return;
+  const int split_len = max(0, min(p.split_keys, keff - split_begin));
   const int nreal = (keff + p.split_keys - 1) / p.split_keys;
   const int ntiles = (split_len + kTileKeys - 1) / kTileKeys;
 
@@ -442,6 +444,53 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + d, acc[row] / sML[kAttnRows + row]);
     return;
   }
+  if (p.cluster) {
+    // ---- split combine inside the thread-block cluster: every split CTA
+    // publishes its state in its own shared memory, then each CTA merges one
+    // slice of the output columns from all peers' shared memory.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __syncthreads();   // ws reads above are done
+    float* pubO = ws;  // [16][128]
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row) pubO[row * kD + d] = acc[row];
+    cluster.sync();
+    const int ns = p.nsplit;
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int cols = kD / ns;                      // ns divides 128 (power of two)
+    for (int o = threadIdx.x; o < kAttnRows * cols; o += kAttnThreads) {
+      const int row = o / cols, col = rank * cols + o % cols;
+      if (row >= nh) continue;
+      float mv[16], lv[16], ov[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (q < ns) {
+          const float* peerML = cluster.map_shared_rank(sML, q);
+          const float* peerO = cluster.map_shared_rank(pubO, q);
+          mv[q] = peerML[row];
+          lv[q] = peerML[kAttnRows + row];
+          ov[q] = peerO[row * kD + col];
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (q < ns) M = fmaxf(M, mv[q]);
+      float L = 0.0f, O = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (q < ns) {
+          float f1, f2;
+          exp2_pair(mv[q] - M, &f1, &f2);
+          L += lv[q] * f1 * f2;
+          O += ov[q] * f1 * f2;
+        }
+      }
+      store_out<OUT>(p.out, (out_row + row) * kD + col, O / L);
+    }
+    cluster.sync();    // peers may still be reading this CTA's shared memory
+    return;
+  }
   float* part = p.partial + ((static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit + blockIdx.x) *
                                 kPartialFloats;
   if (d < kAttnRows) {
@@ -494,8 +543,39 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
   auto kern = sparse_attn_kernel<KV, Q_F16, OUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, dim3(p.nsplit, p.Hkv * p.HG, p.B * p.S), dim3(kAttnThreads), kAttnSmem,
-                       stream, true, p);
+  const dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
+  if (!p.cluster)
+    return launch_kernel(kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true, p);
+  if (p.nsplit > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (p.nsplit > 8) {
+    // a 16-CTA cluster is not portable: if it cannot be placed, merge the
+    // splits through global memory instead
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
+      cudaGetLastError();
+      AttnParams q = p;
+      q.cluster = 0;
+      return launch_kernel(kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true, q);
+    }
+  }
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int KV, bool Q_F16>

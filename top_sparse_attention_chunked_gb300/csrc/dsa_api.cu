@@ -196,6 +196,10 @@ void choose_split(const dsa_problem* p, const Derived& d, int sms, int* split_ke
     const int cap = ceil_div(d.kmax, 64);
     s = s < cap ? s : cap;
     if (s < 1) s = 1;
+    // a power of two, so the cluster combine splits the 128 columns evenly
+    int s2 = 1;
+    while (s2 * 2 <= s) s2 *= 2;
+    s = s2;
     sk = ceil_div(ceil_div(d.kmax, s), 16) * 16;
     const int sk_min = ceil_div(ceil_div(d.kmax, kAttnMaxSplits), 16) * 16;
     if (sk < sk_min) sk = sk_min;
@@ -378,7 +382,10 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
       if (e != cudaSuccess) return cuda_fail(e, "top-k histogram launch");
     }
     timing_before(DSA_KERNEL_TOPK_SELECT, st);
-    e = launch_topk_chunk_select(tp, st);
+    if (topk_cluster_ctas(d.max_n) > 0)
+      e = launch_topk_cluster_select(tp, d.max_n, true, st);
+    else
+      e = launch_topk_chunk_select(tp, st);
     timing_after(DSA_KERNEL_TOPK_SELECT, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-k select launch");
   }
@@ -410,6 +417,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   if (ap.nsplit > kAttnMaxSplits)
     return fail(DSA_ERR_UNSUPPORTED, "attn_split_keys %d gives %d splits (max %d)",
                 p->attn_split_keys, ap.nsplit, kAttnMaxSplits);
+  ap.cluster = (ap.nsplit == 2 || ap.nsplit == 4 || ap.nsplit == 8 || ap.nsplit == 16) ? 1 : 0;
   if (ap.nsplit > splits_bound(p, d))
     return fail(DSA_ERR_UNSUPPORTED, "device has more SMs than the workspace bound assumes");
   const float scale = p->softmax_scale > 0.0f ? p->softmax_scale

@@ -84,6 +84,13 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream);
 // `pdl`: launched right after another kernel of the same call
 cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,
                             cudaStream_t stream);
+// Cluster select: up to kTopkClusterMax CTAs per row (a portable cluster),
+// each holding a slice of at most kTopkClusterSlice keys in shared memory.
+constexpr int kTopkClusterMax = 8;
+constexpr int kTopkClusterSlice = 32768;
+int topk_cluster_ctas(int max_n);   // 0 if the row is too long for it
+cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
+                                       cudaStream_t stream);
 // Longest row the shared-memory whole-row select handles.
 int topk_row_max_len(size_t smem_limit);
 
@@ -100,6 +107,7 @@ struct AttnParams {
   uint32_t* ticket;        // [B*S*Hkv*HG] zeroed when nsplit > 1
   int B, S, Hq, Hkv, G, HG, cap, topk;
   int split_keys, nsplit;
+  int cluster;             // nsplit in {2,4,8,16}: splits merged inside a thread-block cluster
   int q_dtype, out_dtype;
   float scale_log2;        // softmax_scale * log2(e)
   SeqLens lens;

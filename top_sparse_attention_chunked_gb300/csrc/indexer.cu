@@ -33,7 +33,9 @@
 
 namespace dsa {
 
-constexpr int kIdxThreads = 192;
+constexpr int kIdxThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
+constexpr int kIdxEpiThreads = 256;
+constexpr int kMaxAcc = 4;
 constexpr int kIdxMaxStages = 8;
 constexpr uint32_t kATileBytes = kKeyTile * DSA_IDX_DIM * 2;   // 16 KB
 
@@ -83,8 +85,10 @@ template <int N>
 struct IdxCfg {
   static constexpr int QB = N / 16;
   static constexpr uint32_t kBBytes = N * DSA_IDX_DIM * 2;
-  static constexpr uint32_t kTmemCols = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128
-                                      : (2 * N <= 256) ? 256 : 512;
+  // accumulator buffers in tensor memory: 4 for narrow tiles, 2 for wide ones
+  static constexpr int NACC = N <= 64 ? 4 : 2;
+  static constexpr uint32_t kTmemCols = (NACC * N <= 32) ? 32 : (NACC * N <= 64) ? 64
+                                      : (NACC * N <= 128) ? 128 : (NACC * N <= 256) ? 256 : 512;
   // queries whose accumulator columns are read per tcgen05.ld batch
   static constexpr int QG = QB < 4 ? QB : 4;
 };
@@ -93,7 +97,7 @@ struct IdxBarriers {
   uint64_t full[kIdxMaxStages];
   uint64_t empty[kIdxMaxStages];
   uint64_t bfull[2], bempty[2];
-  uint64_t accfull[2], accempty[2];
+  uint64_t accfull[kMaxAcc], accempty[kMaxAcc];
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
@@ -109,7 +113,7 @@ __host__ __device__ inline size_t indexer_smem_layout(int N, bool with_hist, int
   // with histograms a CTA owns one sequence's single block
   o += (with_hist ? 1ull : 2ull) * N * DSA_IDX_DIM * 2;
   *off_w = o;   // one copy of the block's head weights per epilogue warp
-  o += 4ull * QB * 16 * sizeof(float);
+  o += 8ull * QB * 16 * sizeof(float);
   o = (o + 15) & ~size_t(15);
   *off_hist = o;
   if (with_hist) o += static_cast<size_t>(QB) * kHistBins * sizeof(uint32_t);
@@ -165,8 +169,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->bfull[i], 1);
       mbar_init(&bars->bempty[i], 1);
+    }
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&bars->accfull[i], 1);
-      mbar_init(&bars->accempty[i], 4);
+      mbar_init(&bars->accempty[i], 4);   // the 4 warps of one epilogue group
     }
     mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
@@ -241,8 +247,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         const int s = static_cast<int>(i % stages);
         if (!mbar_wait_bounded(&bars->full[s], static_cast<uint32_t>((i / stages) & 1), abort_flag))
           break;
-        const int a = static_cast<int>(i & 1);
-        if (i >= 2 && !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i >> 1) - 1) & 1), abort_flag))
+        const int a = static_cast<int>(i % C::NACC);
+        if (i >= C::NACC &&
+            !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag))
           break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * N;
@@ -262,7 +269,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int et = threadIdx.x - 64;            // 0 .. 127
+    // Two groups of 4 warps take alternate tiles (group = tile index parity);
+    // each group covers all 4 TMEM lane quarters.
+    const int et = threadIdx.x - 64;            // 0 .. 255
+    const int group = (warp - 2) >> 2;
     const int quarter = warp & 3;               // TMEM lanes 32*quarter ..
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     float* wv_warp = sW + (warp - 2) * QB * DSA_IDX_HEADS;
@@ -286,8 +296,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         pb = c.b;
         pqb = c.qb;
       }
-      const int a = static_cast<int>(i & 1);
-      if (!mbar_wait_bounded(&bars->accfull[a], static_cast<uint32_t>((i >> 1) & 1), abort_flag)) break;
+      if ((i & 1) != group) {
+        advance_unit(p, c);
+        continue;
+      }
+      const int a = static_cast<int>(i % C::NACC);
+      if (!mbar_wait_bounded(&bars->accfull[a], static_cast<uint32_t>((i / C::NACC) & 1), abort_flag)) break;
       tc_fence_after();
       const int t = c.kt * kKeyTile + quarter * 32 + lane;
       const int T = p.lens.T[c.b];
@@ -323,13 +337,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
     if constexpr (HIST) {
       // one query block per CTA here (see the unit ranges above)
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kIdxEpiThreads);
       if (count > 0) {
         for (int j = 0; j < QB; ++j) {
           const int s = j;
           if (s >= p.S) break;
           uint32_t* g = p.hist + static_cast<size_t>(hist_b * p.S + s) * kHistBins;
-          for (int bin = et; bin < kHistBins; bin += 128) {
+          for (int bin = et; bin < kHistBins; bin += kIdxEpiThreads) {
             const uint32_t v = sHist[j * kHistBins + bin];
             if (v) atomicAdd(g + bin, v);
           }

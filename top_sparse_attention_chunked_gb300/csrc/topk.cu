@@ -22,6 +22,8 @@
 //      shared memory and emits with block scans.
 //
 // Keys: float_key() maps fp32 to an order-preserving uint32 (-0.0 == +0.0).
+#include <cooperative_groups.h>
+
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 #include "sm100_ptx.cuh"
@@ -368,6 +370,160 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   return launch_kernel(topk_chunk_select_kernel, dim3(p.nchunks, p.nrows), dim3(kSelThreads), smem,
                        stream, true, p);
+}
+
+// ---------------------------------------------------------------------------
+// 2b. cluster select: one thread-block cluster of up to 8 CTAs per row. Each
+// CTA holds a contiguous slice of the row's keys in shared memory. After the
+// threshold bin from the row histogram, the clusters refine the exact
+// threshold composite (key << 32 | ~index) 8 bits at a time, summing every
+// CTA's digit histogram through distributed shared memory; then each CTA
+// emits its own slice in ascending order at the offset given by the peers'
+// selected counts. No global scratch beyond the histogram, no serial tail.
+// ---------------------------------------------------------------------------
+constexpr int kClThreads = 512;
+
+__global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const TopkParams p,
+                                                                           int slice) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ uint32_t skeys[];            // this CTA's slice of keys
+  __shared__ uint32_t h[kHistBins];              // row histogram, then 8-bit digit totals
+  __shared__ uint32_t hd[256];                   // this CTA's digit histogram
+  __shared__ uint32_t warp_tot[32];
+  __shared__ int s_d;
+  __shared__ uint32_t s_above, s_cnt;
+  __shared__ uint32_t s_count;                   // keys this CTA selects
+
+  const int rl = blockIdx.y, r = p.row0 + rl;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int ncta = static_cast<int>(cluster.num_blocks());
+  pdl_wait();      // scores and the histogram come from the previous kernel
+  pdl_trigger();
+  const RowInfo ri = row_info(p, r);
+  const int t0 = rank * slice;
+  const int t1 = min(ri.n, t0 + slice);
+  const int m = max(0, t1 - t0);
+  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
+  for (int i = threadIdx.x; i < m; i += kClThreads) skeys[i] = float_key(row[t0 + i]);
+  const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) h[i] = __ldcg(gh + i);
+  if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; s_count = 0; }
+  __syncthreads();
+  find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
+                                   &s_above, &s_cnt);
+  const uint32_t bin = static_cast<uint32_t>(s_d);
+  uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
+  bool all = (need == s_cnt);
+  unsigned long long prefix = static_cast<unsigned long long>(bin) << 53;
+  unsigned long long mask = ~0ull << 53;
+  const int mround = ((m + 31) / 32) * 32;
+  int hi = 52;
+  while (!all && hi >= 0) {
+    const int w = hi + 1 < 8 ? hi + 1 : 8;
+    const int sh = hi - w + 1;
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < 256; i += kClThreads) hd[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < mround; i += kClThreads) {
+      uint32_t dg = 0xFFFFFFFFu;
+      if (i < m) {
+        const unsigned long long cc = (static_cast<unsigned long long>(skeys[i]) << 32) |
+                                      (0xFFFFFFFFull - static_cast<uint32_t>(t0 + i));
+        if ((cc & mask) == prefix) dg = static_cast<uint32_t>(cc >> sh) & dm;
+      }
+      hist_add_warp(hd, dg);
+    }
+    cluster.sync();                              // every CTA's digit histogram is complete
+    if (threadIdx.x < 256) {
+      uint32_t tot = 0;
+      for (int q = 0; q < ncta; ++q) tot += cluster.map_shared_rank(hd, q)[threadIdx.x];
+      h[threadIdx.x] = tot;
+    }
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+    __syncthreads();
+    find_threshold_digit<kClThreads>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
+    need -= s_above;
+    prefix |= static_cast<unsigned long long>(s_d) << sh;
+    mask |= static_cast<unsigned long long>(dm) << sh;
+    all = (s_cnt == need);
+    cluster.sync();                              // peers are done reading hd
+    hi -= w;
+  }
+  // selected: top 11 bits above the threshold bin, or in it with the
+  // determined composite bits at or above the threshold prefix
+  auto selected = [&](int i) -> bool {
+    const uint32_t key = skeys[i];
+    const uint32_t kb = key >> (32 - kHistBits);
+    if (kb != bin) return kb > bin;
+    const unsigned long long cc = (static_cast<unsigned long long>(key) << 32) |
+                                  (0xFFFFFFFFull - static_cast<uint32_t>(t0 + i));
+    return (cc & mask) >= prefix;
+  };
+  uint32_t mine = 0;
+  for (int i = threadIdx.x; i < m; i += kClThreads) mine += selected(i) ? 1u : 0u;
+  uint32_t total;
+  block_exclusive_scan<kClThreads>(mine, warp_tot, &total);
+  if (threadIdx.x == 0) s_count = total;
+  cluster.sync();                                // every CTA's count is published
+  uint32_t base = 0;
+  for (int q = 0; q < rank; ++q) base += *cluster.map_shared_rank(&s_count, q);
+  // emit this slice in ascending order: tiles of 4 consecutive keys per thread
+  int32_t* out = p.idx + static_cast<size_t>(r) * p.k;
+  for (int tile = 0; tile < m; tile += 4 * kClThreads) {
+    const int i0 = tile + 4 * threadIdx.x;
+    uint32_t sel = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i0 + j < m && selected(i0 + j)) sel |= 1u << j;
+    uint32_t tot;
+    uint32_t pos = base + block_exclusive_scan<kClThreads>(__popc(sel), warp_tot, &tot);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((sel >> j) & 1u) {
+        if (pos < static_cast<uint32_t>(ri.keff)) out[pos] = t0 + i0 + j;
+        ++pos;
+      }
+    base += tot;
+  }
+  if (rank == 0)
+    for (int i = ri.keff + threadIdx.x; i < p.k; i += kClThreads) out[i] = -1;
+  cluster.sync();                                // peers may still read this CTA's s_count
+}
+
+// CTAs per row for the cluster select (0: the row is too long for it).
+int topk_cluster_ctas(int max_n) {
+  const int nch = (max_n + kChunk - 1) / kChunk;
+  const int ctas = nch < kTopkClusterMax ? nch : kTopkClusterMax;
+  const int slice = (max_n + ctas - 1) / ctas;
+  return slice <= kTopkClusterSlice ? ctas : 0;
+}
+
+cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
+                                       cudaStream_t stream) {
+  const int ctas = topk_cluster_ctas(max_n);
+  if (ctas == 0) return cudaErrorInvalidValue;
+  const int slice = (((max_n + ctas - 1) / ctas) + 31) & ~31;
+  const size_t smem = static_cast<size_t>(slice) * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(topk_cluster_select_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, p.nrows);
+  cfg.blockDim = dim3(kClThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ctas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_select_kernel, p, slice);
 }
 
 cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,

@@ -202,6 +202,36 @@ int dsa_sparse_attn_prefill(const dsa_problem* p, const void* q, const void* qI,
                             void* stream);
 
 /*
+ * dsa_topk_noalloc -- dsa_topk for callers that cannot give the library any
+ * device memory. Some callers cannot allocate: an operator plugin whose host
+ * framework hands it only its input and output tensors, a serving engine that
+ * reserves its whole memory budget at start-up and forbids allocations while
+ * requests run, or a latency-critical path that cannot take cudaMalloc's
+ * implicit device synchronisation. This call takes no workspace: its scratch
+ * (radix histograms, tickets, candidates, selection bitmaps) is a static
+ * device array of about 8.2 MiB inside libdsa that every GPU loading the
+ * library holds until the process exits. The pages have no counterpart of
+ * this call.
+ *
+ *   scores, idx   as for dsa_topk (device pointers owned by the caller)
+ *
+ * Limits: at most DSA_TOPK_NOALLOC_MAX_ROWS query rows (batch * q_len) of at
+ * most DSA_TOPK_NOALLOC_MAX_LEN visible keys; larger problems are rejected
+ * with DSA_ERR_UNSUPPORTED before anything is enqueued. The call allocates
+ * nothing (no cudaMalloc, no library allocator). Its first call on a device
+ * looks up the scratch array's device address for that device
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.
+ * Every call shares the one array and its contents persist between calls;
+ * each call clears the parts that must start at zero. Calls that overlap on
+ * the GPU (concurrent streams or host threads) race on the scratch and must
+ * be serialised by the caller. The result equals dsa_topk's bit for bit.
+ */
+#define DSA_TOPK_NOALLOC_MAX_ROWS 8
+#define DSA_TOPK_NOALLOC_MAX_LEN 131072
+int dsa_topk_noalloc(const dsa_problem* p, const float* scores, int32_t* idx,
+                     void* stream);
+
+/*
  * Synchronises `stream`, then copies the device status word from the
  * workspace to *status_out (0 = no device-side problem; bit 0 = a bounded
  * wait ran out). Returns DSA_ERR_TIMEOUT if that bit is set.

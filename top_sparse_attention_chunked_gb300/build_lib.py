@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa.so")
-SOURCES = ["dsa_api.cu", "indexer.cu", "topk.cu", "attention.cu", "prefill_attn.cu"]
+SOURCES = ["dsa_api.cu", "indexer.cu", "topk.cu", "attention.cu", "prefill_attn.cu",
+           "topk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -487,6 +487,18 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
 
 }  // namespace
 
+// ------------------------------------------------------------------ no-alloc top-k helpers
+int noalloc_fail(int status, const char* msg) { return fail(status, "%s", msg); }
+
+int noalloc_check_topk(const dsa_problem* p, int* rows, int* max_n) {
+  Derived d;
+  const int rc = check_problem(p, DSA_OP_TOPK, &d);
+  if (rc) return rc;
+  *rows = d.rows;
+  *max_n = d.max_n;
+  return DSA_OK;
+}
+
 // ------------------------------------------------------------------ timing hook
 void timing_before(int kind, cudaStream_t st) {
   if (kind != g_timing_kind) return;

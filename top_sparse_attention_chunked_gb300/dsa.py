@@ -31,7 +31,7 @@ DSA_KERNEL_TOPK_ROW, DSA_KERNEL_ATTENTION = 3, 4
 EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill",
             "dsa_read_device_status", "dsa_last_error_string", "dsa_status_string",
-            "dsa_version", "dsa_timing_select", "dsa_timing_read"]
+            "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -91,6 +91,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_version": (i32, []),
         "dsa_timing_select": (i32, [i32]),
         "dsa_timing_read": (i32, [ctypes.POINTER(ctypes.c_float)]),
+        "dsa_topk_noalloc": (i32, [P, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -194,6 +195,17 @@ def dsa_topk(p: DsaProblem, scores, idx, workspace, stream=None):
     wp, wn = _ws(workspace)
     _check(lib.dsa_topk(ctypes.byref(p), _ptr(scores, "scores", torch.float32, (B, S, cap)),
                         _ptr(idx, "idx", torch.int32, (B, S, p.top_k)), wp, wn, _stream(stream)))
+
+
+def dsa_topk_noalloc(p: DsaProblem, scores, idx, stream=None):
+    """dsa_topk without a workspace, for callers that cannot allocate device
+    memory (the library keeps the scratch in a static device array; at most
+    8 query rows of at most 131,072 visible keys)."""
+    B, S, cap = p.batch, p.q_len, p.cache_capacity
+    lib = load_library()
+    _check(lib.dsa_topk_noalloc(ctypes.byref(p),
+                                _ptr(scores, "scores", torch.float32, (B, S, cap)),
+                                _ptr(idx, "idx", torch.int32, (B, S, p.top_k)), _stream(stream)))
 
 
 def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream):

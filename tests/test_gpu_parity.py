@@ -136,6 +136,7 @@ def _topk_case(dsa, B, S, T, cap, k, kind, seed):
     (2, 3, [5000, 3000], 5000, 100), (1, 1, 4096, 4096, 512), (2, 2, [2049, 2], 4100, 2048),
     (1, 4, 70, 80, 64), (1, 1, 1, 1, 1), (1, 2, 9000, 9000, 8999),
     (1, 1, 600000, 600000, 2048),   # longer than the cluster select: global merge path
+    (1, 2, 40000, 40000, 3000),     # tie-heavy rows with > 8,192 threshold-bin candidates
 ])
 def test_topk_bitexact_chunked(dsa, kind, B, S, T, cap, k):
     _topk_case(dsa, B, S, T, cap, k, kind, seed=hash((kind, B, S, k)) & 0xFFFF)
@@ -266,6 +267,17 @@ def test_topk_larger_than_context(dsa):
     for s in range(3):
         n = 50 - 3 + s + 1
         assert idx[0, s, :n].tolist() == list(range(n)) and (idx[0, s, n:] == -1).all()
+    check_step(wl, cpu, idx, out)
+
+
+def test_decode_all_equal_scores_long_row(dsa):
+    """kI = 0 over 50,000 keys: every score ties, the threshold bin holds all
+    keys (more than the cluster select gathers), the lowest indices win."""
+    wl = small_workload(batch=1, q_len=1, total_len=50000, top_k=2048, seed=16)
+    cpu = make_inputs(wl)
+    cpu["kI"].zero_()
+    _, idx, out = run_step(dsa, wl, cpu=cpu)
+    assert idx[0, 0].tolist() == list(range(2048))
     check_step(wl, cpu, idx, out)
 
 

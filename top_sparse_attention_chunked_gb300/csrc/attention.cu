@@ -86,14 +86,23 @@ __device__ __forceinline__ uint32_t load_q2(const void* q, size_t elem) {
   }
 }
 
+// Exact float value of the signed byte `i` of `x`: the byte plus 128 lands in
+// the low mantissa bits of 2^23 (a byte permute), and subtracting 2^23 + 128
+// leaves the code. Two plain ALU operations, no int-to-float conversion.
+__device__ __forceinline__ float code_to_float(uint32_t x_biased, int i) {
+  return __uint_as_float(__byte_perm(x_biased, 0x4B000000u, 0x7540u | static_cast<uint32_t>(i))) -
+         8388736.0f;
+}
+
 // 16 INT8 codes -> 16 exact 16-bit values written as two swizzled chunks
 template <bool F16>
 __device__ __forceinline__ void convert_codes16(const uint4 src, uint8_t* tile, int row, int c0) {
-  const int8_t* b = reinterpret_cast<const int8_t*>(&src);
+  const uint32_t wsrc[4] = {src.x ^ 0x80808080u, src.y ^ 0x80808080u, src.z ^ 0x80808080u,
+                            src.w ^ 0x80808080u};
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    w[i] = pack16<F16>(static_cast<float>(b[2 * i]), static_cast<float>(b[2 * i + 1]));
+    w[i] = pack16<F16>(code_to_float(wsrc[i >> 1], (2 * i) & 3), code_to_float(wsrc[i >> 1], (2 * i + 1) & 3));
   *reinterpret_cast<uint4*>(tile + swz(row, c0)) = make_uint4(w[0], w[1], w[2], w[3]);
   *reinterpret_cast<uint4*>(tile + swz(row, c0 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 }
@@ -146,6 +155,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   constexpr bool PV_SPLIT = !PV_F16;   // BF16 P as hi + lo
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
+  __shared__ int32_t s_idx[kAttnMaxSplitKeys];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     const int o = tile * kTileKeys;
     int key = -1;
     if (lane < kTileKeys && o + lane < split_len) {
-      key = idx_row[o + lane];
+      key = s_idx[o + lane];
       if (key < 0 || key >= T) key = -1;
     }
     if constexpr (KV == KV_INT8) {
@@ -241,6 +251,9 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   }
   pdl_wait();       // the selected indices come from the previous kernel
   pdl_trigger();
+  // the split's selected indices, loaded once (all loads in flight together)
+  for (int i = threadIdx.x; i < split_len; i += kAttnThreads) s_idx[i] = __ldcg(idx_row + i);
+  __syncthreads();
   if (my_tiles > 0) issue_tile(0, 0);
   cp_async_commit();
 
@@ -335,22 +348,19 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         tile_sum[e >> 1] += pv;
         pt[n][e] = ptv;
       }
-    // rescale the running state to the new max: l = l * 2^d_old + sum p
-    float alpha[2];
-    bool fast[2];
+    // rescale the running state to the new max: x * 2^d_old as (x * a1) * a2
+    // with both factors formed without underflow (exp2_pair)
+    float a1[2], a2[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      fast[i] = d_old[i] >= -125.0f;
-      alpha[i] = fast[i] ? exp2f(d_old[i]) : 0.0f;
-      l_run[i] = mul_exp2(l_run[i], d_old[i]) + tile_sum[i];
+      exp2_pair(d_old[i], &a1[i], &a2[i]);
+      l_run[i] = l_run[i] * a1[i] * a2[i] + tile_sum[i];
       m_run[i] = m_new[i];
     }
 #pragma unroll
     for (int nd = 0; nd < kD / 8; ++nd)
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        o_acc[nd][e] = fast[e >> 1] ? o_acc[nd][e] * alpha[e >> 1]
-                                    : mul_exp2(o_acc[nd][e], d_old[e >> 1]);
+      for (int e = 0; e < 4; ++e) o_acc[nd][e] = o_acc[nd][e] * a1[e >> 1] * a2[e >> 1];
 
     // ---- O += P V
     uint32_t pa[4], pl[4];
@@ -457,36 +467,60 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     cluster.sync();
     const int ns = p.nsplit;
     const int rank = static_cast<int>(cluster.block_rank());
+    float* cf = pubO + kAttnRows * kD;   // [16 peers][16 rows] factors f1, f2; M, L
+    float* cm = cf + 2 * 16 * kAttnRows;   // [16 peers][16 rows] peer m, then l
+    // every (peer, row) pair in parallel: peer m and l into local shared memory
+    for (int pr = threadIdx.x; pr < 16 * kAttnRows; pr += kAttnThreads) {
+      const int q = pr / kAttnRows, row = pr % kAttnRows;
+      float mq = -INFINITY, lq = 0.0f;
+      if (q < ns) {
+        const float* peerML = cluster.map_shared_rank(sML, q);
+        mq = peerML[row];
+        lq = peerML[kAttnRows + row];
+      }
+      cm[pr] = mq;
+      cm[16 * kAttnRows + pr] = lq;
+    }
+    __syncthreads();
+    float* sMrow = cm + 2 * 16 * kAttnRows;   // M[16], L[16]
+    if (threadIdx.x < kAttnRows) {
+      float M = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) M = fmaxf(M, cm[q * kAttnRows + threadIdx.x]);
+      sMrow[threadIdx.x] = M;
+    }
+    __syncthreads();
+    for (int pr = threadIdx.x; pr < 16 * kAttnRows; pr += kAttnThreads) {
+      const int row = pr % kAttnRows;
+      float f1, f2;
+      exp2_pair(cm[pr] - sMrow[row], &f1, &f2);
+      cf[pr] = f1;
+      cf[16 * kAttnRows + pr] = f2;
+    }
+    __syncthreads();
+    if (threadIdx.x < kAttnRows) {   // row sums in a fixed order (deterministic)
+      float L = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int pr = q * kAttnRows + threadIdx.x;
+        L += cm[16 * kAttnRows + pr] * cf[pr] * cf[16 * kAttnRows + pr];
+      }
+      sMrow[kAttnRows + threadIdx.x] = L;
+    }
+    __syncthreads();
     const int cols = kD / ns;                      // ns divides 128 (power of two)
     for (int o = threadIdx.x; o < kAttnRows * cols; o += kAttnThreads) {
       const int row = o / cols, col = rank * cols + o % cols;
       if (row >= nh) continue;
-      float mv[16], lv[16], ov[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (q < ns) {
-          const float* peerML = cluster.map_shared_rank(sML, q);
-          const float* peerO = cluster.map_shared_rank(pubO, q);
-          mv[q] = peerML[row];
-          lv[q] = peerML[kAttnRows + row];
-          ov[q] = peerO[row * kD + col];
-        }
-      }
-      float M = -INFINITY;
+      float ov[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        if (q < ns) M = fmaxf(M, mv[q]);
-      float L = 0.0f, O = 0.0f;
+        ov[q] = q < ns ? cluster.map_shared_rank(pubO, q)[row * kD + col] : 0.0f;
+      float O = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        if (q < ns) {
-          float f1, f2;
-          exp2_pair(mv[q] - M, &f1, &f2);
-          L += lv[q] * f1 * f2;
-          O += ov[q] * f1 * f2;
-        }
-      }
-      store_out<OUT>(p.out, (out_row + row) * kD + col, O / L);
+      for (int q = 0; q < 16; ++q)
+        O += ov[q] * cf[q * kAttnRows + row] * cf[16 * kAttnRows + q * kAttnRows + row];
+      store_out<OUT>(p.out, (out_row + row) * kD + col, O / sMrow[kAttnRows + row]);
     }
     cluster.sync();    // peers may still be reading this CTA's shared memory
     return;
@@ -564,17 +598,6 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (p.nsplit > 8) {
-    // a 16-CTA cluster is not portable: if it cannot be placed, merge the
-    // splits through global memory instead
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters < 1) {
-      cudaGetLastError();
-      AttnParams q = p;
-      q.cluster = 0;
-      return launch_kernel(kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true, q);
-    }
-  }
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -586,6 +609,36 @@ static cudaError_t launch_out(const AttnParams& p, int out_dtype, cudaStream_t s
     case DSA_FP32: return launch_t<KV, Q_F16, DSA_FP32>(p, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+int attn_max_cluster() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  if (cached[dev]) return cached[dev];
+  int result = 8;
+  auto kern = sparse_attn_kernel<KV_FP16, false, DSA_BF16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) result = 16;
+  }
+  cudaGetLastError();
+  cached[dev] = result;
+  return result;
 }
 
 cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,

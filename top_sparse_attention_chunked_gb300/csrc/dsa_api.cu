@@ -158,9 +158,10 @@ int check_problem(const dsa_problem* p, int op, Derived* d) {
       return fail(DSA_ERR_UNSUPPORTED, "FP16 query with a BF16 cache is not built");
     if (p->out_dtype != DSA_BF16 && p->out_dtype != DSA_FP16 && p->out_dtype != DSA_FP32)
       return fail(DSA_ERR_UNSUPPORTED, "out_dtype must be BF16, FP16 or FP32");
-    if (p->attn_split_keys < 0 || p->attn_split_keys % 16 != 0)
-      return fail(DSA_ERR_INVALID_ARG, "attn_split_keys %d must be 0 or a multiple of 16",
-                  p->attn_split_keys);
+    if (p->attn_split_keys < 0 || p->attn_split_keys % 16 != 0 ||
+        p->attn_split_keys > kAttnMaxSplitKeys)
+      return fail(DSA_ERR_INVALID_ARG, "attn_split_keys %d must be 0 or a multiple of 16 up to %d",
+                  p->attn_split_keys, kAttnMaxSplitKeys);
     if (!(p->softmax_scale >= 0.0f) || std::isinf(p->softmax_scale))
       return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
     d->G = p->num_q_heads / p->num_kv_heads;
@@ -196,9 +197,13 @@ void choose_split(const dsa_problem* p, const Derived& d, int sms, int* split_ke
     const int cap = ceil_div(d.kmax, 64);
     s = s < cap ? s : cap;
     if (s < 1) s = 1;
-    // a power of two, so the cluster combine splits the 128 columns evenly
+    if (s > attn_max_cluster()) s = attn_max_cluster();
+    // a power of two (so the cluster combine splits the 128 columns evenly),
+    // and no split longer than kAttnMaxSplitKeys
+    const int s_min = ceil_div(d.kmax, kAttnMaxSplitKeys);
     int s2 = 1;
     while (s2 * 2 <= s) s2 *= 2;
+    while (s2 < s_min) s2 *= 2;
     s = s2;
     sk = ceil_div(ceil_div(d.kmax, s), 16) * 16;
     const int sk_min = ceil_div(ceil_div(d.kmax, kAttnMaxSplits), 16) * 16;
@@ -369,6 +374,16 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
     if (e != cudaSuccess) return cuda_fail(e, "top-k row launch");
     return DSA_OK;
   }
+  tp.hist_ready = hist_ready ? 1 : 0;
+  if (topk_cluster_ctas(d.max_n) > 0 && topk_cluster_feasible(d.max_n)) {
+    // one cluster per row (it builds the row histogram itself unless the
+    // indexer did); no other scratch
+    timing_before(DSA_KERNEL_TOPK_SELECT, st);
+    e = launch_topk_cluster_select(tp, d.max_n, after_kernel, st);
+    timing_after(DSA_KERNEL_TOPK_SELECT, st);
+    if (e == cudaSuccess) return DSA_OK;
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "top-k cluster launch");
+  }
   // chunked path, in rounds of at most L.topk_rows rows
   for (int r0 = 0; r0 < d.rows; r0 += L.topk_rows) {
     tp.row0 = r0;
@@ -382,10 +397,7 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
       if (e != cudaSuccess) return cuda_fail(e, "top-k histogram launch");
     }
     timing_before(DSA_KERNEL_TOPK_SELECT, st);
-    if (topk_cluster_ctas(d.max_n) > 0)
-      e = launch_topk_cluster_select(tp, d.max_n, true, st);
-    else
-      e = launch_topk_chunk_select(tp, st);
+    e = launch_topk_chunk_select(tp, st);
     timing_after(DSA_KERNEL_TOPK_SELECT, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-k select launch");
   }
@@ -417,7 +429,6 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   if (ap.nsplit > kAttnMaxSplits)
     return fail(DSA_ERR_UNSUPPORTED, "attn_split_keys %d gives %d splits (max %d)",
                 p->attn_split_keys, ap.nsplit, kAttnMaxSplits);
-  ap.cluster = (ap.nsplit == 2 || ap.nsplit == 4 || ap.nsplit == 8 || ap.nsplit == 16) ? 1 : 0;
   if (ap.nsplit > splits_bound(p, d))
     return fail(DSA_ERR_UNSUPPORTED, "device has more SMs than the workspace bound assumes");
   const float scale = p->softmax_scale > 0.0f ? p->softmax_scale
@@ -426,6 +437,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.lens = lens_of(p);
   ap.q_dtype = p->q_dtype;
   ap.out_dtype = p->out_dtype;
+  ap.cluster = attn_uses_cluster(ap.nsplit) ? 1 : 0;
   cudaError_t e;
   timing_before(DSA_KERNEL_ATTENTION, st);
   if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin))
@@ -435,6 +447,13 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   timing_after(DSA_KERNEL_ATTENTION, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return DSA_OK;
+}
+
+bool prefill_tc_ok(const dsa_problem* p, const Derived& d, const DeviceInfo& di) {
+  AttnParams ap{};
+  ap.topk = p->top_k;
+  (void)d;
+  return prefill_tc_supported(ap, p->kv_dtype, di.smem_optin);
 }
 
 int check_attn_ptrs(const dsa_problem* p, const void* q, const void* qI, const float* w,
@@ -471,16 +490,31 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
   rc = device_info(&di);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.zero_begin - 256, 0,
-                                  L.zero_end - L.zero_begin + 256, st);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  const bool decode = (op == DSA_OP_DECODE);
+  // Which kernels run decides what scratch must start at zero: the chunked
+  // top-k needs its histograms, tickets and counters cleared, the split-K
+  // attention outside a cluster its tickets. Otherwise nothing is cleared
+  // (the indexer resets the status word itself).
+  const bool topk_rows = !decode && d.max_n <= topk_row_max_len(di.smem_optin);
+  // decode: the indexer epilogue builds the top-k's row histograms
+  const bool hist_in_indexer = decode;
+  int split_keys = 0, nsplit = 1;
+  choose_split(p, d, di.sms, &split_keys, &nsplit);
+  const bool tc_prefill = !decode && p->attn_split_keys == 0 && prefill_tc_ok(p, d, di);
+  const bool attn_tickets = !tc_prefill && nsplit > 1 && !attn_uses_cluster(nsplit);
+  if (hist_in_indexer || attn_tickets) {
+    // histograms, tickets and counters start at zero; the clearing kernel
+    // overlaps the indexer, which waits for it only before its final flush
+    cudaError_t e = launch_zero_scratch(ws, L.zero_end, st);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  }
   float* scores = at<float>(ws, L.scores);
   int32_t* idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
   uint32_t* status = at<uint32_t>(ws, 0);
-  const bool decode = (op == DSA_OP_DECODE);
-  rc = run_indexer(p, d, di, qI, w, kI, scores, decode ? at<uint32_t>(ws, L.hist) : nullptr, status, st);
+  rc = run_indexer(p, d, di, qI, w, kI, scores, hist_in_indexer ? at<uint32_t>(ws, L.hist) : nullptr,
+                   status, st);
   if (rc) return rc;
-  rc = run_topk(p, d, di, L, scores, idx, ws, decode, !decode, true, st);
+  rc = run_topk(p, d, di, L, scores, idx, ws, hist_in_indexer, topk_rows, true, st);
   if (rc) return rc;
   return run_attention(p, d, di, L, q, k, v, ks, vs, idx, out, ws, !decode, st);
 }

@@ -61,6 +61,8 @@ cudaError_t launch_indexer(const IndexerParams& p, const CUtensorMap& tm_kI,
                            const CUtensorMap& tm_qI, dim3 grid, size_t smem_bytes,
                            int stages, cudaStream_t stream);
 size_t indexer_smem_bytes(int QB, bool with_hist, int* stages_out, size_t smem_limit);
+// Clears `bytes` (a multiple of 16) of scratch; the next kernel may overlap it.
+cudaError_t launch_zero_scratch(void* base, size_t bytes, cudaStream_t stream);
 
 // ---------------------------------------------------------------- top-k
 struct TopkParams {
@@ -76,6 +78,7 @@ struct TopkParams {
   int B, S, cap, k;
   int nchunks;                  // chunks of the longest row
   int row0, nrows;              // rows handled by this launch (workspace rows are local)
+  int hist_ready;               // cluster select: the row histograms are in `hist`
   SeqLens lens;
 };
 
@@ -84,10 +87,9 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream);
 // `pdl`: launched right after another kernel of the same call
 cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,
                             cudaStream_t stream);
-// Cluster select: up to kTopkClusterMax CTAs per row (a portable cluster),
-// each holding a slice of at most kTopkClusterSlice keys in shared memory.
-constexpr int kTopkClusterMax = 8;
-constexpr int kTopkClusterSlice = 32768;
+// Cluster select: up to kTopkClusterMax CTAs per row (16, checked at launch),
+// each owning up to 16,384 keys (32 per thread, in registers).
+constexpr int kTopkClusterMax = 16;
 int topk_cluster_ctas(int max_n);   // 0 if the row is too long for it
 cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
                                        cudaStream_t stream);
@@ -115,10 +117,21 @@ struct AttnParams {
 
 constexpr int kAttnRows = 16;                                   // heads per MMA tile
 constexpr int kAttnMaxSplits = 128;                             // split-K partial states per row
+constexpr int kAttnMaxSplitKeys = 2048;                         // selected keys per split CTA
 constexpr int kPartialFloats = 2 * kAttnRows + kAttnRows * DSA_HEAD_DIM;  // m, l, o
 
 cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
                              cudaStream_t stream);
+
+// Largest thread-block cluster the split-K attention can use on this device
+// (16 if a 16-CTA cluster can be placed, else 8), and whether a split count
+// is merged inside a cluster.
+int attn_max_cluster();
+inline bool attn_uses_cluster(int nsplit) {
+  return (nsplit == 2 || nsplit == 4 || nsplit == 8 || nsplit == 16) && nsplit <= attn_max_cluster();
+}
+// Whether the cluster top-k can be placed for rows of max_n keys.
+bool topk_cluster_feasible(int max_n);
 
 // tcgen05 prefill attention (BF16 / FP16 cache, top_k <= 2048)
 bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin);

@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
   const long long count = u1 - u0;
 
+  // the first block resets the call's device status word (no memset needed)
+  if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.status = 0u;
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&bars->full[i], 1);
@@ -178,6 +180,38 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     bars->abort_flag = 0;
     fence_mbar_init();
   }
+  // Producer state (thread 0).
+  struct ProducerState {
+    UnitCursor c;
+    int pb, pqb, nblk;
+    long long i, issued;
+  } ps{};
+  auto produce = [&](long long limit) {
+    for (; ps.i < limit; ++ps.i) {
+      UnitCursor& c = ps.c;
+      if (c.b != ps.pb || c.qb != ps.pqb) {
+        const int bi = ps.nblk & 1;
+        if (ps.nblk >= 2 &&
+            !mbar_wait_bounded(&bars->bempty[bi], ((ps.nblk >> 1) - 1) & 1, abort_flag))
+          return;
+        mbar_arrive_expect_tx(&bars->bfull[bi], C::kBBytes);
+        tma_load_2d(sB + bi * C::kBBytes, &tm_qI, &bars->bfull[bi], 0,
+                    (c.b * p.S + c.qb * QB) * DSA_IDX_HEADS);
+        ++ps.nblk;
+        ps.pb = c.b;
+        ps.pqb = c.qb;
+      }
+      const int s = static_cast<int>(ps.i % stages);
+      const long long r = ps.i / stages;
+      if (ps.i >= stages &&
+          !mbar_wait_bounded(&bars->empty[s], static_cast<uint32_t>((r - 1) & 1), abort_flag))
+        return;
+      mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
+      tma_load_2d(sA + s * kATileBytes, &tm_kI, &bars->full[s], 0, c.b * p.cap + c.kt * kKeyTile);
+      ++ps.issued;
+      advance_unit(p, c);
+    }
+  };
   if (warp == 1) tmem_alloc(&bars->tmem_base, C::kTmemCols);
   if constexpr (HIST) {
     for (int i = threadIdx.x; i < QB * kHistBins; i += kIdxThreads) sHist[i] = 0u;
@@ -193,38 +227,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     if (lane == 0 && count > 0) {
       tma_prefetch_desc(&tm_kI);
       tma_prefetch_desc(&tm_qI);
-      UnitCursor c = locate_unit(p, u0);
-      int pb = -1, pqb = -1, nblk = 0;
-      long long issued = 0;
-      for (long long i = 0; i < count; ++i) {
-        if (c.b != pb || c.qb != pqb) {
-          const int bi = nblk & 1;
-          if (nblk >= 2 && !mbar_wait_bounded(&bars->bempty[bi], ((nblk >> 1) - 1) & 1, abort_flag))
-            break;
-          mbar_arrive_expect_tx(&bars->bfull[bi], C::kBBytes);
-          tma_load_2d(sB + bi * C::kBBytes, &tm_qI, &bars->bfull[bi], 0,
-                      (c.b * p.S + c.qb * QB) * DSA_IDX_HEADS);
-          ++nblk;
-          pb = c.b;
-          pqb = c.qb;
-        }
-        const int s = static_cast<int>(i % stages);
-        const long long r = i / stages;
-        if (i >= stages && !mbar_wait_bounded(&bars->empty[s], static_cast<uint32_t>((r - 1) & 1), abort_flag))
-          break;
-        mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
-        tma_load_2d(sA + s * kATileBytes, &tm_kI, &bars->full[s], 0,
-                    c.b * p.cap + c.kt * kKeyTile);
-        ++issued;
-        advance_unit(p, c);
-      }
+      ps.c = locate_unit(p, u0);
+      ps.pb = -1;
+      ps.pqb = -1;
+      produce(count);
       if (*abort_flag) {
         // let the copies still in flight land before the CTA can exit
-        const long long first = issued > stages ? issued - stages : 0;
-        for (long long i = first; i < issued; ++i)
+        const long long first = ps.issued > stages ? ps.issued - stages : 0;
+        for (long long i = first; i < ps.issued; ++i)
           mbar_drain(&bars->full[i % stages], static_cast<uint32_t>((i / stages) & 1));
-        for (int k = 0; k < nblk && k < 2; ++k) {
-          const int blk = nblk - 1 - k;
+        for (int k = 0; k < ps.nblk && k < 2; ++k) {
+          const int blk = ps.nblk - 1 - k;
           mbar_drain(&bars->bfull[blk & 1], (blk >> 1) & 1);
         }
       }
@@ -323,10 +336,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           const bool valid = t < visible_len(T, p.S, s);
           if (valid) p.scores[(static_cast<size_t>(c.b) * p.S + s) * p.cap + t] = acc;
           if constexpr (HIST) {
-            const uint32_t bin = valid ? (float_key(acc) >> (32 - kHistBits)) : 0xFFFFFFFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (valid && lane == __ffs(peers) - 1)
-              atomicAdd(&sHist[(jq + g) * kHistBins + bin], static_cast<uint32_t>(__popc(peers)));
+            // plain shared atomics: cheaper than warp-aggregating each update
+            if (valid) atomicAdd(&sHist[(jq + g) * kHistBins + (float_key(acc) >> (32 - kHistBits))], 1u);
           }
         }
       }
@@ -336,7 +347,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       advance_unit(p, c);
     }
     if constexpr (HIST) {
-      // one query block per CTA here (see the unit ranges above)
+      // one query block per CTA here (see the unit ranges above); the global
+      // histograms were cleared by the previous kernel of the call
+      pdl_wait();
       named_bar_sync(1, kIdxEpiThreads);
       if (count > 0) {
         for (int j = 0; j < QB; ++j) {
@@ -359,6 +372,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   if (threadIdx.x == 0 && bars->abort_flag) atomicOr(p.status, kDevTimeout);
 }
 
+// Clears call scratch (histograms, tickets, counters). It lets the next
+// kernel launch at once; that kernel waits for it only where it needs zeros.
+__global__ void zero_scratch_kernel(uint4* base, long long n16) {
+  pdl_trigger();
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    base[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+cudaError_t launch_zero_scratch(void* base, size_t bytes, cudaStream_t stream) {
+  const long long n16 = static_cast<long long>(bytes / 16);
+  const int blocks = static_cast<int>(n16 / 256 + 1 < 64 ? n16 / 256 + 1 : 64);
+  return launch_kernel(zero_scratch_kernel, dim3(blocks), dim3(256), 0, stream, false,
+                       static_cast<uint4*>(base), n16);
+}
+
 size_t indexer_smem_bytes(int QB, bool with_hist, int* stages_out, size_t smem_limit) {
   const int N = QB * 16;
   size_t ob, ow, oh, obar;
@@ -378,7 +407,9 @@ static cudaError_t launch_n(const IndexerParams& p, const CUtensorMap& tm_kI,
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_kernel(kern, grid, dim3(kIdxThreads), smem, stream, false, tm_kI, tm_qI, p, stages);
+  // with histograms the kernel follows the scratch-clearing kernel and waits
+  // for it only before its final flush
+  return launch_kernel(kern, grid, dim3(kIdxThreads), smem, stream, HIST, tm_kI, tm_qI, p, stages);
 }
 
 cudaError_t launch_indexer(const IndexerParams& p, const CUtensorMap& tm_kI,

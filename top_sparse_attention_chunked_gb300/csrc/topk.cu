@@ -374,26 +374,69 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------
 // 2b. cluster select: one thread-block cluster of up to 8 CTAs per row. Each
-// CTA holds a contiguous slice of the row's keys in shared memory. After the
-// threshold bin from the row histogram, the clusters refine the exact
-// threshold composite (key << 32 | ~index) 8 bits at a time, summing every
-// CTA's digit histogram through distributed shared memory; then each CTA
-// emits its own slice in ascending order at the offset given by the peers'
-// selected counts. No global scratch beyond the histogram, no serial tail.
+// CTA holds a contiguous slice of the row's keys in shared memory. From the
+// row histogram every CTA finds the threshold bin and compacts its keys in
+// that bin (the candidates, usually a few hundred). The exact threshold
+// composite (key << 32 | ~index) is then refined 8 bits at a time over the
+// candidates only, summing the CTAs' digit histograms through distributed
+// shared memory. Finally each CTA emits its own slice in ascending order (one
+// block scan) at the offset given by the peers' selected counts. No global
+// scratch beyond the histogram and no serial tail.
 // ---------------------------------------------------------------------------
 constexpr int kClThreads = 512;
+constexpr int kClGatherMax = 8192;   // candidates gathered into every CTA of the cluster
 
-__global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const TopkParams p,
-                                                                           int slice) {
+// Exact threshold over a list of candidate composites held by this CTA:
+// refines (prefix, mask) until `need` candidates are at or above it.
+__device__ void local_composite_select(const unsigned long long* list, int n,
+                                       unsigned long long* prefix, unsigned long long* mask,
+                                       uint32_t need, uint32_t* h, uint32_t* warp_tot, int* sd,
+                                       uint32_t* sabove, uint32_t* scnt) {
+  int hi = 52;
+  bool all = false;
+  while (!all && hi >= 0) {
+    const int w = hi + 1 < 11 ? hi + 1 : 11;
+    const int sh = hi - w + 1;
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < (1 << w); i += kClThreads) h[i] = 0u;
+    __syncthreads();
+    for (int c = threadIdx.x; c < n; c += kClThreads) {
+      const unsigned long long cc = list[c];
+      if ((cc & *mask) == *prefix) atomicAdd(&h[static_cast<uint32_t>(cc >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
+    __syncthreads();
+    find_threshold_digit<kClThreads>(h, 1 << w, need, warp_tot, sd, sabove, scnt);
+    need -= *sabove;
+    *prefix |= static_cast<unsigned long long>(*sd) << sh;
+    *mask |= static_cast<unsigned long long>(dm) << sh;
+    all = (*scnt == need);
+    __syncthreads();
+    hi -= w;
+  }
+}
+
+// Each thread owns PER consecutive keys of the slice, held in registers
+// (PER = 8, 16 or 32), so the emit needs a single block scan and no
+// shared-memory bank conflicts arise; the threshold-bin candidates go to
+// shared memory.
+template <int PER>
+__global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const TopkParams p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ uint32_t skeys[];            // this CTA's slice of keys
-  __shared__ uint32_t h[kHistBins];              // row histogram, then 8-bit digit totals
+  constexpr int kSlice = PER * kClThreads;
+  extern __shared__ unsigned long long scand[];  // candidate composites of this CTA
+  __shared__ uint32_t h[kHistBins];              // row histogram, then digit totals
+  __shared__ uint32_t hloc[kHistBins];           // this CTA's slice histogram
+  __shared__ uint32_t hred[kHistBins];           // the range of bins this CTA sums
   __shared__ uint32_t hd[256];                   // this CTA's digit histogram
   __shared__ uint32_t warp_tot[32];
   __shared__ int s_d;
   __shared__ uint32_t s_above, s_cnt;
   __shared__ uint32_t s_count;                   // keys this CTA selects
+  __shared__ uint32_t s_ncand, s_nsure;          // published candidate / sure counts
+  __shared__ uint32_t s_pc[kTopkClusterMax], s_ps[kTopkClusterMax];
 
   const int rl = blockIdx.y, r = p.row0 + rl;
   const int rank = static_cast<int>(cluster.block_rank());
@@ -401,114 +444,301 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
   pdl_wait();      // scores and the histogram come from the previous kernel
   pdl_trigger();
   const RowInfo ri = row_info(p, r);
-  const int t0 = rank * slice;
-  const int t1 = min(ri.n, t0 + slice);
-  const int m = max(0, t1 - t0);
-  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
-  for (int i = threadIdx.x; i < m; i += kClThreads) skeys[i] = float_key(row[t0 + i]);
-  const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) h[i] = __ldcg(gh + i);
+  const int t0 = rank * kSlice;
+  const int m = max(0, min(ri.n, t0 + kSlice) - t0);
+  const int tb = threadIdx.x * PER;              // this thread's first key in the slice
+  const float* src = p.scores + static_cast<size_t>(r) * p.cap + t0 + tb;
+
+  // ---- this thread's keys into registers (all loads in flight together)
+  uint32_t key[PER];
+  if (tb + PER <= m && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+    for (int v = 0; v < PER / 4; ++v) {
+      const float4 f = __ldcg(reinterpret_cast<const float4*>(src) + v);
+      key[4 * v] = float_key(f.x);
+      key[4 * v + 1] = float_key(f.y);
+      key[4 * v + 2] = float_key(f.z);
+      key[4 * v + 3] = float_key(f.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) key[j] = tb + j < m ? float_key(__ldcg(src + j)) : 0u;
+  }
+  const int nval = max(0, min(PER, m - tb));     // valid keys of this thread
   if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; s_count = 0; }
-  __syncthreads();
+  if (p.hist_ready) {
+    // ---- the row histogram came with the scores (indexer epilogue)
+    const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
+#pragma unroll
+    for (int u = 0; u < kHistBins / kClThreads; ++u)
+      h[u * kClThreads + threadIdx.x] = __ldcg(gh + u * kClThreads + threadIdx.x);
+    __syncthreads();
+  } else {
+    // ---- the row histogram of the top 11 key bits, built by the cluster:
+    // each CTA counts its slice, each CTA then sums one range of bins over all
+    // peers, and every CTA reads the summed ranges back
+    for (int i = threadIdx.x; i < kHistBins; i += kClThreads) hloc[i] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (j < nval) atomicAdd(&hloc[key[j] >> (32 - kHistBits)], 1u);
+    cluster.sync();                              // every CTA's slice histogram is complete
+    {
+      const int b0 = rank * kHistBins / ncta, b1 = (rank + 1) * kHistBins / ncta;
+      for (int b = b0 + static_cast<int>(threadIdx.x); b < b1; b += kClThreads) {
+        uint32_t tot = 0;
+        for (int q = 0; q < ncta; ++q) tot += cluster.map_shared_rank(hloc, q)[b];
+        hred[b] = tot;
+      }
+    }
+    cluster.sync();                              // every range is summed
+#pragma unroll
+    for (int u = 0; u < kHistBins / kClThreads; ++u) {
+      const int b = u * kClThreads + threadIdx.x;
+      const int owner = ((b + 1) * ncta - 1) / kHistBins;
+      h[b] = cluster.map_shared_rank(hred, owner)[b];
+    }
+    __syncthreads();
+  }
   find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
                                    &s_above, &s_cnt);
   const uint32_t bin = static_cast<uint32_t>(s_d);
   uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
   bool all = (need == s_cnt);
+
+  // ---- candidates (this thread's keys in the threshold bin) and sure keys
+  // (above it); candidates are compacted with a block scan (no atomics)
+  uint32_t cmask[(PER + 31) / 32] = {};
+  uint32_t ncmine = 0, nsure = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    if (j < nval) {
+      const uint32_t kb = key[j] >> (32 - kHistBits);
+      if (kb == bin) {
+        cmask[j >> 5] |= 1u << (j & 31);
+        ++ncmine;
+      } else if (kb > bin) {
+        ++nsure;
+      }
+    }
+  uint32_t ncand = 0, nsure_cta = 0;
+  {
+    // one scan of both counts packed in 16-bit halves (a CTA has <= 16,384 keys)
+    uint32_t both;
+    uint32_t cpos = block_exclusive_scan<kClThreads>(ncmine | (nsure << 16), warp_tot, &both) & 0xFFFFu;
+    ncand = both & 0xFFFFu;
+    nsure_cta = both >> 16;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if ((cmask[j >> 5] >> (j & 31)) & 1u)
+        scand[cpos++] = (static_cast<unsigned long long>(key[j]) << 32) |
+                        (0xFFFFFFFFull - static_cast<uint32_t>(t0 + tb + j));
+  }
+  if (threadIdx.x == 0) {
+    s_ncand = ncand;
+    s_nsure = nsure_cta;
+  }
   unsigned long long prefix = static_cast<unsigned long long>(bin) << 53;
   unsigned long long mask = ~0ull << 53;
-  const int mround = ((m + 31) / 32) * 32;
-  int hi = 52;
-  while (!all && hi >= 0) {
-    const int w = hi + 1 < 8 ? hi + 1 : 8;
-    const int sh = hi - w + 1;
-    const uint32_t dm = (1u << w) - 1u;
-    for (int i = threadIdx.x; i < 256; i += kClThreads) hd[i] = 0u;
-    __syncthreads();
-    for (int i = threadIdx.x; i < mround; i += kClThreads) {
-      uint32_t dg = 0xFFFFFFFFu;
-      if (i < m) {
-        const unsigned long long cc = (static_cast<unsigned long long>(skeys[i]) << 32) |
-                                      (0xFFFFFFFFull - static_cast<uint32_t>(t0 + i));
-        if ((cc & mask) == prefix) dg = static_cast<uint32_t>(cc >> sh) & dm;
-      }
-      hist_add_warp(hd, dg);
-    }
-    cluster.sync();                              // every CTA's digit histogram is complete
-    if (threadIdx.x < 256) {
-      uint32_t tot = 0;
-      for (int q = 0; q < ncta; ++q) tot += cluster.map_shared_rank(hd, q)[threadIdx.x];
-      h[threadIdx.x] = tot;
-    }
-    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
-    __syncthreads();
-    find_threshold_digit<kClThreads>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
-    need -= s_above;
-    prefix |= static_cast<unsigned long long>(s_d) << sh;
-    mask |= static_cast<unsigned long long>(dm) << sh;
-    all = (s_cnt == need);
-    cluster.sync();                              // peers are done reading hd
-    hi -= w;
-  }
-  // selected: top 11 bits above the threshold bin, or in it with the
-  // determined composite bits at or above the threshold prefix
-  auto selected = [&](int i) -> bool {
-    const uint32_t key = skeys[i];
-    const uint32_t kb = key >> (32 - kHistBits);
-    if (kb != bin) return kb > bin;
-    const unsigned long long cc = (static_cast<unsigned long long>(key) << 32) |
-                                  (0xFFFFFFFFull - static_cast<uint32_t>(t0 + i));
-    return (cc & mask) >= prefix;
-  };
-  uint32_t mine = 0;
-  for (int i = threadIdx.x; i < m; i += kClThreads) mine += selected(i) ? 1u : 0u;
-  uint32_t total;
-  block_exclusive_scan<kClThreads>(mine, warp_tot, &total);
-  if (threadIdx.x == 0) s_count = total;
-  cluster.sync();                                // every CTA's count is published
-  uint32_t base = 0;
-  for (int q = 0; q < rank; ++q) base += *cluster.map_shared_rank(&s_count, q);
-  // emit this slice in ascending order: tiles of 4 consecutive keys per thread
   int32_t* out = p.idx + static_cast<size_t>(r) * p.k;
-  for (int tile = 0; tile < m; tile += 4 * kClThreads) {
-    const int i0 = tile + 4 * threadIdx.x;
-    uint32_t sel = 0;
+  // the threshold bin's total (s_cnt) is the same in every CTA: all take the
+  // same path
+  const bool gather = all || s_cnt <= static_cast<uint32_t>(kClGatherMax);
+  cluster.sync();                                // candidates and counts are published
+
+  uint32_t pos = 0;                              // this CTA's first output slot
+  if (gather) {
+    // ---- every CTA gathers all candidates and counts, then resolves locally
+    unsigned long long* sg = scand + PER * kClThreads;   // gathered candidates
+    if (threadIdx.x < ncta) {
+      s_pc[threadIdx.x] = *cluster.map_shared_rank(&s_ncand, threadIdx.x);
+      s_ps[threadIdx.x] = *cluster.map_shared_rank(&s_nsure, threadIdx.x);
+    }
+    __syncthreads();
+    int off = 0, off_mine = 0;
+    for (int q = 0; q < ncta; ++q) {
+      if (q == rank) off_mine = off;
+      off += static_cast<int>(s_pc[q]);
+    }
+    if (!all) {
+      // entry e of the concatenated lists: up to kClGatherMax / 512 = 16 per
+      // thread, all loads in flight before the stores
+      constexpr int kG = kClGatherMax / kClThreads;
+      unsigned long long v[kG];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (i0 + j < m && selected(i0 + j)) sel |= 1u << j;
-    uint32_t tot;
-    uint32_t pos = base + block_exclusive_scan<kClThreads>(__popc(sel), warp_tot, &tot);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if ((sel >> j) & 1u) {
-        if (pos < static_cast<uint32_t>(ri.keff)) out[pos] = t0 + i0 + j;
-        ++pos;
+      for (int k = 0; k < kG; ++k) {
+        const int e = k * kClThreads + threadIdx.x;
+        v[k] = 0ull;
+        if (e < off) {
+          int q = 0, base = 0;
+          while (e >= base + static_cast<int>(s_pc[q])) base += static_cast<int>(s_pc[q++]);
+          v[k] = cluster.map_shared_rank(scand, q)[e - base];
+        }
       }
-    base += tot;
+#pragma unroll
+      for (int k = 0; k < kG; ++k) {
+        const int e = k * kClThreads + threadIdx.x;
+        if (e < off) sg[e] = v[k];
+      }
+    }
+    cluster.sync();                              // every CTA is done reading its peers
+    if (!all)
+      local_composite_select(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above, &s_cnt);
+    // selected keys in the lower slices: their sure keys plus their candidates
+    // at or above the threshold
+    uint32_t lower = 0;
+    for (int c = threadIdx.x; c < off_mine; c += kClThreads)
+      lower += (all || (sg[c] & mask) >= prefix) ? 1u : 0u;
+    uint32_t lower_tot;
+    block_exclusive_scan<kClThreads>(lower, warp_tot, &lower_tot);
+    pos = lower_tot;
+    for (int q = 0; q < rank; ++q) pos += s_ps[q];
+  } else {
+    // ---- many candidates (heavy ties): refine the threshold 8 bits at a time,
+    // summing the CTAs' digit histograms through distributed shared memory
+    int hi = 52;
+    while (!all && hi >= 0) {
+      const int w = hi + 1 < 8 ? hi + 1 : 8;
+      const int sh = hi - w + 1;
+      const uint32_t dm = (1u << w) - 1u;
+      if (threadIdx.x < 256) hd[threadIdx.x] = 0u;
+      __syncthreads();
+      const int cround = ((static_cast<int>(ncand) + 31) / 32) * 32;   // whole warps take part
+      for (int c = threadIdx.x; c < cround; c += kClThreads) {
+        uint32_t dg = 0xFFFFFFFFu;
+        if (c < static_cast<int>(ncand)) {
+          const unsigned long long cc = scand[c];
+          if ((cc & mask) == prefix) dg = static_cast<uint32_t>(cc >> sh) & dm;
+        }
+        hist_add_warp(hd, dg);
+      }
+      cluster.sync();                            // every CTA's digit histogram is complete
+      if (threadIdx.x < 256) {
+        uint32_t tot = 0;
+        for (int q = 0; q < ncta; ++q) tot += cluster.map_shared_rank(hd, q)[threadIdx.x];
+        h[threadIdx.x] = tot;
+      }
+      if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+      __syncthreads();
+      find_threshold_digit<kClThreads>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
+      need -= s_above;
+      prefix |= static_cast<unsigned long long>(s_d) << sh;
+      mask |= static_cast<unsigned long long>(dm) << sh;
+      all = (s_cnt == need);
+      cluster.sync();                            // peers are done reading hd
+      hi -= w;
+    }
+  }
+
+  // ---- selection bits: bins above the threshold bin, or in it with the
+  // determined composite bits at or above the threshold prefix
+  uint32_t selm[(PER + 31) / 32] = {};
+  uint32_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    if (j >= nval) break;
+    const uint32_t kb = key[j] >> (32 - kHistBits);
+    bool sel = kb > bin;
+    if (kb == bin) {
+      const unsigned long long cc = (static_cast<unsigned long long>(key[j]) << 32) |
+                                    (0xFFFFFFFFull - static_cast<uint32_t>(t0 + tb + j));
+      sel = (cc & mask) >= prefix;
+    }
+    if (sel) {
+      selm[j >> 5] |= 1u << (j & 31);
+      ++mine;
+    }
+  }
+  uint32_t total;
+  pos += block_exclusive_scan<kClThreads>(mine, warp_tot, &total);
+  if (!gather) {
+    if (threadIdx.x == 0) s_count = total;
+    cluster.sync();                              // every CTA's count is published
+    for (int q = 0; q < rank; ++q) pos += *cluster.map_shared_rank(&s_count, q);
+  }
+#pragma unroll
+  for (int wd = 0; wd < (PER + 31) / 32; ++wd) {
+    uint32_t bits = selm[wd];
+    while (bits) {
+      const int j = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < static_cast<uint32_t>(ri.keff)) out[pos] = t0 + tb + wd * 32 + j;
+      ++pos;
+    }
   }
   if (rank == 0)
     for (int i = ri.keff + threadIdx.x; i < p.k; i += kClThreads) out[i] = -1;
-  cluster.sync();                                // peers may still read this CTA's s_count
+  if (!gather) cluster.sync();                   // peers may still read this CTA's s_count
 }
 
-// CTAs per row for the cluster select (0: the row is too long for it).
+// Cluster shape for rows of up to max_n keys: keys per thread and CTAs per
+// row (0 CTAs: the row is too long for the cluster select).
+static void cluster_shape(int max_n, int* per, int* ctas) {
+  // as few keys per thread as up to 16 CTAs allow: the slice load from L2 and
+  // the per-thread work shrink with the slice
+  *per = max_n <= 16 * 8 * kClThreads ? 8 : max_n <= 16 * 16 * kClThreads ? 16 : 32;
+  *ctas = (max_n + *per * kClThreads - 1) / (*per * kClThreads);
+  if (*ctas > kTopkClusterMax) *ctas = 0;
+}
+
+bool topk_cluster_feasible(int max_n) {
+  int per, ctas;
+  cluster_shape(max_n, &per, &ctas);
+  if (ctas <= 8) return ctas > 0;
+  static int cached[64][3] = {};   // per device: PER 8 / 16 / 32 -> 1 ok, 2 not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const int pi = per == 8 ? 0 : per == 16 ? 1 : 2;
+  if (cached[dev][pi]) return cached[dev][pi] == 1;
+  const size_t smem = (static_cast<size_t>(per) * kClThreads + kClGatherMax) * sizeof(unsigned long long);
+  auto kern = per == 8 ? topk_cluster_select_kernel<8>
+            : per == 16 ? topk_cluster_select_kernel<16> : topk_cluster_select_kernel<32>;
+  bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) == cudaSuccess &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1);
+    cfg.blockDim = dim3(kClThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
+  }
+  cudaGetLastError();
+  cached[dev][pi] = ok ? 1 : 2;
+  return ok;
+}
+
 int topk_cluster_ctas(int max_n) {
-  const int nch = (max_n + kChunk - 1) / kChunk;
-  const int ctas = nch < kTopkClusterMax ? nch : kTopkClusterMax;
-  const int slice = (max_n + ctas - 1) / ctas;
-  return slice <= kTopkClusterSlice ? ctas : 0;
+  int per, ctas;
+  cluster_shape(max_n, &per, &ctas);
+  return ctas;
 }
 
 cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
                                        cudaStream_t stream) {
-  const int ctas = topk_cluster_ctas(max_n);
+  int per, ctas;
+  cluster_shape(max_n, &per, &ctas);
   if (ctas == 0) return cudaErrorInvalidValue;
-  const int slice = (((max_n + ctas - 1) / ctas) + 31) & ~31;
-  const size_t smem = static_cast<size_t>(slice) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_cluster_select_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // worst case every key of the slice is a candidate; then the gathered list
+  const size_t smem = (static_cast<size_t>(per) * kClThreads + kClGatherMax) * sizeof(unsigned long long);
+  auto kern = per == 8 ? topk_cluster_select_kernel<8>
+            : per == 16 ? topk_cluster_select_kernel<16> : topk_cluster_select_kernel<32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  if (ctas > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, p.nrows);
   cfg.blockDim = dim3(kClThreads);
@@ -523,7 +753,8 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, topk_cluster_select_kernel, p, slice);
+  if (ctas > 8 && !topk_cluster_feasible(max_n)) return cudaErrorNotSupported;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,

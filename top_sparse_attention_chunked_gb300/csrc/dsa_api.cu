@@ -108,6 +108,22 @@ int make_map_rows64(CUtensorMap* m, const void* base, long long rows, int box_ro
   return DSA_OK;
 }
 
+// rows x 128 16-bit matrix (one KV head of one token per row), box 64 x 1,
+// 128-byte swizzle: the source of TMA row gathers
+int make_map_kv_rows(CUtensorMap* m, const void* base, long long rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(DSA_HEAD_DIM), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(DSA_HEAD_DIM) * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled (KV rows) failed (%d)", (int)r);
+  return DSA_OK;
+}
+
 // ------------------------------------------------------------------ problem checks
 struct Derived {
   int rows = 0;        // B * S
@@ -369,7 +385,10 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
   const int row_max = topk_row_max_len(di.smem_optin);
   if (!hist_ready && prefer_rows && d.max_n <= row_max) {
     timing_before(DSA_KERNEL_TOPK_ROW, st);
-    e = launch_topk_row(tp, d.max_n, di.smem_optin, after_kernel, st);
+    if (topk_row_reg_per(d.max_n) > 0)
+      e = launch_topk_row_reg(tp, d.max_n, after_kernel, st);
+    else
+      e = launch_topk_row(tp, d.max_n, di.smem_optin, after_kernel, st);
     timing_after(DSA_KERNEL_TOPK_ROW, st);
     if (e != cudaSuccess) return cuda_fail(e, "top-k row launch");
     return DSA_OK;
@@ -440,9 +459,17 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.cluster = attn_uses_cluster(ap.nsplit) ? 1 : 0;
   cudaError_t e;
   timing_before(DSA_KERNEL_ATTENTION, st);
-  if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin))
-    e = launch_prefill_tc(ap, p->kv_dtype, di.sms, at<uint32_t>(ws, 0), st);
-  else
+  if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin)) {
+    CUtensorMap tm_k, tm_v;
+    const long long rows = static_cast<long long>(p->batch) * p->cache_capacity * p->num_kv_heads;
+    int rc = make_map_kv_rows(&tm_k, k, rows);
+    if (rc == DSA_OK) rc = make_map_kv_rows(&tm_v, v, rows);
+    if (rc != DSA_OK) {
+      timing_after(DSA_KERNEL_ATTENTION, st);
+      return rc;
+    }
+    e = launch_prefill_tc(ap, p->kv_dtype, di.sms, tm_k, tm_v, at<uint32_t>(ws, 0), st);
+  } else
     e = launch_attention(ap, p->q_dtype, p->kv_dtype, p->out_dtype, st);
   timing_after(DSA_KERNEL_ATTENTION, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -452,6 +479,9 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
 bool prefill_tc_ok(const dsa_problem* p, const Derived& d, const DeviceInfo& di) {
   AttnParams ap{};
   ap.topk = p->top_k;
+  ap.B = p->batch;
+  ap.cap = p->cache_capacity;
+  ap.Hkv = p->num_kv_heads;
   (void)d;
   return prefill_tc_supported(ap, p->kv_dtype, di.smem_optin);
 }

@@ -93,6 +93,10 @@ constexpr int kTopkClusterMax = 16;
 int topk_cluster_ctas(int max_n);   // 0 if the row is too long for it
 cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
                                        cudaStream_t stream);
+// Whole-row select with the keys in registers: keys per thread for rows of
+// up to max_n keys (0 if too long).
+int topk_row_reg_per(int max_n);
+cudaError_t launch_topk_row_reg(const TopkParams& p, int max_n, bool pdl, cudaStream_t stream);
 // Longest row the shared-memory whole-row select handles.
 int topk_row_max_len(size_t smem_limit);
 
@@ -135,7 +139,7 @@ bool topk_cluster_feasible(int max_n);
 
 // tcgen05 prefill attention (BF16 / FP16 cache, top_k <= 2048)
 bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin);
-cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, uint32_t* status,
-                              cudaStream_t stream);
+cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, uint32_t* status, cudaStream_t stream);
 
 }  // namespace dsa

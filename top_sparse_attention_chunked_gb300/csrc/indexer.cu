@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       tc_fence_after();
       const int t = c.kt * kKeyTile + quarter * 32 + lane;
       const int T = p.lens.T[c.b];
+      float* srow = p.scores + (static_cast<size_t>(c.b) * p.S + c.qb * QB) * p.cap + t;
 #pragma unroll 1
       for (int jq = 0; jq < QB; jq += C::QG) {
         float v[C::QG][16];
@@ -329,12 +330,20 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         for (int g = 0; g < C::QG; ++g) {
           const int s = c.qb * QB + jq + g;
           if (s >= p.S) break;
-          const float* wv = wv_warp + (jq + g) * DSA_IDX_HEADS;
-          float acc = 0.0f;
+          // sum over heads of w_h * ReLU(dot_h), two heads per paired FMA
+          const float4* wv4 = reinterpret_cast<const float4*>(wv_warp + (jq + g) * DSA_IDX_HEADS);
+          float2 acc2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int h = 0; h < DSA_IDX_HEADS; ++h) acc = fmaf(wv[h], fmaxf(v[g][h], 0.0f), acc);
+          for (int h4 = 0; h4 < DSA_IDX_HEADS / 4; ++h4) {
+            const float4 w4 = wv4[h4];
+            acc2 = fma_f32x2(make_float2(w4.x, w4.y),
+                             make_float2(fmaxf(v[g][4 * h4], 0.0f), fmaxf(v[g][4 * h4 + 1], 0.0f)), acc2);
+            acc2 = fma_f32x2(make_float2(w4.z, w4.w),
+                             make_float2(fmaxf(v[g][4 * h4 + 2], 0.0f), fmaxf(v[g][4 * h4 + 3], 0.0f)), acc2);
+          }
+          const float acc = acc2.x + acc2.y;
           const bool valid = t < visible_len(T, p.S, s);
-          if (valid) p.scores[(static_cast<size_t>(c.b) * p.S + s) * p.cap + t] = acc;
+          if (valid) srow[static_cast<size_t>(jq + g) * p.cap] = acc;
           if constexpr (HIST) {
             // plain shared atomics: cheaper than warp-aggregating each update
             if (valid) atomicAdd(&sHist[(jq + g) * kHistBins + (float_key(acc) >> (32 - kHistBits))], 1u);

@@ -19,10 +19,13 @@
 //   3. PV^T: for each tile of 128 gathered V rows, read MN-major (head dim
 //      contiguous) as the A operand, tcgen05.mma accumulates O^T[128 dims x 16
 //      heads] in tensor memory; the epilogue divides by the row sums and stores.
-// Four loader warps gather the selected rows with 16-byte cp.async straight
-// into the swizzled operand layout and signal a ring of shared stages; one
-// warp issues the MMAs and owns tensor memory. A persistent grid of one CTA per
-// SM walks the work items.
+// Four loader warps gather the selected rows with TMA row gathers (four rows
+// of 128 bytes per instruction, 128-byte swizzle applied by the copy engine)
+// into a ring of shared stages; a single warp issues row gathers at only a
+// fraction of the L2 bandwidth, so each loader warp fills a quarter of every
+// tile. One warp issues the MMAs and owns tensor memory. A persistent grid of two CTAs
+// per SM (256 tensor-memory columns and ~112 KB of shared memory each) walks
+// the work items, so one CTA's gather overlaps the other's softmax and MMAs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -33,22 +36,24 @@
 namespace dsa {
 
 namespace pf {
-constexpr int kThreads = 320;          // warp 0 MMA, warp 1 idle, 2-5 softmax, 6-9 loaders
+constexpr int kThreads = 288;          // warp 0 MMA, warps 1-4 softmax, warps 5-8 loaders
+constexpr int kLoadWarps = 4;
 constexpr int kKeys = 128;             // keys per tile (MMA M for QK^T, K for PV^T)
 constexpr int kMaxTiles = 16;          // 2,048 selected keys
-constexpr int kStages = 5;
+constexpr int kStages = 3;             // two CTAs share an SM
 constexpr uint32_t kTileBytes = kKeys * DSA_HEAD_DIM * 2;   // 32 KB: 2 column blocks of 16 KB
 constexpr uint32_t kBlockBytes = kKeys * 128;               // one 64-wide column block
 constexpr uint32_t kQBytes = 16 * DSA_HEAD_DIM * 2;         // 4 KB
 constexpr uint32_t kPBytes = 16 * kKeys * 2;                // 4 KB: [16 heads x 128 keys]
-constexpr int kLogitCols = kMaxTiles * 16;                  // 256
-constexpr int kOCol = kLogitCols;                           // O^T after the logits
-constexpr uint32_t kTmemCols = 512;
+// 16 logit tiles x 16 columns fill the 256 columns; O^T reuses the first
+// logit tile's columns: PV(0) writes them only after P(0) has been formed
+constexpr int kOCol = 0;
+constexpr uint32_t kTmemCols = 256;
 
 struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t q_ready, logits_ready, o_ready, tmem_free;
-  uint64_t p_ready[2], p_free[2];
+  uint64_t p_ready, p_free;
   uint64_t done;
   uint64_t grp;          // barrier of the 128 softmax threads
   uint32_t tmem_base;
@@ -56,7 +61,7 @@ struct Bars {
   float red[2][4][16];   // cross-warp max / sum scratch
 };
 
-constexpr size_t kSmemBytes = 1024 + kStages * kTileBytes + kQBytes + 4 * kPBytes + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + kStages * kTileBytes + kQBytes + 2 * kPBytes + sizeof(Bars);
 }  // namespace pf
 
 // Shared-memory descriptor with explicit leading/stride byte offsets and
@@ -118,34 +123,35 @@ __device__ __forceinline__ PfItem pf_item(const AttnParams& p, long long it) {
   return w;
 }
 
+// tm_k / tm_v view the caches as [B * cap * Hkv rows, 128] 16-bit matrices
+// (row (b * cap + key) * Hkv + g), box 64 x 1, 128-byte swizzle.
 template <bool F16>
-__global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel(const AttnParams p,
-                                                                                  long long n_items,
-                                                                                  uint32_t* status) {
+__global__ void __launch_bounds__(pf::kThreads, 2)
+    sparse_attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                  const __grid_constant__ CUtensorMap tm_v, const AttnParams p,
+                                  long long n_items, uint32_t* status) {
   using namespace pf;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sKV = base;                                 // kStages x 32 KB
   uint8_t* sQ = sKV + kStages * kTileBytes;            // 4 KB
-  uint8_t* sP = sQ + kQBytes;                          // [2 buffers][hi, lo] x 4 KB
-  Bars* bars = reinterpret_cast<Bars*>(sP + 4 * kPBytes);
+  uint8_t* sP = sQ + kQBytes;                          // [hi, lo] x 4 KB
+  Bars* bars = reinterpret_cast<Bars*>(sP + 2 * kPBytes);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&bars->full[i], 128);
+      mbar_init(&bars->full[i], kLoadWarps);
       mbar_init(&bars->empty[i], 1);
     }
     mbar_init(&bars->q_ready, 128);
     mbar_init(&bars->logits_ready, 1);
     mbar_init(&bars->o_ready, 1);
     mbar_init(&bars->tmem_free, 128);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->p_ready[i], 128);
-      mbar_init(&bars->p_free[i], 1);
-    }
+    mbar_init(&bars->p_ready, 128);
+    mbar_init(&bars->p_free, 1);
     mbar_init(&bars->done, 1);
     mbar_init(&bars->grp, 128);
     bars->abort_flag = 0;
@@ -159,56 +165,70 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
   const long long my_first = blockIdx.x;
   const long long stride = gridDim.x;
 
-  if (warp >= 6) {
+  if (warp >= 5) {
     // ------------------------------------------------------------ loaders
+    const int lw = warp - 5;
+    if (threadIdx.x == 160) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
     pdl_wait();      // the selected indices come from the previous kernel
-    const int lt = threadIdx.x - 192;    // 0..127: one key row per thread
+    // lanes 0-15 issue one gather each per tile: rows 4 * grp .. 4 * grp + 3
+    // of the tile, column block cb
+    const int grp = lw * 8 + (lane & 7);
+    const int cb = (lane >> 3) & 1;
+    const bool issuer = lane < 16;
     long long seq = 0;                   // position in the ring (tiles issued)
-    long long arrived = 0;
-    const size_t kv_tok = static_cast<size_t>(p.Hkv) * DSA_HEAD_DIM;
-    const uint16_t* Kb = static_cast<const uint16_t*>(p.k);
-    const uint16_t* Vb = static_cast<const uint16_t*>(p.v);
     bool ok = true;
     for (long long it = my_first; it < n_items && ok; it += stride) {
       const PfItem w = pf_item(p, it);
       const int b = w.r / p.S;
+      const int T = p.lens.T[b];
       const int32_t* idx_row = p.idx + static_cast<size_t>(w.r) * p.topk;
+      // rows past k_eff (and any index outside the visible cache) read key 0,
+      // whose logits the softmax masks
+      auto rows_of = [&](int t, int* y) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = t * kKeys + 4 * grp + e;
+          int key = j < w.keff ? __ldg(idx_row + j) : 0;
+          if (key < 0 || key >= T) key = 0;
+          y[e] = (b * p.cap + key) * p.Hkv + w.g;
+        }
+      };
       for (int pass = 0; pass < 2 && ok; ++pass) {            // K tiles, then V tiles
-        const uint16_t* src = pass == 0 ? Kb : Vb;
+        const CUtensorMap* tm = pass == 0 ? &tm_k : &tm_v;
+        int nxt[4];
+        if (issuer) rows_of(0, nxt);
         for (int t = 0; t < w.ntiles; ++t) {
+          const int y0 = nxt[0], y1 = nxt[1], y2 = nxt[2], y3 = nxt[3];
+          if (issuer && t + 1 < w.ntiles) rows_of(t + 1, nxt);
           const int st = static_cast<int>(seq % kStages);
-          if (seq >= kStages &&
-              !mbar_wait_bounded(&bars->empty[st], static_cast<uint32_t>(((seq / kStages) - 1) & 1),
-                                 abort_flag)) {
+          bool got = seq < kStages ||
+                     mbar_wait_bounded(&bars->empty[st],
+                                       static_cast<uint32_t>(((seq / kStages) - 1) & 1), abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
-          const int j = t * kKeys + lt;
-          int key = j < w.keff ? idx_row[j] : -1;
-          if (key >= p.lens.T[b]) key = -1;
-          const uint16_t* row = src + (static_cast<size_t>(b) * p.cap + (key < 0 ? 0 : key)) * kv_tok +
-                                static_cast<size_t>(w.g) * DSA_HEAD_DIM;
-          uint8_t* dst = sKV + st * kTileBytes;
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            cp_async16(dst + sw128_off(lt, c * 8, kKeys), row + c * 8, key >= 0);
-          cp_async_commit();
+          if (lane == 0) mbar_arrive_expect_tx(&bars->full[st], kTileBytes / kLoadWarps);
+          __syncwarp();
+          if (issuer)
+            tma_gather4(sKV + st * kTileBytes + cb * kBlockBytes + grp * 512, tm, &bars->full[st],
+                        cb * 64, y0, y1, y2, y3);
           ++seq;
-          // signal the tile issued two groups ago
-          if (seq - arrived > 2) {
-            cp_async_wait<2>();
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->full[arrived % kStages]);
-            ++arrived;
-          }
         }
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    while (arrived < seq) {
-      mbar_arrive(&bars->full[arrived % kStages]);
-      ++arrived;
+    if (lane == 0) {
+      // the ring's last copies may still be landing (the consumers may have
+      // given up): wait, bounded, for them before the block can exit
+      for (long long s2 = seq > kStages ? seq - kStages : 0; s2 < seq; ++s2) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&bars->full[s2 % kStages], static_cast<uint32_t>((s2 / kStages) & 1)) &&
+               clock64() - t0 < kWaitBudgetCycles) {
+        }
+      }
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -252,14 +272,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
             ok = false;
             break;
           }
-          const int pb = static_cast<int>(ptile & 1);
-          if (!mbar_wait_bounded(&bars->p_ready[pb], static_cast<uint32_t>((ptile >> 1) & 1), abort_flag)) {
+          if (!mbar_wait_bounded(&bars->p_ready, static_cast<uint32_t>(ptile & 1), abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t v0 = smem_u32(sKV + st * kTileBytes);
-          const uint32_t ph = smem_u32(sP + (2 * pb) * kPBytes);
+          const uint32_t ph = smem_u32(sP);
           const uint32_t pl = ph + kPBytes;
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
               tc_mma_f16(tmem + kOCol, adesc, desc_sw128(pl + poff, 16, 1024), id_pv, 1u);
           }
           tc_commit(&bars->empty[st]);
-          tc_commit(&bars->p_free[pb]);
+          tc_commit(&bars->p_free);
         }
         if (!ok) break;
         tc_commit(&bars->o_ready);
@@ -282,9 +301,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
       while (!mbar_try_wait(&bars->done, 0) && clock64() - t0 < kWaitBudgetCycles) {
       }
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 1) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int et = threadIdx.x - 64;          // 0..127
+    const int et = threadIdx.x - 32;          // 0..127
     const int quarter = warp & 3;
     const int key_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
@@ -345,7 +364,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
         for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
       if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < 16; ++h) bars->red[0][warp - 2][h] = mx[h];
+        for (int h = 0; h < 16; ++h) bars->red[0][warp - 1][h] = mx[h];
       }
       if (!group_sync(&bars->grp, &gphase, abort_flag)) break;
       float M[16];
@@ -359,15 +378,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
 #pragma unroll
       for (int h = 0; h < 16; ++h) lsum[h] = 0.0f;
       for (int t = 0; t < w.ntiles; ++t, ++ptile) {
-        const int pb = static_cast<int>(ptile & 1);
-        if (ptile >= 2 &&
-            !mbar_wait_bounded(&bars->p_free[pb], static_cast<uint32_t>(((ptile >> 1) - 1) & 1), abort_flag))
+        if (ptile >= 1 &&
+            !mbar_wait_bounded(&bars->p_free, static_cast<uint32_t>((ptile - 1) & 1), abort_flag))
           break;
         float v[16];
         tmem_ld16(tmem + lane_addr + t * 16, v);
         tmem_ld_wait();
         const bool valid = t * kKeys + key_in_tile < w.keff;
-        uint8_t* ph = sP + (2 * pb) * kPBytes;
+        uint8_t* ph = sP;
         uint8_t* pl = ph + kPBytes;
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
@@ -383,7 +401,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bars->p_ready[pb]);
+        mbar_arrive(&bars->p_ready);
       }
       // ---- row sums
 #pragma unroll
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
         for (int o = 16; o > 0; o >>= 1) lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], o);
       if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < 16; ++h) bars->red[1][warp - 2][h] = lsum[h];
+        for (int h = 0; h < 16; ++h) bars->red[1][warp - 1][h] = lsum[h];
       }
       if (!group_sync(&bars->grp, &gphase, abort_flag)) break;
       // ---- O^T: TMEM lane = head dim, columns = heads
@@ -429,28 +447,31 @@ __global__ void __launch_bounds__(pf::kThreads, 1) sparse_attn_prefill_tc_kernel
 }
 
 bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin) {
+  // gather row coordinates are signed 32-bit
+  const long long rows = static_cast<long long>(p.B) * p.cap * p.Hkv;
   return (kv_dtype == DSA_BF16 || kv_dtype == DSA_FP16) && p.topk <= pf::kMaxTiles * pf::kKeys &&
-         pf::kSmemBytes <= smem_optin;
+         rows < (1LL << 31) && pf::kSmemBytes <= smem_optin;
 }
 
-cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, uint32_t* status,
-                              cudaStream_t stream) {
+cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, uint32_t* status, cudaStream_t stream) {
   const long long n_items = static_cast<long long>(p.B) * p.S * p.Hkv * p.HG;
-  const int grid = static_cast<int>(n_items < sms ? n_items : sms);
+  // two CTAs per SM: one gathers while the other computes
+  const int grid = static_cast<int>(n_items < 2 * sms ? n_items : 2 * sms);
   if (kv_dtype == DSA_FP16) {
     auto k = sparse_attn_prefill_tc_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::kSmemBytes));
     if (e != cudaSuccess) return e;
-    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, p, n_items,
-                         status);
+    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, tm_k, tm_v, p,
+                         n_items, status);
   } else {
     auto k = sparse_attn_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::kSmemBytes));
     if (e != cudaSuccess) return e;
-    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, p, n_items,
-                         status);
+    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, tm_k, tm_v, p,
+                         n_items, status);
   }
 }
 

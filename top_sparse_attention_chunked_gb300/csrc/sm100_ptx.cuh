@@ -89,6 +89,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* map, uin
       : "memory");
 }
 
+// Row gather: rows y0..y3 of a 2D tensor map whose box is one row high, columns
+// x .. x + box - 1 of each, into four consecutive box-sized slots at smem_dst
+// (swizzled by the map's mode from the slot addresses), completing the bytes
+// on `bar`.
+__device__ __forceinline__ void tma_gather4(void* smem_dst, const void* map, uint64_t* bar, int x,
+                                            int y0, int y1, int y2, int y3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Tensor-memory allocation by one full warp; the base address lands in *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -173,6 +186,19 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- paired fp32
+// d = a * b + c on two fp32 lanes at once (sm_100 family), round to nearest.
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
 }
 
 // ---------------------------------------------------------------- PDL

@@ -354,6 +354,222 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
   for (int i = ri.keff + threadIdx.x; i < p.k; i += kRowThreads) out[i] = -1;
 }
 
+constexpr int kClThreads = 512;
+constexpr int kClGatherMax = 8192;   // candidates gathered into every CTA of the cluster
+
+// Exact threshold over a list of candidate composites held by this CTA:
+// refines (prefix, mask) until `need` candidates are at or above it.
+// `hi` is the highest composite bit not yet fixed by (prefix, mask).
+template <int NT>
+__device__ void local_composite_select(const unsigned long long* list, int n,
+                                       unsigned long long* prefix, unsigned long long* mask,
+                                       uint32_t need, uint32_t* h, uint32_t* warp_tot, int* sd,
+                                       uint32_t* sabove, uint32_t* scnt, int hi = 52) {
+  bool all = false;
+  while (!all && hi >= 0) {
+    const int w = hi + 1 < 11 ? hi + 1 : 11;
+    const int sh = hi - w + 1;
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < (1 << w); i += NT) h[i] = 0u;
+    __syncthreads();
+    for (int c = threadIdx.x; c < n; c += NT) {
+      const unsigned long long cc = list[c];
+      if ((cc & *mask) == *prefix) atomicAdd(&h[static_cast<uint32_t>(cc >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
+    __syncthreads();
+    find_threshold_digit<NT>(h, 1 << w, need, warp_tot, sd, sabove, scnt);
+    need -= *sabove;
+    *prefix |= static_cast<unsigned long long>(*sd) << sh;
+    *mask |= static_cast<unsigned long long>(dm) << sh;
+    all = (*scnt == need);
+    __syncthreads();
+    hi -= w;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3b. whole-row select with the keys in registers (one CTA per row, up to
+// 40,960 keys). Warp w owns keys [w * 32 * PER, (w + 1) * 32 * PER) and lane l
+// holds key w * 32 * PER + 32 * i + l in key[i]. A sample of the row (every
+// 16th key) gives a provisional threshold theta a little below the k-th key;
+// the keys at or above theta (a few thousand) are resolved exactly in shared
+// memory. If the sample misleads (fewer than k keys at or above theta, or too
+// many), the threshold is found by radix passes over all keys instead. The
+// selection is emitted in index order with one scan over the warps' counts.
+// ---------------------------------------------------------------------------
+constexpr int kRrThreads = 512;
+constexpr int kRrWarps = kRrThreads / 32;
+constexpr int kRrCandMax = 4096;
+constexpr int kRrMaxPer = 80;
+
+template <int PER>
+__global__ void __launch_bounds__(kRrThreads) topk_row_reg_kernel(const TopkParams p) {
+  __shared__ uint32_t h[kHistBins];
+  __shared__ unsigned long long scand[kRrCandMax];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ uint32_t s_wcnt[kRrWarps];
+  __shared__ int s_d;
+  __shared__ uint32_t s_above, s_cnt;
+
+  const int r = blockIdx.x;
+  pdl_wait();      // scores come from the previous kernel
+  pdl_trigger();
+  const RowInfo ri = row_info(p, r);
+  const int n = ri.n, keff = ri.keff;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wbase = warp * 32 * PER;
+  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
+  uint32_t key[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int t = wbase + 32 * i + lane;
+    key[i] = t < n ? float_key(__ldcg(row + t)) : 0u;
+  }
+  auto valid = [&](int i) { return wbase + 32 * i + lane < n; };
+  auto comp = [&](int i) {
+    return (static_cast<unsigned long long>(key[i]) << 32) |
+           (0xFFFFFFFFull - static_cast<uint32_t>(wbase + 32 * i + lane));
+  };
+
+  // ---- provisional threshold from a sample
+  for (int i = threadIdx.x; i < kHistBins; i += kRrThreads) h[i] = 0u;
+  if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+  __syncthreads();
+  uint32_t nsmp = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    if (((i + lane) & 15) == 0 && valid(i)) {
+      atomicAdd(&h[key[i] >> 21], 1u);
+      ++nsmp;
+    }
+  uint32_t ns;
+  block_exclusive_scan<kRrThreads>(nsmp, warp_tot, &ns);
+  // target rank in the sample: 25 % and 16 keys of slack above k's share
+  uint32_t rs = static_cast<uint32_t>((static_cast<unsigned long long>(keff) * ns * 5 + 4ull * n - 1) /
+                                      (4ull * n)) + 16u;
+  if (rs > ns) rs = ns;
+  uint32_t theta = 0;
+  if (rs > 0) {
+    find_threshold_digit<kRrThreads>(h, kHistBins, rs, warp_tot, &s_d, &s_above, &s_cnt);
+    const uint32_t b1 = static_cast<uint32_t>(s_d);
+    const uint32_t need2 = rs - s_above;
+    for (int i = threadIdx.x; i < kHistBins; i += kRrThreads) h[i] = 0u;
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (((i + lane) & 15) == 0 && valid(i) && (key[i] >> 21) == b1)
+        atomicAdd(&h[(key[i] >> 10) & 0x7FFu], 1u);
+    __syncthreads();
+    find_threshold_digit<kRrThreads>(h, kHistBins, need2, warp_tot, &s_d, &s_above, &s_cnt);
+    theta = (b1 << 21) | (static_cast<uint32_t>(s_d) << 10);
+  }
+  // ---- keys at or above theta
+  uint32_t mine = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mine += (valid(i) && key[i] >= theta) ? 1u : 0u;
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) s_wcnt[warp] = mine;
+  __syncthreads();
+  uint32_t c = 0, wb = 0;
+  for (int w = 0; w < kRrWarps; ++w) {
+    if (w == warp) wb = c;
+    c += s_wcnt[w];
+  }
+  unsigned long long prefix = 0ull, mask = 0ull;
+  const bool use_cand = c >= static_cast<uint32_t>(keff) && c <= static_cast<uint32_t>(kRrCandMax);
+  // only keys at or above theta can be selected on the candidate path (the
+  // resolve may stop at a prefix that keys below theta share)
+  const uint32_t floor_key = use_cand ? theta : 0u;
+  if (use_cand) {
+    // few candidates: gather their composites and resolve exactly
+    uint32_t off = wb;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const bool f = valid(i) && key[i] >= theta;
+      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      if (f) scand[off + __popc(bal & ((1u << lane) - 1u))] = comp(i);
+      off += __popc(bal);
+    }
+    __syncthreads();
+    local_composite_select<kRrThreads>(scand, static_cast<int>(c), &prefix, &mask,
+                                       static_cast<uint32_t>(keff), h, warp_tot, &s_d, &s_above,
+                                       &s_cnt, 63);
+  } else {
+    // the sample misled: radix passes over every key (11 composite bits each)
+    uint32_t need = static_cast<uint32_t>(keff);
+    bool all = false;
+    int hi = 63;
+    while (!all && hi >= 0) {
+      const int w = hi + 1 < 11 ? hi + 1 : 11;
+      const int sh = hi - w + 1;
+      const uint32_t dm = (1u << w) - 1u;
+      for (int i = threadIdx.x; i < (1 << w); i += kRrThreads) h[i] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const unsigned long long cc = comp(i);
+        const uint32_t dg = (valid(i) && (cc & mask) == prefix)
+                                ? static_cast<uint32_t>(cc >> sh) & dm : 0xFFFFFFFFu;
+        hist_add_warp(h, dg);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+      __syncthreads();
+      find_threshold_digit<kRrThreads>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
+      need -= s_above;
+      prefix |= static_cast<unsigned long long>(s_d) << sh;
+      mask |= static_cast<unsigned long long>(dm) << sh;
+      all = (s_cnt == need);
+      __syncthreads();
+      hi -= w;
+    }
+  }
+  // ---- emit the selection in index order
+  __syncthreads();
+  mine = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i)
+    mine += (valid(i) && key[i] >= floor_key && (comp(i) & mask) >= prefix) ? 1u : 0u;
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) s_wcnt[warp] = mine;
+  __syncthreads();
+  uint32_t pos = 0;
+  for (int w = 0; w < warp; ++w) pos += s_wcnt[w];
+  int32_t* out = p.idx + static_cast<size_t>(r) * p.k;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const bool f = valid(i) && key[i] >= floor_key && (comp(i) & mask) >= prefix;
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    const uint32_t at = pos + __popc(bal & ((1u << lane) - 1u));
+    if (f && at < static_cast<uint32_t>(keff)) out[at] = wbase + 32 * i + lane;
+    pos += __popc(bal);
+  }
+  for (int i = keff + threadIdx.x; i < p.k; i += kRrThreads) out[i] = -1;
+}
+
+int topk_row_reg_per(int max_n) {
+  const int per = (max_n + kRrThreads - 1) / kRrThreads;
+  const int per16 = ((per + 15) / 16) * 16;
+  return per16 <= kRrMaxPer ? per16 : 0;
+}
+
+cudaError_t launch_topk_row_reg(const TopkParams& p, int max_n, bool pdl, cudaStream_t stream) {
+  const int per = topk_row_reg_per(max_n);
+  void (*kern)(const TopkParams) = nullptr;
+  switch (per) {
+    case 16: kern = topk_row_reg_kernel<16>; break;
+    case 32: kern = topk_row_reg_kernel<32>; break;
+    case 48: kern = topk_row_reg_kernel<48>; break;
+    case 64: kern = topk_row_reg_kernel<64>; break;
+    case 80: kern = topk_row_reg_kernel<80>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  return launch_kernel(kern, dim3(p.B * p.S), dim3(kRrThreads), 0, stream, pdl, p);
+}
+
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
@@ -383,40 +599,6 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
 // block scan) at the offset given by the peers' selected counts. No global
 // scratch beyond the histogram and no serial tail.
 // ---------------------------------------------------------------------------
-constexpr int kClThreads = 512;
-constexpr int kClGatherMax = 8192;   // candidates gathered into every CTA of the cluster
-
-// Exact threshold over a list of candidate composites held by this CTA:
-// refines (prefix, mask) until `need` candidates are at or above it.
-__device__ void local_composite_select(const unsigned long long* list, int n,
-                                       unsigned long long* prefix, unsigned long long* mask,
-                                       uint32_t need, uint32_t* h, uint32_t* warp_tot, int* sd,
-                                       uint32_t* sabove, uint32_t* scnt) {
-  int hi = 52;
-  bool all = false;
-  while (!all && hi >= 0) {
-    const int w = hi + 1 < 11 ? hi + 1 : 11;
-    const int sh = hi - w + 1;
-    const uint32_t dm = (1u << w) - 1u;
-    for (int i = threadIdx.x; i < (1 << w); i += kClThreads) h[i] = 0u;
-    __syncthreads();
-    for (int c = threadIdx.x; c < n; c += kClThreads) {
-      const unsigned long long cc = list[c];
-      if ((cc & *mask) == *prefix) atomicAdd(&h[static_cast<uint32_t>(cc >> sh) & dm], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
-    __syncthreads();
-    find_threshold_digit<kClThreads>(h, 1 << w, need, warp_tot, sd, sabove, scnt);
-    need -= *sabove;
-    *prefix |= static_cast<unsigned long long>(*sd) << sh;
-    *mask |= static_cast<unsigned long long>(dm) << sh;
-    all = (*scnt == need);
-    __syncthreads();
-    hi -= w;
-  }
-}
-
 // Each thread owns PER consecutive keys of the slice, held in registers
 // (PER = 8, 16 or 32), so the emit needs a single block scan and no
 // shared-memory bank conflicts arise; the threshold-bin candidates go to
@@ -583,7 +765,8 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
     }
     cluster.sync();                              // every CTA is done reading its peers
     if (!all)
-      local_composite_select(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above, &s_cnt);
+      local_composite_select<kClThreads>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
+                                         &s_cnt);
     // selected keys in the lower slices: their sure keys plus their candidates
     // at or above the threshold
     uint32_t lower = 0;

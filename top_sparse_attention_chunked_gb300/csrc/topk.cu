@@ -389,6 +389,41 @@ __device__ void local_composite_select(const unsigned long long* list, int n,
   }
 }
 
+// Refines the threshold among n composites in shared memory whose bits above
+// `hi` are fixed by prefix/mask, 11 bits per round: the block histograms the
+// composites that match the prefix, one warp picks the digit. `hbuf` is 2,048
+// words of 16-byte-aligned shared scratch.
+template <int NT>
+__device__ void resolve_composites(const unsigned long long* list, int n, unsigned long long* prefix,
+                                   unsigned long long* mask, uint32_t need, uint32_t* hbuf, int* sd,
+                                   uint32_t* sabove, uint32_t* scnt, int hi) {
+  bool all = false;
+  while (!all && hi >= 0) {
+    const int w = hi + 1 < 11 ? hi + 1 : 11;
+    const int sh = hi - w + 1;
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < kHistBins; i += NT) hbuf[i] = 0u;
+    __syncthreads();
+    for (int c = threadIdx.x; c < n; c += NT) {
+      const unsigned long long cc = list[c];
+      if ((cc & *mask) == *prefix) atomicAdd(&hbuf[static_cast<uint32_t>(cc >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+      int d;
+      uint32_t ab, ct;
+      warp_find_threshold<kHistBins>(hbuf, need, &d, &ab, &ct);
+      if (threadIdx.x == 0) { *sd = d; *sabove = ab; *scnt = ct; }
+    }
+    __syncthreads();
+    need -= *sabove;
+    *prefix |= static_cast<unsigned long long>(*sd) << sh;
+    *mask |= static_cast<unsigned long long>(dm) << sh;
+    all = (*scnt == need);
+    hi -= w;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 3b. whole-row select with the keys in registers (one CTA per row, up to
 // 40,960 keys). Warp w owns keys [w * 32 * PER, (w + 1) * 32 * PER) and lane l
@@ -604,12 +639,12 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
 // shared-memory bank conflicts arise; the threshold-bin candidates go to
 // shared memory.
 template <int PER>
-__global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(const TopkParams p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int kSlice = PER * kClThreads;
   extern __shared__ unsigned long long scand[];  // candidate composites of this CTA
-  __shared__ uint32_t h[kHistBins];              // row histogram, then digit totals
+  __shared__ __align__(16) uint32_t h[kHistBins];   // row histogram, then digit counts
   __shared__ uint32_t hloc[kHistBins];           // this CTA's slice histogram
   __shared__ uint32_t hred[kHistBins];           // the range of bins this CTA sums
   __shared__ uint32_t hd[256];                   // this CTA's digit histogram
@@ -623,6 +658,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
   const int rl = blockIdx.y, r = p.row0 + rl;
   const int rank = static_cast<int>(cluster.block_rank());
   const int ncta = static_cast<int>(cluster.num_blocks());
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();      // scores and the histogram come from the previous kernel
   pdl_trigger();
   const RowInfo ri = row_info(p, r);
@@ -647,7 +683,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
     for (int j = 0; j < PER; ++j) key[j] = tb + j < m ? float_key(__ldcg(src + j)) : 0u;
   }
   const int nval = max(0, min(PER, m - tb));     // valid keys of this thread
-  if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; s_count = 0; }
+  if (threadIdx.x == 0) { s_count = 0; s_ncand = 0; s_nsure = 0; }
   if (p.hist_ready) {
     // ---- the row histogram came with the scores (indexer epilogue)
     const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
@@ -682,14 +718,21 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
     }
     __syncthreads();
   }
-  find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
-                                   &s_above, &s_cnt);
+  // ---- threshold bin: one warp scans the histogram
+  if (warp == 0) {
+    int d;
+    uint32_t ab, ct;
+    warp_find_threshold<kHistBins>(h, static_cast<uint32_t>(ri.keff), &d, &ab, &ct);
+    if (lane == 0) { s_d = d; s_above = ab; s_cnt = ct; }
+  }
+  __syncthreads();
   const uint32_t bin = static_cast<uint32_t>(s_d);
   uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
-  bool all = (need == s_cnt);
+  const bool all0 = (need == s_cnt);             // the whole threshold bin is selected
+  bool all = all0;
 
   // ---- candidates (this thread's keys in the threshold bin) and sure keys
-  // (above it); candidates are compacted with a block scan (no atomics)
+  // (above it); each warp reserves its candidates' slots with one atomic
   uint32_t cmask[(PER + 31) / 32] = {};
   uint32_t ncmine = 0, nsure = 0;
 #pragma unroll
@@ -703,22 +746,25 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
         ++nsure;
       }
     }
-  uint32_t ncand = 0, nsure_cta = 0;
   {
-    // one scan of both counts packed in 16-bit halves (a CTA has <= 16,384 keys)
-    uint32_t both;
-    uint32_t cpos = block_exclusive_scan<kClThreads>(ncmine | (nsure << 16), warp_tot, &both) & 0xFFFFu;
-    ncand = both & 0xFFFFu;
-    nsure_cta = both >> 16;
+    uint32_t incl = ncmine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t wbase = 0;
+    if (lane == 31 && incl) wbase = atomicAdd(&s_ncand, incl);
+    uint32_t cpos = __shfl_sync(0xffffffffu, wbase, 31) + incl - ncmine;
 #pragma unroll
     for (int j = 0; j < PER; ++j)
       if ((cmask[j >> 5] >> (j & 31)) & 1u)
         scand[cpos++] = (static_cast<unsigned long long>(key[j]) << 32) |
                         (0xFFFFFFFFull - static_cast<uint32_t>(t0 + tb + j));
-  }
-  if (threadIdx.x == 0) {
-    s_ncand = ncand;
-    s_nsure = nsure_cta;
+    uint32_t ns = nsure;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ns += __shfl_xor_sync(0xffffffffu, ns, o);
+    if (lane == 0 && ns) atomicAdd(&s_nsure, ns);
   }
   unsigned long long prefix = static_cast<unsigned long long>(bin) << 53;
   unsigned long long mask = ~0ull << 53;
@@ -729,6 +775,7 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
   cluster.sync();                                // candidates and counts are published
 
   uint32_t pos = 0;                              // this CTA's first output slot
+  int off_mine = 0;                              // gathered candidates of lower ranks
   if (gather) {
     // ---- every CTA gathers all candidates and counts, then resolves locally
     unsigned long long* sg = scand + PER * kClThreads;   // gathered candidates
@@ -737,48 +784,44 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
       s_ps[threadIdx.x] = *cluster.map_shared_rank(&s_nsure, threadIdx.x);
     }
     __syncthreads();
-    int off = 0, off_mine = 0;
+    int off = 0;
     for (int q = 0; q < ncta; ++q) {
       if (q == rank) off_mine = off;
       off += static_cast<int>(s_pc[q]);
+      if (q < rank) pos += s_ps[q] + (all0 ? s_pc[q] : 0u);
     }
-    if (!all) {
-      // entry e of the concatenated lists: up to kClGatherMax / 512 = 16 per
-      // thread, all loads in flight before the stores
-      constexpr int kG = kClGatherMax / kClThreads;
-      unsigned long long v[kG];
+    if (!all0) {
+      // warp q copies peer q's list (at most 16 peers, 16 warps), four
+      // loads in flight per lane
+      if (warp < ncta) {
+        int base = 0;
+        for (int q = 0; q < warp; ++q) base += static_cast<int>(s_pc[q]);
+        const int cnt = static_cast<int>(s_pc[warp]);
+        const unsigned long long* peer = cluster.map_shared_rank(scand, warp);
+        for (int i0 = 0; i0 < cnt; i0 += 128) {
+          unsigned long long v[4];
 #pragma unroll
-      for (int k = 0; k < kG; ++k) {
-        const int e = k * kClThreads + threadIdx.x;
-        v[k] = 0ull;
-        if (e < off) {
-          int q = 0, base = 0;
-          while (e >= base + static_cast<int>(s_pc[q])) base += static_cast<int>(s_pc[q++]);
-          v[k] = cluster.map_shared_rank(scand, q)[e - base];
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 32 + lane;
+            v[u] = i < cnt ? peer[i] : 0ull;
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * 32 + lane;
+            if (i < cnt) sg[base + i] = v[u];
+          }
         }
       }
-#pragma unroll
-      for (int k = 0; k < kG; ++k) {
-        const int e = k * kClThreads + threadIdx.x;
-        if (e < off) sg[e] = v[k];
-      }
+      __syncthreads();
     }
-    cluster.sync();                              // every CTA is done reading its peers
-    if (!all)
-      local_composite_select<kClThreads>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
-                                         &s_cnt);
-    // selected keys in the lower slices: their sure keys plus their candidates
-    // at or above the threshold
-    uint32_t lower = 0;
-    for (int c = threadIdx.x; c < off_mine; c += kClThreads)
-      lower += (all || (sg[c] & mask) >= prefix) ? 1u : 0u;
-    uint32_t lower_tot;
-    block_exclusive_scan<kClThreads>(lower, warp_tot, &lower_tot);
-    pos = lower_tot;
-    for (int q = 0; q < rank; ++q) pos += s_ps[q];
+    // this CTA is done reading its peers: arrive now, wait before exiting
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (!all0)
+      resolve_composites<kClThreads>(sg, off, &prefix, &mask, need, h, &s_d, &s_above, &s_cnt, 52);
   } else {
     // ---- many candidates (heavy ties): refine the threshold 8 bits at a time,
     // summing the CTAs' digit histograms through distributed shared memory
+    const uint32_t ncand = s_ncand;
     int hi = 52;
     while (!all && hi >= 0) {
       const int w = hi + 1 < 8 ? hi + 1 : 8;
@@ -814,7 +857,9 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
   }
 
   // ---- selection bits: bins above the threshold bin, or in it with the
-  // determined composite bits at or above the threshold prefix
+  // determined composite bits at or above the threshold prefix; one block
+  // scan gives both the in-CTA positions (low half) and, on the gather path,
+  // the lower ranks' selected candidates (high half)
   uint32_t selm[(PER + 31) / 32] = {};
   uint32_t mine = 0;
 #pragma unroll
@@ -832,10 +877,16 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
       ++mine;
     }
   }
+  uint32_t lower = 0;
+  if (gather && !all0) {
+    const unsigned long long* sg = scand + PER * kClThreads;
+    for (int c = threadIdx.x; c < off_mine; c += kClThreads) lower += (sg[c] & mask) >= prefix ? 1u : 0u;
+  }
   uint32_t total;
-  pos += block_exclusive_scan<kClThreads>(mine, warp_tot, &total);
+  const uint32_t packed = block_exclusive_scan<kClThreads>(mine | (lower << 16), warp_tot, &total);
+  pos += (packed & 0xFFFFu) + (total >> 16);
   if (!gather) {
-    if (threadIdx.x == 0) s_count = total;
+    if (threadIdx.x == 0) s_count = total & 0xFFFFu;
     cluster.sync();                              // every CTA's count is published
     for (int q = 0; q < rank; ++q) pos += *cluster.map_shared_rank(&s_count, q);
   }
@@ -851,7 +902,8 @@ __global__ void __launch_bounds__(kClThreads) topk_cluster_select_kernel(const T
   }
   if (rank == 0)
     for (int i = ri.keff + threadIdx.x; i < p.k; i += kClThreads) out[i] = -1;
-  if (!gather) cluster.sync();                   // peers may still read this CTA's s_count
+  if (gather) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  else cluster.sync();                           // peers may still read this CTA's s_count
 }
 
 // Cluster shape for rows of up to max_n keys: keys per thread and CTAs per

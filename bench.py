@@ -46,6 +46,33 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# ------------------------------------------------------------------ measured traffic
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one indexer
+# launch per workload, from an ncu capture of that launch at full size (see
+# profiles/). They hold for the indexer source they were taken on: when any of
+# these files changes, the figure is dropped (null) until it is measured again.
+TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh", "dsa_internal.h"]
+TRAFFIC_SOURCE_SHA = "df66407283e0dec9"
+INDEXER_TRAFFIC = {
+    "decode_4k": 573440,
+    "grouped_decode_32k": 16913920,
+    "decode_128k": 16826880,
+    "decode_256k_int8": 33626368,
+}
+
+
+def indexer_traffic(name):
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_sparse_attention_chunked_gb300", "csrc")
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != TRAFFIC_SOURCE_SHA:
+        return None
+    return INDEXER_TRAFFIC.get(name)
+
+
 # ------------------------------------------------------------------ algorithmic bytes
 def algorithmic_bytes(wl, idx_np=None):
     """Bytes the method itself must move per step (DRAM), excluding work the
@@ -244,10 +271,21 @@ def run_libdsa(args, wl):
         call(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"], dev["k_scale"],
              dev["v_scale"], idx, out, ws)
 
+    if args.profile_calls:
+        # untimed calls only, for an ncu capture of the step's kernels
+        for _ in range(args.profile_calls):
+            step()
+        torch.cuda.synchronize()
+        assert D.dsa_read_device_status(ws) == 0
+        if rank == 0:
+            print(json.dumps({"profile_calls": args.profile_calls, "workload": wl.name,
+                              "kernels_per_step": D.dsa_last_launches()}), flush=True)
+        return
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     assert D.dsa_read_device_status(ws) == 0
+    kernels_per_step = D.dsa_last_launches()   # what one call enqueues
     graph = None
 
     def capture():
@@ -381,7 +419,8 @@ def run_libdsa(args, wl):
         achieved = ab["indexer"] / (idx_us * 1e-6) / 1e9
         roof = {"kernel": "indexer_tc_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes": ab["indexer"],
+                "peak_kind": peak_kind, "traffic": indexer_traffic(wl.name),
+                "algorithmic_bytes": ab["indexer"],
                 "launch_us": round(idx_us, 2)}
     if rank == 0:
         line = {
@@ -400,10 +439,10 @@ def run_libdsa(args, wl):
             "cpu_baseline": cpu_base,
             "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
-            "gpu_launches": 3 * args.steps,
-            "kernels_per_step": ["indexer_tc_kernel",
-                                 "topk_row_kernel" if prefill else "topk_chunk_select_kernel",
-                                 "sparse_attn_prefill_tc_kernel" if prefill else "sparse_attn_kernel"],
+            # the library's own count of the kernels one call enqueues, times
+            # the timed steps of the headline loop
+            "gpu_launches": len(kernels_per_step) * args.steps,
+            "kernels_per_step": kernels_per_step,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -420,11 +459,25 @@ def main():
     ap.add_argument("--workload", default="decode_128k")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="run this many untimed calls and exit (for ncu captures)")
+    ap.add_argument("--q-len", type=int, default=0,
+                    help="with --profile-calls: query tokens per sequence of a reduced case")
+    ap.add_argument("--context", type=int, default=0,
+                    help="with --profile-calls: cache length of a reduced case")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     from dsa_inputs import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.profile_calls and (args.q_len or args.context):
+        # a reduced case of the same structure (heads, top_k, dtypes)
+        from dsa_inputs import small_workload
+        wl = small_workload(name=f"{wl.name}_reduced", batch=wl.batch,
+                            q_len=args.q_len or wl.q_len, total_len=args.context or wl.total_len,
+                            num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                            top_k=wl.top_k, q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype,
+                            bias_frac=wl.bias_frac, seed=wl.seed)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

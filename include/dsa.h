@@ -249,6 +249,17 @@ const char* dsa_status_string(int status);
 int dsa_version(void);
 
 /*
+ * dsa_last_launches -- the kernels that the last dsa_index_scores, dsa_topk,
+ * dsa_topk_noalloc, dsa_sparse_attn_decode or dsa_sparse_attn_prefill call on
+ * this host thread enqueued. Returns how many (0 after a call that failed
+ * before launching); when buf is not NULL, writes their names in launch order,
+ * comma-separated and NUL-terminated, truncated to fit buflen bytes. No
+ * counterpart in the pages: an accounting aid (a benchmark reports how many
+ * of the library's kernels one step runs).
+ */
+int dsa_last_launches(char* buf, size_t buflen);
+
+/*
  * Kernel timing (diagnostics). dsa_timing_select(kind) makes the following
  * calls on this host thread record a pair of CUDA events around every launch
  * of one kernel kind (DSA_KERNEL_*) on the caller's stream (-1 turns it off;

@@ -579,7 +579,7 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
   if (!p.cluster)
-    return launch_kernel(kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true, p);
+    return launch_kernel("sparse_attn_kernel", kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true, p);
   if (p.nsplit > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -598,7 +598,9 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e == cudaSuccess) note_launch("sparse_attn_kernel");
+  return e;
 }
 
 template <int KV, bool Q_F16>

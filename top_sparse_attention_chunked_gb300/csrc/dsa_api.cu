@@ -16,6 +16,20 @@ thread_local std::string g_err;
 thread_local int g_timing_kind = -1;
 thread_local cudaEvent_t g_ev[2] = {nullptr, nullptr};
 thread_local bool g_ev_recorded = false;
+constexpr int kLaunchLog = 16;
+thread_local int g_nlaunch = 0;                       // kernels of the current call
+thread_local const char* g_launch[kLaunchLog] = {};
+
+}  // namespace
+
+void note_launch(const char* name) {
+  if (g_nlaunch < kLaunchLog) g_launch[g_nlaunch] = name;
+  ++g_nlaunch;
+}
+
+void reset_launches() { g_nlaunch = 0; }
+
+namespace {
 
 int fail(int status, const char* fmt, ...) {
   char buf[512];
@@ -508,6 +522,7 @@ int check_attn_ptrs(const dsa_problem* p, const void* q, const void* qI, const f
 int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const float* w,
               const void* kI, const void* k, const void* v, const float* ks, const float* vs,
               int32_t* idx_out, void* out, void* ws, size_t ws_bytes, void* stream) {
+  reset_launches();
   Derived d;
   int rc = check_problem(p, op, &d);
   if (rc) return rc;
@@ -555,6 +570,7 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
 int noalloc_fail(int status, const char* msg) { return fail(status, "%s", msg); }
 
 int noalloc_check_topk(const dsa_problem* p, int* rows, int* max_n) {
+  reset_launches();
   Derived d;
   const int rc = check_problem(p, DSA_OP_TOPK, &d);
   if (rc) return rc;
@@ -608,6 +624,7 @@ size_t dsa_workspace_size(const dsa_problem* p, int op) {
 
 int dsa_index_scores(const dsa_problem* p, const void* qI, const float* w, const void* kI,
                      float* scores, void* ws, size_t ws_bytes, void* stream) {
+  reset_launches();
   Derived d;
   int rc = check_problem(p, DSA_OP_INDEX_SCORES, &d);
   if (rc) return rc;
@@ -628,6 +645,7 @@ int dsa_index_scores(const dsa_problem* p, const void* qI, const float* w, const
 
 int dsa_topk(const dsa_problem* p, const float* scores, int32_t* idx, void* ws, size_t ws_bytes,
              void* stream) {
+  reset_launches();
   Derived d;
   int rc = check_problem(p, DSA_OP_TOPK, &d);
   if (rc) return rc;
@@ -695,6 +713,20 @@ const char* dsa_status_string(int s) {
 }
 
 int dsa_version(void) { return 100; }
+
+int dsa_last_launches(char* buf, size_t buflen) {
+  if (buf && buflen > 0) {
+    size_t o = 0;
+    buf[0] = '\0';
+    const int n = g_nlaunch < kLaunchLog ? g_nlaunch : kLaunchLog;
+    for (int i = 0; i < n; ++i) {
+      const int w = snprintf(buf + o, buflen - o, "%s%s", i ? "," : "", g_launch[i]);
+      if (w < 0 || static_cast<size_t>(w) >= buflen - o) break;
+      o += static_cast<size_t>(w);
+    }
+  }
+  return g_nlaunch;
+}
 
 int dsa_timing_select(int kind) {
   if (kind < -1 || kind > DSA_KERNEL_ATTENTION) return fail(DSA_ERR_INVALID_ARG, "unknown kernel kind %d", kind);

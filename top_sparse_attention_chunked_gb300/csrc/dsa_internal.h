@@ -10,12 +10,18 @@
 
 namespace dsa {
 
-// Launch `kern` on `stream`; with `pdl` the launch may overlap the tail of the
+// Kernels enqueued by the current public call on this host thread, in order
+// (reported by dsa_last_launches). Every launch site records its kernel's name
+// once the launch has been accepted.
+void note_launch(const char* name);
+void reset_launches();
+
+// Launch `kern` (recorded as `name`) on `stream`; with `pdl` the launch may overlap the tail of the
 // previous kernel in the stream (the kernel calls pdl_wait() before reading
 // what that kernel wrote).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t stream, bool pdl, Args... args) {
+cudaError_t launch_kernel(const char* name, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                          size_t smem, cudaStream_t stream, bool pdl, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -26,7 +32,9 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+  if (e == cudaSuccess) note_launch(name);
+  return e;
 }
 
 constexpr int kChunk = DSA_CHUNK;          // 2,048-key chunks (indexer + top-k)

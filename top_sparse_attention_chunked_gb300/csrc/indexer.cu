@@ -393,7 +393,7 @@ __global__ void zero_scratch_kernel(uint4* base, long long n16) {
 cudaError_t launch_zero_scratch(void* base, size_t bytes, cudaStream_t stream) {
   const long long n16 = static_cast<long long>(bytes / 16);
   const int blocks = static_cast<int>(n16 / 256 + 1 < 64 ? n16 / 256 + 1 : 64);
-  return launch_kernel(zero_scratch_kernel, dim3(blocks), dim3(256), 0, stream, false,
+  return launch_kernel("zero_scratch_kernel", zero_scratch_kernel, dim3(blocks), dim3(256), 0, stream, false,
                        static_cast<uint4*>(base), n16);
 }
 
@@ -418,7 +418,8 @@ static cudaError_t launch_n(const IndexerParams& p, const CUtensorMap& tm_kI,
   if (e != cudaSuccess) return e;
   // with histograms the kernel follows the scratch-clearing kernel and waits
   // for it only before its final flush
-  return launch_kernel(kern, grid, dim3(kIdxThreads), smem, stream, HIST, tm_kI, tm_qI, p, stages);
+  return launch_kernel("indexer_tc_kernel", kern, grid, dim3(kIdxThreads), smem, stream, HIST, tm_kI,
+                       tm_qI, p, stages);
 }
 
 cudaError_t launch_indexer(const IndexerParams& p, const CUtensorMap& tm_kI,

@@ -463,14 +463,16 @@ cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, const 
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::kSmemBytes));
     if (e != cudaSuccess) return e;
-    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, tm_k, tm_v, p,
+    return launch_kernel("sparse_attn_prefill_tc_kernel", k, dim3(grid), dim3(pf::kThreads),
+                         pf::kSmemBytes, stream, true, tm_k, tm_v, p,
                          n_items, status);
   } else {
     auto k = sparse_attn_prefill_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pf::kSmemBytes));
     if (e != cudaSuccess) return e;
-    return launch_kernel(k, dim3(grid), dim3(pf::kThreads), pf::kSmemBytes, stream, true, tm_k, tm_v, p,
+    return launch_kernel("sparse_attn_prefill_tc_kernel", k, dim3(grid), dim3(pf::kThreads),
+                         pf::kSmemBytes, stream, true, tm_k, tm_v, p,
                          n_items, status);
   }
 }

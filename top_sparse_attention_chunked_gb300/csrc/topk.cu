@@ -602,14 +602,14 @@ cudaError_t launch_topk_row_reg(const TopkParams& p, int max_n, bool pdl, cudaSt
     case 80: kern = topk_row_reg_kernel<80>; break;
     default: return cudaErrorInvalidValue;
   }
-  return launch_kernel(kern, dim3(p.B * p.S), dim3(kRrThreads), 0, stream, pdl, p);
+  return launch_kernel("topk_row_reg_kernel", kern, dim3(p.B * p.S), dim3(kRrThreads), 0, stream, pdl, p);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream) {
-  return launch_kernel(topk_hist_kernel, dim3(p.nchunks, p.nrows), dim3(kHistThreads), 0, stream,
+  return launch_kernel("topk_hist_kernel", topk_hist_kernel, dim3(p.nchunks, p.nrows), dim3(kHistThreads), 0, stream,
                        false, p);
 }
 
@@ -619,7 +619,7 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_kernel(topk_chunk_select_kernel, dim3(p.nchunks, p.nrows), dim3(kSelThreads), smem,
+  return launch_kernel("topk_chunk_select_kernel", topk_chunk_select_kernel, dim3(p.nchunks, p.nrows), dim3(kSelThreads), smem,
                        stream, true, p);
 }
 
@@ -989,7 +989,9 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
   if (ctas > 8 && !topk_cluster_feasible(max_n)) return cudaErrorNotSupported;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, p);
+  if (le == cudaSuccess) note_launch("topk_cluster_select_kernel");
+  return le;
 }
 
 cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, bool pdl,
@@ -1000,7 +1002,7 @@ cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, b
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_kernel(topk_row_kernel, dim3(p.B * p.S), dim3(kRowThreads), smem, stream, pdl, p);
+  return launch_kernel("topk_row_kernel", topk_row_kernel, dim3(p.B * p.S), dim3(kRowThreads), smem, stream, pdl, p);
 }
 
 }  // namespace dsa

@@ -31,7 +31,8 @@ DSA_KERNEL_TOPK_ROW, DSA_KERNEL_ATTENTION = 3, 4
 EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill",
             "dsa_read_device_status", "dsa_last_error_string", "dsa_status_string",
-            "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc"]
+            "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc",
+            "dsa_last_launches"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -89,6 +90,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_last_error_string": (ctypes.c_char_p, []),
         "dsa_status_string": (ctypes.c_char_p, [i32]),
         "dsa_version": (i32, []),
+        "dsa_last_launches": (i32, [ctypes.c_char_p, ctypes.c_size_t]),
         "dsa_timing_select": (i32, [i32]),
         "dsa_timing_read": (i32, [ctypes.POINTER(ctypes.c_float)]),
         "dsa_topk_noalloc": (i32, [P, vp, vp, vp]),
@@ -258,6 +260,14 @@ def dsa_timing_read() -> float:
     ms = ctypes.c_float(0.0)
     _check(load_library().dsa_timing_read(ctypes.byref(ms)))
     return ms.value
+
+
+def dsa_last_launches() -> list:
+    """Names of the kernels the last library call on this thread enqueued."""
+    buf = ctypes.create_string_buffer(1024)
+    n = load_library().dsa_last_launches(buf, len(buf))
+    names = [x for x in buf.value.decode().split(",") if x]
+    return names if len(names) == n else names + ["?"] * (n - len(names))
 
 
 def dsa_version() -> int:

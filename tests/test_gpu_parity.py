@@ -302,7 +302,7 @@ def test_uniform_query_averages_selected_values(dsa):
 
 
 @pytest.mark.parametrize("spacing", [0, 14, 15, 16, 40, 100])
-@pytest.mark.parametrize("split", [16, 32, 2048])
+@pytest.mark.parametrize("split", [0, 16, 32, 2048])
 def test_int8_large_value_scale_worked_example(dsa, spacing, split):
     """PR #33847's case: logits 0 and 88, value codes 1 and 0, value scale
     2^120; expected 2^120 e^-88 / (1 + e^-88). Keys with logit -1000 pad the
@@ -344,3 +344,24 @@ def test_workspace_reuse_across_shapes(dsa):
                                    dev["v"], None, None, None, out, ws)
         outs.append(out.float().cpu())
     assert torch.equal(outs[0], outs[2])
+
+
+# ---------------------------------------------------------------- single-token decode
+@pytest.mark.parametrize("kv", ["bf16", "fp16", "int8"])
+def test_single_token_ragged_batch(dsa, kv):
+    wl = small_workload(batch=3, q_len=1, total_len=40000, capacity=40000, num_q_heads=24,
+                        num_kv_heads=2, top_k=2048, kv_dtype=kv, seed=31)
+    cpu = make_inputs(wl)
+    lens = [40000, 17, 25000]
+    cpu["total_len"] = torch.tensor(lens, dtype=torch.int32)
+    _, idx, out = run_step(dsa, wl, cpu=cpu, total_len=lens, out_dtype="fp32")
+    assert (idx[1, 0, :17] == np.arange(17)).all() and (idx[1, 0, 17:] == -1).all()
+    check_step(wl, cpu, idx, out)
+
+
+def test_single_token_topk_above_context(dsa):
+    wl = small_workload(batch=2, q_len=1, total_len=50, capacity=4096, top_k=4000, seed=41)
+    cpu, idx, out = run_step(dsa, wl)
+    for b in range(2):
+        assert idx[b, 0, :50].tolist() == list(range(50)) and (idx[b, 0, 50:] == -1).all()
+    check_step(wl, cpu, idx, out)

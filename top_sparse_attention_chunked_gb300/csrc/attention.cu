@@ -13,7 +13,9 @@
 // Layout of the work: one CTA per (split of the selected keys, KV head x group
 // of <= 16 query heads, query row). The group's query heads form the M = 16
 // rows of warp-level m16n8k16 MMAs; each warp gathers 16 selected rows of K
-// and V per tile with 16-byte cp.async into a swizzled double buffer, computes
+// and V per tile into a double buffer -- TMA row gathers (tile::gather4,
+// four rows per instruction, 128-byte swizzle applied by the copy engine) for
+// a 16-bit cache, 16-byte cp.async for INT8 codes -- computes
 // S = Q K^T (16 heads x 16 keys), the online softmax in registers, and
 // O += P V. Warps, then splits, are merged with an LSE combine whose scaling
 // never forms a subnormal factor (mul_exp2).
@@ -39,20 +41,34 @@ constexpr int kTileKeys = 16;
 constexpr int kD = DSA_HEAD_DIM;
 constexpr int kTile16 = kTileKeys * kD * 2;      // 4 KB: one 16-key tile, 16-bit
 constexpr int kTile8 = kTileKeys * kD;           // 2 KB: one 16-key tile, INT8
-// Per-warp shared memory. 16-bit caches: K stage 0/1, V stage 0/1 (4 x 4 KB).
-// INT8: converted K and V tiles (2 x 4 KB), code staging K 0/1, V 0/1
-// (4 x 2 KB) and the k/v scales of both stages (256 B).
-constexpr int kWarpSmem = 4 * kTile16 + 2 * 4 * kTileKeys * 4;
+// Per-warp shared memory, every tile 1024-byte aligned (the swizzle of the
+// row gathers follows the address bits). 16-bit caches: K stage 0/1, V stage
+// 0/1 (4 x 4 KB). INT8: converted K and V tiles (2 x 4 KB), code staging K
+// 0/1, V 0/1 (4 x 2 KB). The INT8 scales sit in static shared memory. Three
+// CTAs fit on an SM.
+constexpr int kWarpSmem = 4 * kTile16;
 // the split combine merges up to kAttnMaxSplits partial states
 constexpr int kMaxCombine = kAttnMaxSplits;
 constexpr int kMergeFloats = kAttnWarps * kPartialFloats + 2 * kMaxCombine * kAttnRows + 2 * kAttnRows;
-constexpr int kAttnSmem = (kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnWarps * kWarpSmem
-                                                                       : kMergeFloats * 4;
+constexpr int kAttnSmem = ((kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnWarps * kWarpSmem
+                                                                        : kMergeFloats * 4) +
+                          1024;   // slack to align the base to 1024 bytes
 
 enum { KV_BF16 = 0, KV_FP16 = 1, KV_INT8 = 2 };
 
-// byte offset of 16-byte chunk c of row r in a swizzled 16-bit tile
-__device__ __forceinline__ int swz(int r, int c) { return r * (kD * 2) + ((c ^ (r & 7)) << 4); }
+// Byte offset of 16-byte chunk c (0..15) of row r in a 16-row 16-bit tile:
+// two 64-column blocks of 16 x 128 B, chunk positions XOR-swizzled by the row
+// within each 128-byte row (the layout a 128-byte-swizzled TMA copy writes).
+__device__ __forceinline__ int swz(int r, int c) {
+  return ((c >> 3) << 11) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// Bounded wait used on the unwinding path: ignores the abort flag.
+__device__ __forceinline__ void mbar_drain_attn(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitBudgetCycles) return;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -148,14 +164,23 @@ __device__ __forceinline__ void combine_factors(const float* st, int stride, int
   sML[kAttnRows + row] = L;
 }
 
+// tm_k / tm_v view the caches as [B * cap * Hkv rows, 128] (16-bit: box 64 x 1;
+// INT8: box 128 x 1), 128-byte swizzle; row (b * cap + key) * Hkv + g.
 template <int KV, bool Q_F16, int OUT>
-__global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                   const __grid_constant__ CUtensorMap tm_v,
+                                                                   const AttnParams p) {
   constexpr bool QK_F16 = (KV == KV_FP16) || (KV == KV_INT8 && Q_F16);
   constexpr bool PV_F16 = (KV == KV_FP16);
   constexpr bool PV_SPLIT = !PV_F16;   // BF16 P as hi + lo
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   __shared__ int s_last;
   __shared__ int32_t s_idx[kAttnMaxSplitKeys];
+  __shared__ uint64_t s_bar[kAttnWarps][2];     // per warp and stage: the tile's rows landed
+  __shared__ int s_abort;
+  __shared__ float s_sc[kAttnWarps][64];        // INT8: [stage][k 16 | v 16] scales per warp
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates
@@ -180,14 +205,20 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   // INT8 only: converted tiles live in sK[0] / sK[1]'s space, staging after
   uint8_t* sKc[2] = {wsm + 2 * kTile16, wsm + 2 * kTile16 + kTile8};
   uint8_t* sVc[2] = {wsm + 3 * kTile16, wsm + 3 * kTile16 + kTile8};
-  float* sSc = reinterpret_cast<float*>(wsm + 4 * kTile16);   // [stage][k 16 | v 16]
+  float* sSc = s_sc[warp];
+  if (lane == 0) {
+    mbar_init(&s_bar[warp][0], 1);
+    mbar_init(&s_bar[warp][1], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) s_abort = 0;
 
   const int32_t* idx_row = p.idx + static_cast<size_t>(r) * p.topk + split_begin;
-  const size_t kv_row_elems = static_cast<size_t>(p.Hkv) * kD;   // per cache token
-  const size_t kv_base = (static_cast<size_t>(b) * p.cap) * kv_row_elems + static_cast<size_t>(g) * kD;
   const size_t sc_base = static_cast<size_t>(b) * p.cap * p.Hkv + g;
 
-  // gather the 16 selected rows of tile `it` (this warp's it-th tile) into stage st
+  // gather the 16 selected rows of tile `it` (this warp's it-th tile) into
+  // stage st: lane l < 16 holds key l's row; rows past the split (and any
+  // index outside the visible cache) read key 0, whose logits are masked
   auto issue_tile = [&](int it, int st) {
     const int tile = warp + it * kAttnWarps;
     const int o = tile * kTileKeys;
@@ -197,6 +228,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       if (key < 0 || key >= T) key = -1;
     }
     if constexpr (KV == KV_INT8) {
+      // INT8 rows (128 B): 16-byte cp.async measured faster here than row
+      // gathers; codes and scales land zero-filled for invalid keys
       const int8_t* kb = static_cast<const int8_t*>(p.k);
       const int8_t* vb = static_cast<const int8_t*>(p.v);
 #pragma unroll
@@ -204,7 +237,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
         const int j = lane + 32 * i;            // 0..127: row j/8, chunk j%8
         const int row = j >> 3, c = j & 7;
         const int kr = __shfl_sync(0xffffffffu, key, row);
-        const size_t off = kv_base + static_cast<size_t>(kr < 0 ? 0 : kr) * kv_row_elems + c * 16;
+        const size_t off = ((static_cast<size_t>(b) * p.cap + (kr < 0 ? 0 : kr)) * p.Hkv + g) * kD + c * 16;
         cp_async16(sKc[st] + row * kD + c * 16, kb + off, kr >= 0);
         cp_async16(sVc[st] + row * kD + c * 16, vb + off, kr >= 0);
       }
@@ -213,17 +246,20 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       if (lane < 16) cp_async4(sSc + st * 32 + lane, p.k_scale + so, kr >= 0);
       else cp_async4(sSc + st * 32 + lane, p.v_scale + so, kr >= 0);
     } else {
-      const uint16_t* kb = static_cast<const uint16_t*>(p.k);
-      const uint16_t* vb = static_cast<const uint16_t*>(p.v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int j = lane + 32 * i;            // 0..255: row j/16, chunk j%16
-        const int row = j >> 4, c = j & 15;
-        const int kr = __shfl_sync(0xffffffffu, key, row);
-        const size_t off = kv_base + static_cast<size_t>(kr < 0 ? 0 : kr) * kv_row_elems + c * 8;
-        cp_async16(sK[st] + swz(row, c), kb + off, kr >= 0);
-        cp_async16(sV[st] + swz(row, c), vb + off, kr >= 0);
-      }
+      // 16-bit rows (256 B): TMA row gathers, lane l of the first 16 issuing
+      // one for 4 rows (grp) of one column block (blk) of K or V (tsr)
+      const int yrow = (b * p.cap + (key < 0 ? 0 : key)) * p.Hkv + g;
+      const int grp = lane & 3, blk = (lane >> 2) & 1, tsr = lane >> 3;
+      const int y0 = __shfl_sync(0xffffffffu, yrow, 4 * grp);
+      const int y1 = __shfl_sync(0xffffffffu, yrow, 4 * grp + 1);
+      const int y2 = __shfl_sync(0xffffffffu, yrow, 4 * grp + 2);
+      const int y3 = __shfl_sync(0xffffffffu, yrow, 4 * grp + 3);
+      if (lane == 0) mbar_arrive_expect_tx(&s_bar[warp][st], 2 * kTile16);
+      __syncwarp();
+      if (lane < 16)
+        tma_gather4((tsr ? sV[st] : sK[st]) + blk * 2048 + grp * 512,
+                    tsr ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k),
+                    &s_bar[warp][st], blk * 64, y0, y1, y2, y3);
     }
   };
 
@@ -249,6 +285,10 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
       qa[kk][3] = ok1 ? load_q2<Q_F16, QK_F16>(p.q, qrow1 + c + 8) : 0u;
     }
   }
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
   pdl_wait();       // the selected indices come from the previous kernel
   pdl_trigger();
   // the split's selected indices, loaded once (all loads in flight together)
@@ -256,12 +296,22 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
   __syncthreads();
   if (my_tiles > 0) issue_tile(0, 0);
   cp_async_commit();
+  int issued = my_tiles > 0 ? 1 : 0, landed = 0;
 
   for (int it = 0; it < my_tiles; ++it) {
     const int st = it & 1;
-    if (it + 1 < my_tiles) issue_tile(it + 1, st ^ 1);
+    if (it + 1 < my_tiles) {
+      issue_tile(it + 1, st ^ 1);
+      ++issued;
+    }
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<1>();   // INT8 tiles
+    if constexpr (KV != KV_INT8) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_bar[warp][st],
+                                                      static_cast<uint32_t>((it >> 1) & 1), &s_abort)))
+        break;
+    }
+    landed = it + 1;
     __syncwarp();
     const int tile = warp + it * kAttnWarps;
     const int nvalid = min(kTileKeys, split_len - tile * kTileKeys);
@@ -405,6 +455,11 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     __syncwarp();
   }
   cp_async_wait<0>();
+  // after a wait that gave up, let this warp's copies land before the
+  // buffers are reused
+  if (KV != KV_INT8 && landed < issued && lane == 0)
+    for (int t = landed; t < issued; ++t)
+      mbar_drain_attn(&s_bar[warp][t & 1], static_cast<uint32_t>((t >> 1) & 1));
 
   // ---- merge the warps of this CTA
 #pragma unroll
@@ -413,6 +468,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
     l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], 2);
   }
   __syncthreads();   // stage buffers become the merge area
+  if (threadIdx.x == 0 && s_abort && p.status) atomicOr(p.status, kDevTimeout);
   float* ws = reinterpret_cast<float*>(smem);      // [warps][kPartialFloats]
   float* fac1 = ws + kAttnWarps * kPartialFloats;  // [max(warps, splits)][16]
   float* fac2 = fac1 + kMaxCombine * kAttnRows;
@@ -573,13 +629,15 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const AttnPar
 }
 
 template <int KV, bool Q_F16, int OUT>
-static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
+static cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                            cudaStream_t stream) {
   auto kern = sparse_attn_kernel<KV, Q_F16, OUT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
   if (!p.cluster)
-    return launch_kernel("sparse_attn_kernel", kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true, p);
+    return launch_kernel("sparse_attn_kernel", kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true,
+                         tm_k, tm_v, p);
   if (p.nsplit > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -598,17 +656,18 @@ static cudaError_t launch_t(const AttnParams& p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, p);
+  e = cudaLaunchKernelEx(&cfg, kern, tm_k, tm_v, p);
   if (e == cudaSuccess) note_launch("sparse_attn_kernel");
   return e;
 }
 
 template <int KV, bool Q_F16>
-static cudaError_t launch_out(const AttnParams& p, int out_dtype, cudaStream_t stream) {
+static cudaError_t launch_out(const AttnParams& p, int out_dtype, const CUtensorMap& tm_k,
+                              const CUtensorMap& tm_v, cudaStream_t stream) {
   switch (out_dtype) {
-    case DSA_BF16: return launch_t<KV, Q_F16, DSA_BF16>(p, stream);
-    case DSA_FP16: return launch_t<KV, Q_F16, DSA_FP16>(p, stream);
-    case DSA_FP32: return launch_t<KV, Q_F16, DSA_FP32>(p, stream);
+    case DSA_BF16: return launch_t<KV, Q_F16, DSA_BF16>(p, tm_k, tm_v, stream);
+    case DSA_FP16: return launch_t<KV, Q_F16, DSA_FP16>(p, tm_k, tm_v, stream);
+    case DSA_FP32: return launch_t<KV, Q_F16, DSA_FP32>(p, tm_k, tm_v, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -644,18 +703,18 @@ int attn_max_cluster() {
 }
 
 cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
-                             cudaStream_t stream) {
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream) {
   const bool qf16 = (q_dtype == DSA_FP16);
   switch (kv_dtype) {
     case DSA_BF16:
       if (qf16) return cudaErrorInvalidValue;
-      return launch_out<KV_BF16, false>(p, out_dtype, stream);
+      return launch_out<KV_BF16, false>(p, out_dtype, tm_k, tm_v, stream);
     case DSA_FP16:
-      return qf16 ? launch_out<KV_FP16, true>(p, out_dtype, stream)
-                  : launch_out<KV_FP16, false>(p, out_dtype, stream);
+      return qf16 ? launch_out<KV_FP16, true>(p, out_dtype, tm_k, tm_v, stream)
+                  : launch_out<KV_FP16, false>(p, out_dtype, tm_k, tm_v, stream);
     case DSA_INT8:
-      return qf16 ? launch_out<KV_INT8, true>(p, out_dtype, stream)
-                  : launch_out<KV_INT8, false>(p, out_dtype, stream);
+      return qf16 ? launch_out<KV_INT8, true>(p, out_dtype, tm_k, tm_v, stream)
+                  : launch_out<KV_INT8, false>(p, out_dtype, tm_k, tm_v, stream);
     default:
       return cudaErrorInvalidValue;
   }

@@ -471,6 +471,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.q_dtype = p->q_dtype;
   ap.out_dtype = p->out_dtype;
   ap.cluster = attn_uses_cluster(ap.nsplit) ? 1 : 0;
+  ap.status = at<uint32_t>(ws, 0);
   cudaError_t e;
   timing_before(DSA_KERNEL_ATTENTION, st);
   if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin)) {
@@ -483,8 +484,25 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
       return rc;
     }
     e = launch_prefill_tc(ap, p->kv_dtype, di.sms, tm_k, tm_v, at<uint32_t>(ws, 0), st);
-  } else
-    e = launch_attention(ap, p->q_dtype, p->kv_dtype, p->out_dtype, st);
+  } else {
+    // row gathers (16-bit caches) address rows with signed 32-bit coordinates
+    const long long rows = static_cast<long long>(p->batch) * p->cache_capacity * p->num_kv_heads;
+    if (p->kv_dtype != DSA_INT8 && rows >= (1LL << 31)) {
+      timing_after(DSA_KERNEL_ATTENTION, st);
+      return fail(DSA_ERR_UNSUPPORTED, "batch * cache_capacity * num_kv_heads must be below 2^31");
+    }
+    CUtensorMap tm_k{}, tm_v{};   // INT8 caches are gathered with cp.async
+    int rc = DSA_OK;
+    if (p->kv_dtype != DSA_INT8) {
+      rc = make_map_kv_rows(&tm_k, k, rows);
+      if (rc == DSA_OK) rc = make_map_kv_rows(&tm_v, v, rows);
+    }
+    if (rc != DSA_OK) {
+      timing_after(DSA_KERNEL_ATTENTION, st);
+      return rc;
+    }
+    e = launch_attention(ap, p->q_dtype, p->kv_dtype, p->out_dtype, tm_k, tm_v, st);
+  }
   timing_after(DSA_KERNEL_ATTENTION, st);
   if (e != cudaSuccess) return cuda_fail(e, "attention launch");
   return DSA_OK;

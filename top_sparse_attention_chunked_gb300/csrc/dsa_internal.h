@@ -124,6 +124,7 @@ struct AttnParams {
   int cluster;             // nsplit in {2,4,8,16}: splits merged inside a thread-block cluster
   int q_dtype, out_dtype;
   float scale_log2;        // softmax_scale * log2(e)
+  uint32_t* status;        // device status word (a bounded wait that ran out)
   SeqLens lens;
 };
 
@@ -132,8 +133,10 @@ constexpr int kAttnMaxSplits = 128;                             // split-K parti
 constexpr int kAttnMaxSplitKeys = 2048;                         // selected keys per split CTA
 constexpr int kPartialFloats = 2 * kAttnRows + kAttnRows * DSA_HEAD_DIM;  // m, l, o
 
+// tm_k / tm_v: the caches as [B * cap * Hkv, 128] rows, 128-byte swizzle,
+// box of one row (16-bit: 64 columns; INT8: 128 columns)
 cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
-                             cudaStream_t stream);
+                             const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream);
 
 // Largest thread-block cluster the split-K attention can use on this device
 // (16 if a 16-CTA cluster can be placed, else 8), and whether a split count

@@ -234,6 +234,30 @@ def config_of(wl, graph):
             "cuda_graph": bool(graph)}
 
 
+# ------------------------------------------------------------------ replicas
+# Multi-GPU runs are independent replicas of the workload (the method has no
+# exchange step): one process per GPU, each with its own seeded inputs; the
+# job's time is the slowest rank's and its throughput counts every rank.
+def replica_seed(wl, rank):
+    return wl.seed + 7919 * rank
+
+
+def slowest_rank_ms(ms, world, device=None):
+    """The largest per-step time over all ranks (every rank receives it)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world, query_tokens, ms):
+    """Query tokens per second processed by all ranks together."""
+    return world * query_tokens / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ libdsa arm
 def run_libdsa(args, wl):
     import numpy as np
@@ -254,7 +278,7 @@ def run_libdsa(args, wl):
     D.load_library()
     dev_index = torch.cuda.current_device()
 
-    cpu = make_inputs(wl, seed=wl.seed + 7919 * rank)   # an independent replica per rank
+    cpu = make_inputs(wl, seed=replica_seed(wl, rank))   # an independent replica per rank
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
     p = D.problem_for(wl)
     ws = D.alloc_workspace(p, D.DSA_OP_PREFILL if wl.q_len > 16 else D.DSA_OP_DECODE)
@@ -339,11 +363,7 @@ def run_libdsa(args, wl):
     clocks.start()
     step_ms, _ = timed_loop(False)
     clk = clocks.stop()
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank_ms(statistics.mean(step_ms), world, device="cuda")
     # the roofline loop: same steps with events recorded around the indexer
     D.dsa_timing_select(D.DSA_KERNEL_INDEXER)
     graph = capture() if args.graph else None
@@ -352,7 +372,7 @@ def run_libdsa(args, wl):
     idx_np = idx.cpu().numpy()
     ab = algorithmic_bytes(wl, idx_np)
     hbm, bf16, peak_kind = peaks()
-    value = world * wl.query_tokens / (ms / 1e3)
+    value = whole_job_value(world, wl.query_tokens, ms)
 
     # ---------------- per-kernel breakdown (separate short eager loop)
     per_kernel = {}
@@ -393,7 +413,8 @@ def run_libdsa(args, wl):
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e = world * wl.query_tokens / (statistics.mean(e2e_ms) / 1e3)
+    e2e = whole_job_value(world, wl.query_tokens,
+                          slowest_rank_ms(statistics.mean(e2e_ms), world, device="cuda"))
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu_base = None

@@ -116,9 +116,12 @@ __device__ __forceinline__ void warp_find_threshold(const uint32_t* h, uint32_t 
   const int b0 = NB - (lane + 1) * PL;        // lowest bin of this lane's run
   const uint4* hv = reinterpret_cast<const uint4*>(h + b0);
   uint32_t s = 0;
+  // the lanes' runs are PL words apart, which maps every lane to the same
+  // banks; each lane starts its run at a different chunk so that a warp-wide
+  // 16-byte load touches every bank group (4 wavefronts instead of 32)
 #pragma unroll
   for (int i = 0; i < PL / 4; ++i) {
-    const uint4 v = hv[i];
+    const uint4 v = hv[(i + lane) % (PL / 4)];
     s += v.x + v.y + v.z + v.w;
   }
   uint32_t incl = s;

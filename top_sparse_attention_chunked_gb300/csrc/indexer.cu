@@ -89,8 +89,9 @@ struct IdxCfg {
   static constexpr int NACC = N <= 64 ? 4 : 2;
   static constexpr uint32_t kTmemCols = (NACC * N <= 32) ? 32 : (NACC * N <= 64) ? 64
                                       : (NACC * N <= 128) ? 128 : (NACC * N <= 256) ? 256 : 512;
-  // queries whose accumulator columns are read per tcgen05.ld batch
-  static constexpr int QG = QB < 4 ? QB : 4;
+  // queries whose accumulator columns are read per tcgen05.ld batch (two
+  // batches in flight: the next is loaded while the current is summed)
+  static constexpr int QG = QB < 2 ? QB : 2;
 };
 
 struct IdxBarriers {
@@ -319,17 +320,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const int t = c.kt * kKeyTile + quarter * 32 + lane;
       const int T = p.lens.T[c.b];
       float* srow = p.scores + (static_cast<size_t>(c.b) * p.S + c.qb * QB) * p.cap + t;
-#pragma unroll 1
-      for (int jq = 0; jq < QB; jq += C::QG) {
-        float v[C::QG][16];
-#pragma unroll
-        for (int g = 0; g < C::QG; ++g)
-          tmem_ld16(tmem_base + lane_addr + a * N + (jq + g) * 16, v[g]);
-        tmem_ld_wait();
+      const uint32_t acc_addr = tmem_base + lane_addr + a * N;
+      // weighted head sum of query column group jq (buffer vb), then store
+      auto finish = [&](const float (&vb)[C::QG][16], int jq) {
 #pragma unroll
         for (int g = 0; g < C::QG; ++g) {
           const int s = c.qb * QB + jq + g;
-          if (s >= p.S) break;
           // sum over heads of w_h * ReLU(dot_h), two heads per paired FMA
           const float4* wv4 = reinterpret_cast<const float4*>(wv_warp + (jq + g) * DSA_IDX_HEADS);
           float2 acc2 = make_float2(0.0f, 0.0f);
@@ -337,17 +333,40 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int h4 = 0; h4 < DSA_IDX_HEADS / 4; ++h4) {
             const float4 w4 = wv4[h4];
             acc2 = fma_f32x2(make_float2(w4.x, w4.y),
-                             make_float2(fmaxf(v[g][4 * h4], 0.0f), fmaxf(v[g][4 * h4 + 1], 0.0f)), acc2);
+                             make_float2(fmaxf(vb[g][4 * h4], 0.0f), fmaxf(vb[g][4 * h4 + 1], 0.0f)), acc2);
             acc2 = fma_f32x2(make_float2(w4.z, w4.w),
-                             make_float2(fmaxf(v[g][4 * h4 + 2], 0.0f), fmaxf(v[g][4 * h4 + 3], 0.0f)), acc2);
+                             make_float2(fmaxf(vb[g][4 * h4 + 2], 0.0f), fmaxf(vb[g][4 * h4 + 3], 0.0f)), acc2);
           }
           const float acc = acc2.x + acc2.y;
-          const bool valid = t < visible_len(T, p.S, s);
+          // queries past S (padding of the last block) are computed, not kept
+          const bool valid = s < p.S && t < visible_len(T, p.S, s);
           if (valid) srow[static_cast<size_t>(jq + g) * p.cap] = acc;
           if constexpr (HIST) {
             // plain shared atomics: cheaper than warp-aggregating each update
             if (valid) atomicAdd(&sHist[(jq + g) * kHistBins + (float_key(acc) >> (32 - kHistBits))], 1u);
           }
+        }
+      };
+      float v0[C::QG][16], v1[C::QG][16];
+#pragma unroll
+      for (int g = 0; g < C::QG; ++g) tmem_ld16(acc_addr + g * 16, v0[g]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int jq = 0; jq < QB; jq += 2 * C::QG) {
+        // buffer v0 holds group jq; load jq + QG into v1 while v0 is summed
+        if (jq + C::QG < QB) {
+#pragma unroll
+          for (int g = 0; g < C::QG; ++g) tmem_ld16(acc_addr + (jq + C::QG + g) * 16, v1[g]);
+        }
+        finish(v0, jq);
+        tmem_ld_wait();
+        if (jq + C::QG < QB) {
+          if (jq + 2 * C::QG < QB) {
+#pragma unroll
+            for (int g = 0; g < C::QG; ++g) tmem_ld16(acc_addr + (jq + 2 * C::QG + g) * 16, v0[g]);
+          }
+          finish(v1, jq + C::QG);
+          tmem_ld_wait();
         }
       }
       tc_fence_before();

@@ -425,8 +425,8 @@ __device__ void resolve_composites(const unsigned long long* list, int n, unsign
 }
 
 // ---------------------------------------------------------------------------
-// 3b. whole-row select with the keys in registers (one CTA per row, up to
-// 40,960 keys). Warp w owns keys [w * 32 * PER, (w + 1) * 32 * PER) and lane l
+// 3b. whole-row select with the keys in registers (one CTA of 640 threads per
+// row, up to 64 keys per thread: 40,960 keys). Warp w owns keys [w * 32 * PER, (w + 1) * 32 * PER) and lane l
 // holds key w * 32 * PER + 32 * i + l in key[i]. A sample of the row (every
 // 16th key) gives a provisional threshold theta a little below the k-th key;
 // the keys at or above theta (a few thousand) are resolved exactly in shared
@@ -434,13 +434,13 @@ __device__ void resolve_composites(const unsigned long long* list, int n, unsign
 // many), the threshold is found by radix passes over all keys instead. The
 // selection is emitted in index order with one scan over the warps' counts.
 // ---------------------------------------------------------------------------
-constexpr int kRrThreads = 512;
+constexpr int kRrThreads = 640;   // 20 warps; at most ~100 registers each, keys included
 constexpr int kRrWarps = kRrThreads / 32;
 constexpr int kRrCandMax = 4096;
-constexpr int kRrMaxPer = 80;
+constexpr int kRrMaxPer = 64;
 
 template <int PER>
-__global__ void __launch_bounds__(kRrThreads) topk_row_reg_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kRrThreads, 1) topk_row_reg_kernel(const TopkParams p) {
   __shared__ uint32_t h[kHistBins];
   __shared__ unsigned long long scand[kRrCandMax];
   __shared__ uint32_t warp_tot[32];
@@ -599,7 +599,6 @@ cudaError_t launch_topk_row_reg(const TopkParams& p, int max_n, bool pdl, cudaSt
     case 32: kern = topk_row_reg_kernel<32>; break;
     case 48: kern = topk_row_reg_kernel<48>; break;
     case 64: kern = topk_row_reg_kernel<64>; break;
-    case 80: kern = topk_row_reg_kernel<80>; break;
     default: return cudaErrorInvalidValue;
   }
   return launch_kernel("topk_row_reg_kernel", kern, dim3(p.B * p.S), dim3(kRrThreads), 0, stream, pdl, p);

@@ -100,82 +100,4 @@ __device__ __forceinline__ void find_threshold_digit(const uint32_t* h, int nb, 
   __syncthreads();
 }
 
-// One warp finds the digit d of a histogram h[0..NB) in shared memory (16-byte
-// aligned) such that (entries in bins above d) < need <= that + h[d], scanning
-// from the top bin down; every lane gets d, the count above it and h[d] (all
-// zero if need is 0 or above the total). Two shuffle scans: lane l first sums
-// the run of NB/32 bins counted l-th from the top, then the warp spreads the
-// crossing lane's run over its lanes and scans again.
-template <int NB>
-__device__ __forceinline__ void warp_find_threshold(const uint32_t* h, uint32_t need, int* d_out,
-                                                    uint32_t* above_out, uint32_t* cnt_out) {
-  constexpr int PL = NB / 32;                 // bins per lane in the first level
-  constexpr int Q = (PL + 31) / 32;           // bins per lane in the second level
-  static_assert(PL % 4 == 0, "runs of whole uint4");
-  const int lane = threadIdx.x & 31;
-  const int b0 = NB - (lane + 1) * PL;        // lowest bin of this lane's run
-  const uint4* hv = reinterpret_cast<const uint4*>(h + b0);
-  uint32_t s = 0;
-  // the lanes' runs are PL words apart, which maps every lane to the same
-  // banks; each lane starts its run at a different chunk so that a warp-wide
-  // 16-byte load touches every bank group (4 wavefronts instead of 32)
-#pragma unroll
-  for (int i = 0; i < PL / 4; ++i) {
-    const uint4 v = hv[(i + lane) % (PL / 4)];
-    s += v.x + v.y + v.z + v.w;
-  }
-  uint32_t incl = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const uint32_t excl = incl - s;
-  const uint32_t bal = __ballot_sync(0xffffffffu, excl < need && need <= incl);
-  if (bal == 0u) {
-    *d_out = 0;
-    *above_out = 0u;
-    *cnt_out = 0u;
-    return;
-  }
-  const int src = __ffs(bal) - 1;
-  const uint32_t base = __shfl_sync(0xffffffffu, excl, src);
-  const int top = NB - 1 - src * PL;          // highest bin of the crossing run
-  // second level: lane l holds bins top - l*Q .. top - l*Q - Q + 1
-  uint32_t v2[Q];
-  uint32_t s2 = 0;
-#pragma unroll
-  for (int q = 0; q < Q; ++q) {
-    const int k = lane * Q + q;
-    v2[q] = k < PL ? h[top - k] : 0u;
-    s2 += v2[q];
-  }
-  uint32_t incl2 = s2;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl2, o);
-    if (lane >= o) incl2 += y;
-  }
-  const uint32_t excl2 = base + incl2 - s2;
-  const uint32_t bal2 = __ballot_sync(0xffffffffu, excl2 < need && need <= excl2 + s2);
-  const int src2 = __ffs(bal2) - 1;
-  int d = 0;
-  uint32_t ab = 0, ct = 0;
-  if (lane == src2) {
-    uint32_t acc = excl2;
-#pragma unroll
-    for (int q = 0; q < Q; ++q) {
-      if (acc < need && need <= acc + v2[q]) {
-        d = top - (lane * Q + q);
-        ab = acc;
-        ct = v2[q];
-      }
-      acc += v2[q];
-    }
-  }
-  *d_out = __shfl_sync(0xffffffffu, d, src2);
-  *above_out = __shfl_sync(0xffffffffu, ab, src2);
-  *cnt_out = __shfl_sync(0xffffffffu, ct, src2);
-}
-
 }  // namespace dsa

@@ -391,31 +391,27 @@ __device__ void local_composite_select(const unsigned long long* list, int n,
 
 // Refines the threshold among n composites in shared memory whose bits above
 // `hi` are fixed by prefix/mask, 11 bits per round: the block histograms the
-// composites that match the prefix, one warp picks the digit. `hbuf` is 2,048
-// words of 16-byte-aligned shared scratch.
+// composites that match the prefix and scans it for the digit. `hbuf` is
+// 2,048 words of shared scratch, `warp_tot` the block scan's.
 template <int NT>
 __device__ void resolve_composites(const unsigned long long* list, int n, unsigned long long* prefix,
-                                   unsigned long long* mask, uint32_t need, uint32_t* hbuf, int* sd,
-                                   uint32_t* sabove, uint32_t* scnt, int hi) {
+                                   unsigned long long* mask, uint32_t need, uint32_t* hbuf,
+                                   uint32_t* warp_tot, int* sd, uint32_t* sabove, uint32_t* scnt,
+                                   int hi) {
   bool all = false;
   while (!all && hi >= 0) {
     const int w = hi + 1 < 11 ? hi + 1 : 11;
     const int sh = hi - w + 1;
     const uint32_t dm = (1u << w) - 1u;
     for (int i = threadIdx.x; i < kHistBins; i += NT) hbuf[i] = 0u;
-    __syncthreads();
+    __syncthreads();   // every thread is also past the previous round's reads
+    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
     for (int c = threadIdx.x; c < n; c += NT) {
       const unsigned long long cc = list[c];
       if ((cc & *mask) == *prefix) atomicAdd(&hbuf[static_cast<uint32_t>(cc >> sh) & dm], 1u);
     }
     __syncthreads();
-    if ((threadIdx.x >> 5) == 0) {
-      int d;
-      uint32_t ab, ct;
-      warp_find_threshold<kHistBins>(hbuf, need, &d, &ab, &ct);
-      if (threadIdx.x == 0) { *sd = d; *sabove = ab; *scnt = ct; }
-    }
-    __syncthreads();
+    find_threshold_digit<NT>(hbuf, 1 << w, need, warp_tot, sd, sabove, scnt);
     need -= *sabove;
     *prefix |= static_cast<unsigned long long>(*sd) << sh;
     *mask |= static_cast<unsigned long long>(dm) << sh;
@@ -426,7 +422,8 @@ __device__ void resolve_composites(const unsigned long long* list, int n, unsign
 
 // ---------------------------------------------------------------------------
 // 3b. whole-row select with the keys in registers (one CTA of 640 threads per
-// row, up to 64 keys per thread: 40,960 keys). Warp w owns keys [w * 32 * PER, (w + 1) * 32 * PER) and lane l
+// row, up to 64 keys per thread: 40,960 keys). Warp w owns keys
+// [w * 32 * PER, (w + 1) * 32 * PER) and lane l
 // holds key w * 32 * PER + 32 * i + l in key[i]. A sample of the row (every
 // 16th key) gives a provisional threshold theta a little below the k-th key;
 // the keys at or above theta (a few thousand) are resolved exactly in shared
@@ -682,7 +679,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     for (int j = 0; j < PER; ++j) key[j] = tb + j < m ? float_key(__ldcg(src + j)) : 0u;
   }
   const int nval = max(0, min(PER, m - tb));     // valid keys of this thread
-  if (threadIdx.x == 0) { s_count = 0; s_ncand = 0; s_nsure = 0; }
+  if (threadIdx.x == 0) { s_count = 0; s_ncand = 0; s_nsure = 0; s_d = 0; s_above = 0; s_cnt = 0; }
   if (p.hist_ready) {
     // ---- the row histogram came with the scores (indexer epilogue)
     const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
@@ -717,14 +714,9 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
     __syncthreads();
   }
-  // ---- threshold bin: one warp scans the histogram
-  if (warp == 0) {
-    int d;
-    uint32_t ab, ct;
-    warp_find_threshold<kHistBins>(h, static_cast<uint32_t>(ri.keff), &d, &ab, &ct);
-    if (lane == 0) { s_d = d; s_above = ab; s_cnt = ct; }
-  }
-  __syncthreads();
+  // ---- threshold bin: a block-wide scan of the histogram
+  find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
+                                   &s_above, &s_cnt);
   const uint32_t bin = static_cast<uint32_t>(s_d);
   uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
   const bool all0 = (need == s_cnt);             // the whole threshold bin is selected
@@ -816,7 +808,8 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     // this CTA is done reading its peers: arrive now, wait before exiting
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (!all0)
-      resolve_composites<kClThreads>(sg, off, &prefix, &mask, need, h, &s_d, &s_above, &s_cnt, 52);
+      resolve_composites<kClThreads>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
+                                     &s_cnt, 52);
   } else {
     // ---- many candidates (heavy ties): refine the threshold 8 bits at a time,
     // summing the CTAs' digit histograms through distributed shared memory

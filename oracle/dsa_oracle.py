@@ -37,6 +37,14 @@ R4  attention: head h uses KV head g = h // (Hq/Hkv) (consecutive grouping);
     logits = scale * q_h . K^[t,g] with scale = 1/sqrt(head_dim) unless given;
     exact softmax over the selected keys; out_h = sum_t p_t V^[t,g].
 R5  INT8 cache: K^[t,g,:] = code[t,g,:] * k_scale[t,g] (same for V).
+R6  cache append (the step before the indexer): the S new tokens of a
+    sequence are written to cache rows T-S .. T-1 (R1). An INT8 cache stores,
+    per token and KV head, scale = absmax/127 and code = clamp(rint(x /
+    scale), -127, 127) with ties to even (scale 0 and codes 0 for an all-zero
+    row). The codes are integers decided by floating point, so they are
+    computed in fp32 (the kernel's precision): absmax and x are exact fp32
+    values, scale and x / scale are IEEE fp32 divisions. A 16-bit cache of
+    the other 16-bit type takes the value rounded to nearest even.
 
 Parity pins for every function live in tests/test_oracle_pins.py.
 """
@@ -194,3 +202,57 @@ def sparse_attention_step(inp: dict, num_kv_heads: int, top_k: int,
                            inp.get("k_scale"), inp.get("v_scale"),
                            softmax_scale, rows=rows)
     return {"scores": scores, "idx": idx, "out": out}
+
+
+# ---------------------------------------------------------------------------
+# cache append (R6)
+# ---------------------------------------------------------------------------
+def quantize_row_int8(x) -> tuple:
+    """One token's KV-head row (any length) -> (int8 codes, fp32 scale), with
+    every decision in fp32 as R6 states."""
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x32))) if x32.size else np.float32(0.0)
+    scale = np.float32(amax / np.float32(127.0))
+    if scale == np.float32(0.0):
+        return np.zeros(x32.shape, dtype=np.int8), np.float32(0.0)
+    q = np.rint(x32 / scale).astype(np.float32)          # fp32 division, ties to even
+    return np.clip(q, -127, 127).astype(np.int8), scale
+
+
+def round_to(values, dtype: str) -> np.ndarray:
+    """float64 values rounded (nearest, ties to even) to bf16 / fp16 / fp32 and
+    returned as float64. Uses torch's CPU casts as the rounding routine."""
+    import torch
+    t = torch.as_tensor(np.asarray(values, dtype=np.float64))
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[dtype]
+    return t.to(torch.float32).to(tdt).to(torch.float64).numpy()
+
+
+def cache_append(kI, k, v, k_scale, v_scale, kI_new, k_new, v_new, total_len, kv_dtype: str):
+    """Write the S new tokens of every sequence into copies of the caches (R6).
+
+    kI [B,cap,64], k/v [B,cap,Hkv,128] (INT8: codes as float64), k_scale /
+    v_scale [B,cap,Hkv] (INT8 only, else None); kI_new [B,S,64], k_new / v_new
+    [B,S,Hkv,128] exact float64 values; total_len [B]. Returns the updated
+    (kI, k, v, k_scale, v_scale).
+    """
+    kI, k, v = kI.copy(), k.copy(), v.copy()
+    k_scale = None if k_scale is None else k_scale.copy()
+    v_scale = None if v_scale is None else v_scale.copy()
+    B, S = k_new.shape[0], k_new.shape[1]
+    Hkv = k_new.shape[2]
+    for b in range(B):
+        for s in range(S):
+            t = int(total_len[b]) - S + s                    # R1: the last S rows
+            if t < 0:
+                raise ValueError("new tokens precede the cache start")
+            kI[b, t] = kI_new[b, s]                          # bf16 to bf16: a copy
+            for g in range(Hkv):
+                for dst, dsc, src in ((k, k_scale, k_new), (v, v_scale, v_new)):
+                    if kv_dtype == "int8":
+                        codes, sc = quantize_row_int8(src[b, s, g])
+                        dst[b, t, g] = codes.astype(np.float64)
+                        dsc[b, t, g] = float(sc)
+                    else:
+                        dst[b, t, g] = round_to(src[b, s, g], kv_dtype)
+    return kI, k, v, k_scale, v_scale

@@ -341,6 +341,79 @@ def test_full_step_on_workload_shapes():
 
 
 # ---------------------------------------------------------------------------
+# cache append (R6)
+# ---------------------------------------------------------------------------
+def check_quantize_fixture(mod):
+    for case in _load("int8_quantize_tiny.json")["cases"]:
+        codes, scale = mod.quantize_row_int8(np.array(case["x"], dtype=np.float64))
+        assert codes.tolist() == case["codes"], (case, codes)
+        assert float(scale) == case["scale"], (case, scale)
+
+
+def check_quantize_invariants(mod):
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        x = (rng.standard_normal(128) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        codes, scale = mod.quantize_row_int8(x)
+        amax = np.abs(x).max()
+        # the absmax element maps to +-127 and every code is within range
+        assert np.abs(codes.astype(np.int32)).max() == 127
+        # scale * 127 recovers the absmax to fp32 rounding
+        assert abs(float(scale) * 127.0 - float(amax)) <= 1e-6 * float(amax)
+        # rounding to nearest: every value within half a step (plus fp32 slack)
+        err = np.abs(x.astype(np.float64) - codes.astype(np.float64) * float(scale))
+        assert err.max() <= 0.5 * float(scale) * (1 + 1e-5)
+
+
+def check_append_positions(mod):
+    """B = 2, S = 2, cap = 6, T = (5, 3): the new tokens land in rows 3, 4 of
+    sequence 0 and rows 1, 2 of sequence 1; every other row keeps its value."""
+    B, S, cap, Hkv = 2, 2, 6, 1
+    kI = np.full((B, cap, 2), -9.0)
+    k = np.full((B, cap, Hkv, 2), -9.0)
+    v = np.full((B, cap, Hkv, 2), -9.0)
+    kI_new = np.arange(B * S * 2, dtype=np.float64).reshape(B, S, 2)
+    k_new = 10 + np.arange(B * S * Hkv * 2, dtype=np.float64).reshape(B, S, Hkv, 2)
+    v_new = 20 + np.arange(B * S * Hkv * 2, dtype=np.float64).reshape(B, S, Hkv, 2)
+    out = mod.cache_append(kI, k, v, None, None, kI_new, k_new, v_new, [5, 3], "bf16")
+    kI2, k2, v2 = out[0], out[1], out[2]
+    rows = {0: (3, 4), 1: (1, 2)}
+    for b in range(B):
+        for t in range(cap):
+            if t in rows[b]:
+                s_ = rows[b].index(t)
+                assert kI2[b, t].tolist() == kI_new[b, s_].tolist()
+                assert k2[b, t].tolist() == k_new[b, s_].tolist()
+                assert v2[b, t].tolist() == v_new[b, s_].tolist()
+            else:
+                assert (kI2[b, t] == -9).all() and (k2[b, t] == -9).all() and (v2[b, t] == -9).all()
+
+
+def test_quantize_golden_fixture():
+    check_quantize_fixture(O)
+
+
+def test_quantize_invariants():
+    check_quantize_invariants(O)
+
+
+def test_append_positions():
+    check_append_positions(O)
+
+
+def test_append_int8_dequantises_to_within_half_a_step():
+    rng = np.random.default_rng(3)
+    B, S, cap, Hkv = 1, 3, 8, 2
+    new = rng.standard_normal((B, S, Hkv, 128)).astype(np.float32).astype(np.float64)
+    zeros = np.zeros((B, cap, Hkv, 128))
+    sc = np.zeros((B, cap, Hkv))
+    _, k2, _, ks2, _ = O.cache_append(np.zeros((B, cap, 64)), zeros, zeros, sc, sc,
+                                      np.zeros((B, S, 64)), new, new, [8], "int8")
+    deq = O.dequantize(k2[0, 5:8], ks2[0, 5:8])
+    assert np.abs(deq - new[0]).max() <= 0.5 * ks2[0, 5:8].max() * (1 + 1e-5)
+
+
+# ---------------------------------------------------------------------------
 # mutation tests: plant a mistake in a copy of the oracle, a pin must fail
 # ---------------------------------------------------------------------------
 class _Mutant:
@@ -438,3 +511,32 @@ def test_mutant_value_scale_dropped_is_caught():
     def bad(codes, scale):
         return codes
     assert _fails(check_worked_example, _Mutant(dequantize=bad))
+
+
+def test_mutant_round_half_up_is_caught():
+    def bad(x):
+        x32 = np.asarray(x, dtype=np.float32)
+        scale = np.float32(np.float32(np.max(np.abs(x32))) / np.float32(127.0))
+        if scale == 0:
+            return np.zeros(x32.shape, dtype=np.int8), np.float32(0.0)
+        q = np.floor(x32 / scale + np.float32(0.5))
+        return np.clip(q, -127, 127).astype(np.int8), scale
+    assert _fails(check_quantize_fixture, _Mutant(quantize_row_int8=bad))
+
+
+def test_mutant_scale_over_128_is_caught():
+    def bad(x):
+        x32 = np.asarray(x, dtype=np.float32)
+        scale = np.float32(np.float32(np.max(np.abs(x32))) / np.float32(128.0))
+        if scale == 0:
+            return np.zeros(x32.shape, dtype=np.int8), np.float32(0.0)
+        return np.clip(np.rint(x32 / scale), -127, 127).astype(np.int8), scale
+    m = _Mutant(quantize_row_int8=bad)
+    assert _fails(check_quantize_fixture, m) and _fails(check_quantize_invariants, m)
+
+
+def test_mutant_append_one_row_late_is_caught():
+    def bad(kI, k, v, k_scale, v_scale, kI_new, k_new, v_new, total_len, kv_dtype):
+        return O.cache_append(kI, k, v, k_scale, v_scale, kI_new, k_new, v_new,
+                              [t + 1 if t + 1 <= kI.shape[1] else t for t in total_len], kv_dtype)
+    assert _fails(check_append_positions, _Mutant(cache_append=bad))

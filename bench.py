@@ -3,7 +3,7 @@ sparse attention step (indexer -> radix top-k -> sparse GQA attention) at a
 131,072-token context with top_k = 2,048, on synthetic data.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libdsa|reference]
-                    [--workload NAME] [--no-graph]
+                    [--workload NAME] [--no-graph] [--op step|append [--q-len S]]
 
 One JSON line on stdout (rank 0). A step is one call of the whole decode path
 (dsa_sparse_attn_decode) over one batch of query tokens with inputs resident
@@ -14,6 +14,9 @@ times the same call eagerly with the step's inputs copied from pinned host
 memory and its output copied back. Under torchrun every rank runs its own
 replica of the workload (the path shards by sequence with no exchange:
 weak scaling); the slowest rank's time is reported.
+
+--op append times dsa_cache_append alone (the cache write before the step) on
+the workload's shape and reports its HBM GB/s.
 
 --impl reference times the float64 CPU oracle on the same workload (rank 0
 only) -- a deliberately slow baseline, not the optimisation target.
@@ -471,6 +474,120 @@ def run_libdsa(args, wl):
         dist.destroy_process_group()
 
 
+def append_bytes(batch, q_len, num_kv_heads, q_dtype, kv_dtype):
+    """Algorithmic bytes of one cache append: every new-token byte read once
+    and every cache byte it produces written once (index key 64 bf16; K and V
+    rows of 128 elements per KV head; INT8 adds a 4-byte scale per row)."""
+    tokens = batch * q_len
+    read = tokens * (64 * 2 + 2 * num_kv_heads * 128 * 2)
+    row_out = 128 + 4 if kv_dtype == "int8" else 256
+    write = tokens * (64 * 2 + 2 * num_kv_heads * row_out)
+    return read + write
+
+
+def run_append_bench(args, wl):
+    """--op append: dsa_cache_append alone on the workload's shape (batch,
+    KV heads, dtypes; --q-len new tokens per sequence, default the
+    workload's), timed per call with CUDA events after an L2 flush."""
+    import torch
+
+    from dsa_inputs import make_append_inputs
+    from top_sparse_attention_chunked_gb300 import build_lib
+    from top_sparse_attention_chunked_gb300 import dsa as D
+
+    build_lib.build()
+    D.load_library()
+    S = args.q_len or wl.q_len
+    T = max(wl.total_len, S)
+    cap = T
+    cpu = make_append_inputs(wl.batch, S, wl.num_kv_heads, cap, [T] * wl.batch, wl.q_dtype,
+                             wl.kv_dtype, seed=wl.seed, specials=False)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    p = D.make_problem(batch=wl.batch, q_len=S, total_len=[T] * wl.batch, top_k=1,
+                       num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                       cache_capacity=cap, q_dtype=wl.q_dtype, kv_dtype=wl.kv_dtype)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        D.dsa_cache_append(p, dev["kI_new"], dev["k_new"], dev["v_new"], dev["kI"], dev["k"],
+                           dev["v"], dev["k_scale"], dev["v_scale"])
+
+    if args.profile_calls:
+        for _ in range(args.profile_calls):
+            step()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_calls": args.profile_calls, "op": "append",
+                          "kernels_per_step": D.dsa_last_launches()}), flush=True)
+        return
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    kernels = D.dsa_last_launches()
+
+    def graph_of():
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(g, kernel_events):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        kern = []
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            g.replay()
+            evs[i][1].record(stream)
+            if kernel_events:
+                torch.cuda.synchronize()
+                kern.append(D.dsa_timing_read())
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in evs), kern
+
+    # the step as a caller replays it (graph), then the kernel alone (events
+    # recorded by the library around its launch, captured in the graph)
+    D.dsa_timing_select(-1)
+    g = graph_of()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    ms, _ = timed(g, False)
+    clk = clocks.stop()
+    D.dsa_timing_select(D.DSA_KERNEL_APPEND)
+    g = graph_of()
+    _, kern_ms = timed(g, True)
+    D.dsa_timing_select(-1)
+    kms = statistics.mean(kern_ms)
+    nbytes = append_bytes(wl.batch, S, wl.num_kv_heads, wl.q_dtype, wl.kv_dtype)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    kgbs = nbytes / (kms * 1e-3) / 1e9
+    hbm, _, peak_kind = peaks()
+    print(json.dumps({
+        "metric": "cache append achieved HBM GB/s", "value": round(gbs, 1), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": f"{wl.q_dtype}->{wl.kv_dtype}",
+        "data": "synthetic (seeded N(0,1) rows of magnitude 10^U(-3,3), see dsa_inputs.py)",
+        "config": {"workload": f"cache append of {S} tokens x {wl.batch} sequence(s), "
+                               f"{wl.num_kv_heads} KV heads, {wl.q_dtype} -> {wl.kv_dtype}",
+                   "l2": "flushed (256 MiB write) before every step", "graph": True},
+        "tokens_per_s": wl.batch * S / (ms * 1e-3),
+        "roofline": {"kernel": "cache_append_kernel", "bound": "hbm", "achieved": round(kgbs, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(kgbs / hbm, 4),
+                     "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes": nbytes,
+                     "launch_us": round(kms * 1e3, 2)},
+        "gpu_launches": len(kernels) * args.steps, "kernels_per_step": kernels,
+        "clocks": clk}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,8 +599,11 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="run this many untimed calls and exit (for ncu captures)")
+    ap.add_argument("--op", default="step", choices=["step", "append"],
+                    help="append: time dsa_cache_append alone on the workload's shape")
     ap.add_argument("--q-len", type=int, default=0,
-                    help="with --profile-calls: query tokens per sequence of a reduced case")
+                    help="with --profile-calls: query tokens per sequence of a reduced case; "
+                         "with --op append: new tokens per sequence")
     ap.add_argument("--context", type=int, default=0,
                     help="with --profile-calls: cache length of a reduced case")
     args = ap.parse_args()
@@ -491,6 +611,9 @@ def main():
         args.warmup = 3
     from dsa_inputs import WORKLOADS
     wl = WORKLOADS[args.workload]
+    if args.op == "append":
+        run_append_bench(args, wl)
+        return
     if args.profile_calls and (args.q_len or args.context):
         # a reduced case of the same structure (heads, top_k, dtypes)
         from dsa_inputs import small_workload

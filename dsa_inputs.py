@@ -136,6 +136,52 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> Dict[str, torch.Ten
     return out
 
 
+def make_append_inputs(batch: int, q_len: int, num_kv_heads: int, capacity: int,
+                       total_len, q_dtype: str, kv_dtype: str, seed: int = 0,
+                       specials: bool = True) -> Dict[str, torch.Tensor]:
+    """CPU tensors for a cache append: the new tokens and the caches they are
+    written into, from one seeded generator.
+
+    New K/V rows are N(0,1) times a per-row magnitude 10^U(-3,3); with
+    ``specials`` a few rows are replaced by an all-zero row, a row with one
+    non-zero element, and (BF16 new tokens only) a row holding 70000 and 1e-6.
+    The caches are filled with random sentinel values (INT8: random codes and
+    positive scales) so that rows the append must not touch are recognisable.
+    Returns kI_new [B,S,64] bf16, k_new / v_new [B,S,Hkv,128] q_dtype, kI
+    [B,cap,64] bf16, k / v [B,cap,Hkv,128] kv_dtype, k_scale / v_scale
+    [B,cap,Hkv] fp32 or None, total_len [B] int32.
+    """
+    g = torch.Generator().manual_seed(seed)
+    B, S, H, cap = batch, q_len, num_kv_heads, capacity
+    T = [int(t) for t in (total_len if hasattr(total_len, "__len__") else [total_len] * B)]
+    kI_new = torch.randn(B, S, 64, generator=g).to(torch.bfloat16)
+    new = []
+    for _ in range(2):
+        x = torch.randn(B, S, H, 128, generator=g)
+        mag = 10.0 ** (torch.rand(B, S, H, 1, generator=g) * 6 - 3)
+        x = x * mag
+        if specials and B * S * H >= 3:
+            flat = x.view(-1, 128)
+            flat[0].zero_()
+            flat[1].zero_()
+            flat[1, 77] = -0.375
+            if q_dtype == "bf16":
+                flat[2, 5] = 70000.0
+                flat[2, 6] = 1e-6
+        new.append(x.to(DTYPES[q_dtype]).contiguous())
+    out = {"kI_new": kI_new.contiguous(), "k_new": new[0], "v_new": new[1],
+           "kI": torch.randn(B, cap, 64, generator=g).to(torch.bfloat16).contiguous(),
+           "total_len": torch.tensor(T, dtype=torch.int32), "k_scale": None, "v_scale": None}
+    for name in ("k", "v"):
+        if kv_dtype == "int8":
+            out[name] = torch.randint(-127, 128, (B, cap, H, 128), generator=g,
+                                      dtype=torch.int64).to(torch.int8)
+            out[name + "_scale"] = torch.rand(B, cap, H, generator=g) + 0.5
+        else:
+            out[name] = torch.randn(B, cap, H, 128, generator=g).to(DTYPES[kv_dtype]).contiguous()
+    return out
+
+
 def small_workload(name="small", batch=2, q_len=3, total_len=1000, num_q_heads=8,
                    num_kv_heads=2, top_k=64, q_dtype="bf16", kv_dtype="bf16",
                    capacity=None, bias_frac=0.0, seed=7) -> Workload:

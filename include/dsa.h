@@ -202,6 +202,37 @@ int dsa_sparse_attn_prefill(const dsa_problem* p, const void* q, const void* qI,
                             void* stream);
 
 /*
+ * dsa_cache_append -- write the q_len new tokens of every sequence into the
+ * caches, the step that comes before the indexer. PR #33997 "[CUDA] Support
+ * FP16 KV cache and FP16 query/key in DynamicSparseAttention<BFloat16> ...":
+ * its Files changed table puts the cache writes in the implementation file
+ * beside the attention kernels, and its description names the quantized
+ * (INT8) cache, whose per-token per-head scale this call produces.
+ *
+ * Token s of sequence b goes to cache row T_b - q_len + s, with
+ * T_b = total_len[b] counting the new tokens (the positions rule above), so
+ * the same problem then drives dsa_sparse_attn_decode / _prefill. `p` is
+ * validated as for dsa_sparse_attn_prefill (top_k and the output fields too).
+ *
+ *   kI_new        [B, q_len, 64] bf16 new index keys, 16-byte aligned
+ *   k_new, v_new  [B, q_len, Hkv, 128] q_dtype new keys / values, 16-byte aligned
+ *   kI            [B, cap, 64] bf16 index-key cache (rows T_b-q_len..T_b-1 written)
+ *   k, v          [B, cap, Hkv, 128] kv_dtype caches (the same rows written)
+ *   k_scale, v_scale  [B, cap, Hkv] fp32, required iff kv_dtype == DSA_INT8
+ *                 (else NULL). For an INT8 cache each new (token, KV head) row
+ *                 gets scale = absmax/127 and code = round-half-even(x /
+ *                 scale) clamped to +-127, both divisions IEEE fp32; an
+ *                 all-zero row gets scale 0 and codes 0. A 16-bit cache of the
+ *                 other 16-bit type takes x rounded to nearest even.
+ * No other row and no other byte is written. The new-token tensors must not
+ * overlap any cache (checked, DSA_ERR_INVALID_ARG). Values must be finite. One
+ * kernel launch; no workspace.
+ */
+int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new,
+                     const void* v_new, void* kI, void* k, void* v, float* k_scale,
+                     float* v_scale, void* stream);
+
+/*
  * dsa_topk_noalloc -- dsa_topk for callers that cannot give the library any
  * device memory. Some callers cannot allocate: an operator plugin whose host
  * framework hands it only its input and output tensors, a serving engine that
@@ -250,7 +281,8 @@ int dsa_version(void);
 
 /*
  * dsa_last_launches -- the kernels that the last dsa_index_scores, dsa_topk,
- * dsa_topk_noalloc, dsa_sparse_attn_decode or dsa_sparse_attn_prefill call on
+ * dsa_topk_noalloc, dsa_cache_append, dsa_sparse_attn_decode or
+ * dsa_sparse_attn_prefill call on
  * this host thread enqueued. Returns how many (0 after a call that failed
  * before launching); when buf is not NULL, writes their names in launch order,
  * comma-separated and NUL-terminated, truncated to fit buflen bytes. No
@@ -272,7 +304,8 @@ enum {
   DSA_KERNEL_TOPK_HIST = 1,     /* chunk histograms (dsa_topk only)           */
   DSA_KERNEL_TOPK_SELECT = 2,   /* chunk select + final merge-and-emit        */
   DSA_KERNEL_TOPK_ROW = 3,      /* whole-row shared-memory select             */
-  DSA_KERNEL_ATTENTION = 4      /* sparse attention (+ split combine)         */
+  DSA_KERNEL_ATTENTION = 4,     /* sparse attention (+ split combine)         */
+  DSA_KERNEL_APPEND = 5         /* cache append (dsa_cache_append)            */
 };
 int dsa_timing_select(int kernel_kind);
 int dsa_timing_read(float* ms);

@@ -122,3 +122,41 @@ def test_status_strings(lib):
     assert lib.dsa_status_string(0) == b"DSA_OK"
     assert lib.dsa_status_string(6) == b"DSA_ERR_TIMEOUT"
     assert lib.dsa_version() >= 100
+
+
+def _call_append(lib, p, ptrs=None):
+    a = {"kI_new": 0x1000, "k_new": 0x10000, "v_new": 0x20000, "kI": 0x100000,
+         "k": 0x1000000, "v": 0x2000000}
+    a.update(ptrs or {})
+    vals = [a[n] for n in ("kI_new", "k_new", "v_new", "kI", "k", "v")]
+    return lib.dsa_cache_append(ctypes.byref(p), *[ctypes.c_void_p(v) for v in vals],
+                                ctypes.c_void_p(a.get("ks")), ctypes.c_void_p(a.get("vs")), None)
+
+
+def test_cache_append_rejects_bad_arguments_before_cuda(lib):
+    from top_sparse_attention_chunked_gb300.dsa import (DSA_ERR_INVALID_ARG, DSA_ERR_MISALIGNED,
+                                                        DSA_ERR_UNSUPPORTED)
+    p = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8)   # 2 KV heads, FP16 cache
+    assert _call_append(lib, p, {"k_new": 0}) == DSA_ERR_INVALID_ARG
+    assert _call_append(lib, p, {"v": 0x2000008}) == DSA_ERR_MISALIGNED
+    assert _call_append(lib, p, {"ks": 0x3000000, "vs": 0x3001000}) == DSA_ERR_INVALID_ARG
+    # new K rows (4 x 2 x 256 B = 2 KiB from 0x10000) overlapping the V cache
+    assert _call_append(lib, p, {"v": 0x10400}) == DSA_ERR_INVALID_ARG
+    assert "overlaps" in lib.dsa_last_error_string().decode()
+    # adjacent but disjoint is fine up to the device check
+    p8 = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8, kv_dtype="int8")
+    assert _call_append(lib, p8) == DSA_ERR_INVALID_ARG                 # scales missing
+    assert _call_append(lib, p8, {"ks": 0x3000000, "vs": 0x3000002}) == DSA_ERR_MISALIGNED
+    assert _call_append(lib, _prob(q_len=65, total_len=64, cache_capacity=64, top_k=8)) \
+        == DSA_ERR_INVALID_ARG                                          # q_len > total_len
+    assert _call_append(lib, _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8,
+                                   q_dtype="fp16", kv_dtype="bf16")) == DSA_ERR_UNSUPPORTED
+
+
+def test_cache_append_without_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_NO_DEVICE
+    p = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8)
+    assert _call_append(lib, p, {"v_new": 0x10800}) == DSA_ERR_NO_DEVICE

@@ -700,6 +700,68 @@ int dsa_sparse_attn_prefill(const dsa_problem* p, const void* q, const void* qI,
                    ws_bytes, stream);
 }
 
+int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new,
+                     const void* v_new, void* kI, void* k, void* v, float* k_scale,
+                     float* v_scale, void* stream) {
+  reset_launches();
+  Derived d;
+  int rc = check_problem(p, DSA_OP_PREFILL, &d);
+  if (rc) return rc;
+  if (!kI_new || !k_new || !v_new || !kI || !k || !v)
+    return fail(DSA_ERR_INVALID_ARG, "a required tensor pointer is NULL");
+  const bool int8 = (p->kv_dtype == DSA_INT8);
+  if (int8) {
+    if (!k_scale || !v_scale) return fail(DSA_ERR_INVALID_ARG, "INT8 cache needs k_scale and v_scale");
+    if (!aligned(k_scale, 4) || !aligned(v_scale, 4))
+      return fail(DSA_ERR_MISALIGNED, "scales must be 4-byte aligned");
+  } else if (k_scale || v_scale) {
+    return fail(DSA_ERR_INVALID_ARG, "k_scale/v_scale must be NULL unless the cache is INT8");
+  }
+  if (!aligned(kI_new, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kI, 16) ||
+      !aligned(k, 16) || !aligned(v, 16))
+    return fail(DSA_ERR_MISALIGNED, "kI_new, k_new, v_new, kI, k and v must be 16-byte aligned");
+  // the new tokens are read while the caches are written: no input may overlap an output
+  const long long B = p->batch, S = p->q_len, H = p->num_kv_heads, cap = p->cache_capacity;
+  struct Span { const void* p; long long n; };
+  const Span in[3] = {{kI_new, B * S * DSA_IDX_DIM * 2}, {k_new, B * S * H * DSA_HEAD_DIM * 2},
+                      {v_new, B * S * H * DSA_HEAD_DIM * 2}};
+  const long long row_bytes = int8 ? DSA_HEAD_DIM : DSA_HEAD_DIM * 2;
+  const Span out[5] = {{kI, B * cap * DSA_IDX_DIM * 2}, {k, B * cap * H * row_bytes},
+                       {v, B * cap * H * row_bytes}, {k_scale, int8 ? B * cap * H * 4 : 0},
+                       {v_scale, int8 ? B * cap * H * 4 : 0}};
+  for (const Span& a : in)
+    for (const Span& o : out) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), o0 = reinterpret_cast<uintptr_t>(o.p);
+      if (o.n > 0 && a0 < o0 + static_cast<uintptr_t>(o.n) && o0 < a0 + static_cast<uintptr_t>(a.n))
+        return fail(DSA_ERR_INVALID_ARG, "a new-token tensor overlaps a cache");
+    }
+  DeviceInfo di;
+  rc = device_info(&di);
+  if (rc) return rc;
+  AppendParams ap{};
+  ap.kI_new = kI_new;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.kI = kI;
+  ap.k = k;
+  ap.v = v;
+  ap.k_scale = k_scale;
+  ap.v_scale = v_scale;
+  ap.B = p->batch;
+  ap.S = p->q_len;
+  ap.Hkv = p->num_kv_heads;
+  ap.cap = p->cache_capacity;
+  ap.q_dtype = p->q_dtype;
+  ap.kv_dtype = p->kv_dtype;
+  for (int b = 0; b < p->batch; ++b) ap.lens.T[b] = p->total_len[b];
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  timing_before(DSA_KERNEL_APPEND, st);
+  const cudaError_t e = launch_cache_append(ap, di.sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cache append launch");
+  timing_after(DSA_KERNEL_APPEND, st);
+  return DSA_OK;
+}
+
 int dsa_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* status_out) {
   if (!ws || ws_bytes < 256 || !status_out)
     return fail(DSA_ERR_INVALID_ARG, "workspace or status_out invalid");
@@ -747,7 +809,7 @@ int dsa_last_launches(char* buf, size_t buflen) {
 }
 
 int dsa_timing_select(int kind) {
-  if (kind < -1 || kind > DSA_KERNEL_ATTENTION) return fail(DSA_ERR_INVALID_ARG, "unknown kernel kind %d", kind);
+  if (kind < -1 || kind > DSA_KERNEL_APPEND) return fail(DSA_ERR_INVALID_ARG, "unknown kernel kind %d", kind);
   g_timing_kind = kind;
   g_ev_recorded = false;
   return DSA_OK;

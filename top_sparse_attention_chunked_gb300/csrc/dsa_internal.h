@@ -153,4 +153,21 @@ bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin);
 cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, uint32_t* status, cudaStream_t stream);
 
+// ---------------------------------------------------------------- cache append
+struct AppendParams {
+  const void* kI_new;      // [B, S, 64] bf16
+  const void* k_new;       // [B, S, Hkv, 128] q_dtype
+  const void* v_new;
+  void* kI;                // [B, cap, 64] bf16
+  void* k;                 // [B, cap, Hkv, 128] kv_dtype
+  void* v;
+  float* k_scale;          // [B, cap, Hkv] (INT8 only)
+  float* v_scale;
+  int B, S, Hkv, cap;
+  int q_dtype, kv_dtype;
+  SeqLens lens;
+};
+
+cudaError_t launch_cache_append(const AppendParams& p, int sms, cudaStream_t stream);
+
 }  // namespace dsa

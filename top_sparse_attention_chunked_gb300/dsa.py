@@ -26,13 +26,13 @@ DSA_BF16, DSA_FP16, DSA_INT8, DSA_FP32 = 0, 1, 2, 3
 DSA_OP_INDEX_SCORES, DSA_OP_TOPK, DSA_OP_DECODE, DSA_OP_PREFILL = 0, 1, 2, 3
 DSA_MAX_BATCH = 64
 DSA_KERNEL_INDEXER, DSA_KERNEL_TOPK_HIST, DSA_KERNEL_TOPK_SELECT = 0, 1, 2
-DSA_KERNEL_TOPK_ROW, DSA_KERNEL_ATTENTION = 3, 4
+DSA_KERNEL_TOPK_ROW, DSA_KERNEL_ATTENTION, DSA_KERNEL_APPEND = 3, 4, 5
 
 EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill",
             "dsa_read_device_status", "dsa_last_error_string", "dsa_status_string",
             "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc",
-            "dsa_last_launches"]
+            "dsa_last_launches", "dsa_cache_append"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -94,6 +94,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_timing_select": (i32, [i32]),
         "dsa_timing_read": (i32, [ctypes.POINTER(ctypes.c_float)]),
         "dsa_topk_noalloc": (i32, [P, vp, vp, vp]),
+        "dsa_cache_append": (i32, [P] + [vp] * 9),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -208,6 +209,22 @@ def dsa_topk_noalloc(p: DsaProblem, scores, idx, stream=None):
     _check(lib.dsa_topk_noalloc(ctypes.byref(p),
                                 _ptr(scores, "scores", torch.float32, (B, S, cap)),
                                 _ptr(idx, "idx", torch.int32, (B, S, p.top_k)), _stream(stream)))
+
+
+def dsa_cache_append(p: DsaProblem, kI_new, k_new, v_new, kI, k, v, k_scale=None,
+                     v_scale=None, stream=None):
+    """Write the q_len new tokens of every sequence into cache rows
+    total_len[b]-q_len .. total_len[b]-1 (INT8 caches: quantised on write)."""
+    B, S, cap, Hkv = p.batch, p.q_len, p.cache_capacity, p.num_kv_heads
+    lib = load_library()
+    qdt, kvdt = _TORCH_DT[p.q_dtype], _TORCH_DT[p.kv_dtype]
+    _check(lib.dsa_cache_append(
+        ctypes.byref(p), _ptr(kI_new, "kI_new", torch.bfloat16, (B, S, 64)),
+        _ptr(k_new, "k_new", qdt, (B, S, Hkv, 128)), _ptr(v_new, "v_new", qdt, (B, S, Hkv, 128)),
+        _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)), _ptr(k, "k", kvdt, (B, cap, Hkv, 128)),
+        _ptr(v, "v", kvdt, (B, cap, Hkv, 128)),
+        _ptr(k_scale, "k_scale", torch.float32, (B, cap, Hkv)),
+        _ptr(v_scale, "v_scale", torch.float32, (B, cap, Hkv)), _stream(stream)))
 
 
 def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream):

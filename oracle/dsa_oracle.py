@@ -37,7 +37,7 @@ R4  attention: head h uses KV head g = h // (Hq/Hkv) (consecutive grouping);
     logits = scale * q_h . K^[t,g] with scale = 1/sqrt(head_dim) unless given;
     exact softmax over the selected keys; out_h = sum_t p_t V^[t,g].
 R5  INT8 cache: K^[t,g,:] = code[t,g,:] * k_scale[t,g] (same for V).
-R6  cache append (the step before the indexer): the S new tokens of a
+R11 cache append (the step before the indexer): the S new tokens of a
     sequence are written to cache rows T-S .. T-1 (R1). An INT8 cache stores,
     per token and KV head, scale = absmax/127 and code = clamp(rint(x /
     scale), -127, 127) with ties to even (scale 0 and codes 0 for an all-zero
@@ -205,11 +205,11 @@ def sparse_attention_step(inp: dict, num_kv_heads: int, top_k: int,
 
 
 # ---------------------------------------------------------------------------
-# cache append (R6)
+# cache append (R11)
 # ---------------------------------------------------------------------------
 def quantize_row_int8(x) -> tuple:
     """One token's KV-head row (any length) -> (int8 codes, fp32 scale), with
-    every decision in fp32 as R6 states."""
+    every decision in fp32 as R11 states."""
     x32 = np.asarray(x, dtype=np.float32)
     amax = np.float32(np.max(np.abs(x32))) if x32.size else np.float32(0.0)
     scale = np.float32(amax / np.float32(127.0))
@@ -229,7 +229,7 @@ def round_to(values, dtype: str) -> np.ndarray:
 
 
 def cache_append(kI, k, v, k_scale, v_scale, kI_new, k_new, v_new, total_len, kv_dtype: str):
-    """Write the S new tokens of every sequence into copies of the caches (R6).
+    """Write the S new tokens of every sequence into copies of the caches (R11).
 
     kI [B,cap,64], k/v [B,cap,Hkv,128] (INT8: codes as float64), k_scale /
     v_scale [B,cap,Hkv] (INT8 only, else None); kI_new [B,S,64], k_new / v_new

@@ -341,7 +341,7 @@ def test_full_step_on_workload_shapes():
 
 
 # ---------------------------------------------------------------------------
-# cache append (R6)
+# cache append (R11)
 # ---------------------------------------------------------------------------
 def check_quantize_fixture(mod):
     for case in _load("int8_quantize_tiny.json")["cases"]:

@@ -263,9 +263,78 @@ int dsa_topk_noalloc(const dsa_problem* p, const float* scores, int32_t* idx,
                      void* stream);
 
 /*
+ * Paged caches. On the page of ONNX Runtime PR #33802, the companion
+ * onnxruntime-genai change (#2840), Summary item 1: the KV and indexer caches
+ * of a 256K request live in a pool of fixed-size token blocks (block_size 256,
+ * num_blocks 1,037, of which 1,024 hold the target's 262,144 tokens); paged
+ * attention walks a per-sequence block table (PR #34117, "quantized paged
+ * attention"; PR #28200's paged-KV gather on the same page set).
+ *
+ * With a paged cache, kI, K, V and the INT8 scales are pools of
+ * num_blocks * block_size token rows: kI [num_blocks * block_size, 64] bf16,
+ * K / V [num_blocks * block_size, Hkv, 128] kv_dtype, k_scale / v_scale
+ * [num_blocks * block_size, Hkv] fp32. Token t of sequence b (its logical
+ * position, the same one the dense layout uses) lives in pool row
+ *     block_table[b * blocks_per_seq + t / block_size] * block_size
+ *         + t % block_size.
+ * The problem's cache_capacity must equal blocks_per_seq * block_size; it
+ * remains the row stride of the score tensor. Every other argument, the
+ * workspace size (dsa_workspace_size with the same op) and every result are
+ * those of the dense call on the gathered (logical) caches, bit for bit.
+ *
+ *   block_size      tokens per block: a power of two from 128 to 2^20 (a
+ *                   128-key indexer tile never straddles two blocks)
+ *   num_blocks      blocks in the pool (num_blocks * block_size * Hkv < 2^31)
+ *   blocks_per_seq  columns of the block table
+ *   block_table     DEVICE [B, blocks_per_seq] int32, 4-byte aligned, owned by
+ *                   the caller. Entries of blocks that hold any of a
+ *                   sequence's first total_len[b] tokens must lie in
+ *                   [0, num_blocks); the others are never read. An entry
+ *                   outside the pool is read as block 0 (no memory outside the
+ *                   pool is touched): a gathered key from such a block sets
+ *                   bit 1 of the device status word, and dsa_cache_append_paged
+ *                   writes nothing through such an entry.
+ * Blocks may be shared between sequences (a common prefix); the append must
+ * not write a block another sequence reads in the same step.
+ */
+typedef struct dsa_kv_pages {
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t blocks_per_seq;
+  const int32_t* block_table;
+} dsa_kv_pages;
+
+/* dsa_index_scores on a paged index-key pool (kI as described above). */
+int dsa_index_scores_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* qI,
+                           const float* w, const void* kI, float* scores, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* dsa_sparse_attn_decode on paged kI / K / V / scale pools. */
+int dsa_sparse_attn_decode_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* q,
+                                 const void* qI, const float* w, const void* kI, const void* k,
+                                 const void* v, const float* k_scale, const float* v_scale,
+                                 int32_t* idx_out, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/* dsa_sparse_attn_prefill on paged kI / K / V / scale pools. */
+int dsa_sparse_attn_prefill_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* q,
+                                  const void* qI, const float* w, const void* kI, const void* k,
+                                  const void* v, const float* k_scale, const float* v_scale,
+                                  int32_t* idx_out, void* out, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* dsa_cache_append into paged pools: token s of sequence b goes to the pool
+ * row of logical position total_len[b] - q_len + s. */
+int dsa_cache_append_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* kI_new,
+                           const void* k_new, const void* v_new, void* kI, void* k, void* v,
+                           float* k_scale, float* v_scale, void* stream);
+
+/*
  * Synchronises `stream`, then copies the device status word from the
  * workspace to *status_out (0 = no device-side problem; bit 0 = a bounded
- * wait ran out). Returns DSA_ERR_TIMEOUT if that bit is set.
+ * wait ran out; bit 1 = a gathered key's block-table entry lay outside the
+ * pool). Returns DSA_ERR_TIMEOUT if bit 0 is set, else DSA_ERR_INVALID_ARG if
+ * bit 1 is set.
  */
 int dsa_read_device_status(const void* workspace, size_t workspace_bytes,
                            void* stream, uint32_t* status_out);

@@ -45,6 +45,10 @@ R11 cache append (the step before the indexer): the S new tokens of a
     computed in fp32 (the kernel's precision): absmax and x are exact fp32
     values, scale and x / scale are IEEE fp32 divisions. A 16-bit cache of
     the other 16-bit type takes the value rounded to nearest even.
+R12 paged caches (PR #33802's page, the companion 256K change: a pool of
+    block_size-token blocks and a per-sequence block table): token t of
+    sequence b is pool row table[b, t // block_size] * block_size
+    + t % block_size; every result is the dense one on the gathered caches.
 
 Parity pins for every function live in tests/test_oracle_pins.py.
 """
@@ -256,3 +260,21 @@ def cache_append(kI, k, v, k_scale, v_scale, kI_new, k_new, v_new, total_len, kv
                     else:
                         dst[b, t, g] = round_to(src[b, s, g], kv_dtype)
     return kI, k, v, k_scale, v_scale
+
+
+# ---------------------------------------------------------------------------
+# paged caches (R12)
+# ---------------------------------------------------------------------------
+def gather_pages(pool, table, block_size: int, total_len):
+    """Logical [B, cap, ...] cache of a paged pool: row t of sequence b is
+    pool[table[b, t // block_size] * block_size + t % block_size] for
+    t < total_len[b]; rows past a sequence's length are zero (never read)."""
+    pool = np.asarray(pool)
+    table = np.asarray(table)
+    B, per_seq = table.shape
+    cap = per_seq * block_size
+    out = np.zeros((B, cap) + pool.shape[1:], dtype=np.float64)
+    for b in range(B):
+        for t in range(int(total_len[b])):
+            out[b, t] = pool[table[b, t // block_size] * block_size + t % block_size]
+    return out

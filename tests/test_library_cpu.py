@@ -160,3 +160,59 @@ def test_cache_append_without_gpu_reports_no_device(lib):
     from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_NO_DEVICE
     p = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8)
     assert _call_append(lib, p, {"v_new": 0x10800}) == DSA_ERR_NO_DEVICE
+
+
+def _pages(bs=256, nb=1037, per_seq=1024, table=0x40000):
+    from top_sparse_attention_chunked_gb300.dsa import DsaKvPages
+    return DsaKvPages(bs, nb, per_seq, table)
+
+
+def _call_decode_paged(lib, p, pg, ws_bytes, ws=0x10000):
+    vals = [0x1000] * 6
+    return lib.dsa_sparse_attn_decode_paged(ctypes.byref(p), ctypes.byref(pg) if pg else None,
+                                            *[ctypes.c_void_p(v) for v in vals], None, None, None,
+                                            ctypes.c_void_p(0x2000), ctypes.c_void_p(ws),
+                                            ws_bytes, None)
+
+
+@pytest.mark.parametrize("pg_kw,status,frag", [
+    (dict(bs=100, per_seq=1311), 2, "power of two"),
+    (dict(bs=64, per_seq=2048), 2, "power of two"),
+    (dict(nb=0), 1, "num_blocks"),
+    (dict(per_seq=1000), 1, "blocks_per_seq * block_size"),
+    (dict(table=0), 1, "block_table is NULL"),
+    (dict(table=0x40002), 4, "4-byte aligned"),
+    (dict(nb=1 << 22), 2, "below 2^31"),
+])
+def test_paged_descriptor_rejected_on_host(lib, pg_kw, status, frag):
+    from top_sparse_attention_chunked_gb300.dsa import DSA_OP_DECODE
+    p = _prob(q_len=8, total_len=262144, kv_dtype="int8")
+    need = lib.dsa_workspace_size(ctypes.byref(p), DSA_OP_DECODE)
+    assert _call_decode_paged(lib, p, _pages(**pg_kw), need) == status
+    assert frag in lib.dsa_last_error_string().decode()
+
+
+def test_paged_calls_need_a_descriptor(lib):
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_INVALID_ARG, DSA_OP_DECODE
+    p = _prob(q_len=8, total_len=262144, kv_dtype="int8")
+    need = lib.dsa_workspace_size(ctypes.byref(p), DSA_OP_DECODE)
+    assert _call_decode_paged(lib, p, None, need) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_append_paged(ctypes.byref(p), None, *([None] * 9)) == DSA_ERR_INVALID_ARG
+    assert lib.dsa_index_scores_paged(ctypes.byref(p), None, None, None, None, None, None, 0,
+                                      None) == DSA_ERR_INVALID_ARG
+
+
+def test_paged_valid_call_without_gpu_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_NO_DEVICE, DSA_OP_DECODE
+    p = _prob(q_len=8, total_len=262144, kv_dtype="int8")
+    need = lib.dsa_workspace_size(ctypes.byref(p), DSA_OP_DECODE)
+    vals = [0x1000] * 6
+    rc = lib.dsa_sparse_attn_decode_paged(ctypes.byref(p), ctypes.byref(_pages()),
+                                          *[ctypes.c_void_p(v) for v in vals],
+                                          ctypes.c_void_p(0x3000), ctypes.c_void_p(0x3000), None,
+                                          ctypes.c_void_p(0x2000), ctypes.c_void_p(0x10000), need,
+                                          None)
+    assert rc == DSA_ERR_NO_DEVICE

@@ -414,6 +414,21 @@ def test_append_int8_dequantises_to_within_half_a_step():
 
 
 # ---------------------------------------------------------------------------
+# paged caches (R12)
+# ---------------------------------------------------------------------------
+def check_gather_pages(mod):
+    """block_size 2, pool rows labelled 10*row; table [[2, 0], [1, 3]]:
+    sequence 0 is pool rows 4, 5, 0 (3 tokens), sequence 1 rows 2, 3, 6, 7."""
+    pool = (10.0 * np.arange(8)).reshape(8, 1)
+    view = mod.gather_pages(pool, np.array([[2, 0], [1, 3]]), 2, [3, 4])
+    assert view[:, :, 0].tolist() == [[40.0, 50.0, 0.0, 0.0], [20.0, 30.0, 60.0, 70.0]]
+
+
+def test_gather_pages_hand_case():
+    check_gather_pages(O)
+
+
+# ---------------------------------------------------------------------------
 # mutation tests: plant a mistake in a copy of the oracle, a pin must fail
 # ---------------------------------------------------------------------------
 class _Mutant:
@@ -540,3 +555,16 @@ def test_mutant_append_one_row_late_is_caught():
         return O.cache_append(kI, k, v, k_scale, v_scale, kI_new, k_new, v_new,
                               [t + 1 if t + 1 <= kI.shape[1] else t for t in total_len], kv_dtype)
     assert _fails(check_append_positions, _Mutant(cache_append=bad))
+
+
+def test_mutant_page_index_swapped_is_caught():
+    def bad(pool, table, block_size, total_len):
+        pool = np.asarray(pool)
+        table = np.asarray(table)
+        B, per_seq = table.shape
+        out = np.zeros((B, per_seq * block_size) + pool.shape[1:])
+        for b in range(B):
+            for t in range(int(total_len[b])):
+                out[b, t] = pool[table[b, t % per_seq] * block_size + t // per_seq]
+        return out
+    assert _fails(check_gather_pages, _Mutant(gather_pages=bad))

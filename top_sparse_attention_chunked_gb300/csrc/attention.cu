@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   if (threadIdx.x == 0) s_abort = 0;
 
   const int32_t* idx_row = p.idx + static_cast<size_t>(r) * p.topk + split_begin;
-  const size_t sc_base = static_cast<size_t>(b) * p.cap * p.Hkv + g;
+  bool bad_page = false;   // a gathered key's block-table entry lay outside the pool
 
   // gather the 16 selected rows of tile `it` (this warp's it-th tile) into
   // stage st: lane l < 16 holds key l's row; rows past the split (and any
@@ -227,6 +227,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       key = s_idx[o + lane];
       if (key < 0 || key >= T) key = -1;
     }
+    // the key's cache row (key 0's for invalid keys, whose logits are masked)
+    const long long crow = cache_row(p.pg, b, p.cap, key < 0 ? 0 : key, &bad_page);
     if constexpr (KV == KV_INT8) {
       // INT8 rows (128 B): 16-byte cp.async measured faster here than row
       // gathers; codes and scales land zero-filled for invalid keys
@@ -237,18 +239,20 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
         const int j = lane + 32 * i;            // 0..127: row j/8, chunk j%8
         const int row = j >> 3, c = j & 7;
         const int kr = __shfl_sync(0xffffffffu, key, row);
-        const size_t off = ((static_cast<size_t>(b) * p.cap + (kr < 0 ? 0 : kr)) * p.Hkv + g) * kD + c * 16;
+        const long long cr = __shfl_sync(0xffffffffu, crow, row);
+        const size_t off = (static_cast<size_t>(cr) * p.Hkv + g) * kD + c * 16;
         cp_async16(sKc[st] + row * kD + c * 16, kb + off, kr >= 0);
         cp_async16(sVc[st] + row * kD + c * 16, vb + off, kr >= 0);
       }
       const int kr = __shfl_sync(0xffffffffu, key, lane & 15);
-      const size_t so = sc_base + static_cast<size_t>(kr < 0 ? 0 : kr) * p.Hkv;
+      const long long cr = __shfl_sync(0xffffffffu, crow, lane & 15);
+      const size_t so = static_cast<size_t>(cr) * p.Hkv + g;
       if (lane < 16) cp_async4(sSc + st * 32 + lane, p.k_scale + so, kr >= 0);
       else cp_async4(sSc + st * 32 + lane, p.v_scale + so, kr >= 0);
     } else {
       // 16-bit rows (256 B): TMA row gathers, lane l of the first 16 issuing
       // one for 4 rows (grp) of one column block (blk) of K or V (tsr)
-      const int yrow = (b * p.cap + (key < 0 ? 0 : key)) * p.Hkv + g;
+      const int yrow = static_cast<int>(crow * p.Hkv + g);
       const int grp = lane & 3, blk = (lane >> 2) & 1, tsr = lane >> 3;
       const int y0 = __shfl_sync(0xffffffffu, yrow, 4 * grp);
       const int y1 = __shfl_sync(0xffffffffu, yrow, 4 * grp + 1);
@@ -469,6 +473,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   }
   __syncthreads();   // stage buffers become the merge area
   if (threadIdx.x == 0 && s_abort && p.status) atomicOr(p.status, kDevTimeout);
+  if (__any_sync(0xffffffffu, bad_page) && lane == 0 && p.status) atomicOr(p.status, kDevBadPage);
   float* ws = reinterpret_cast<float*>(smem);      // [warps][kPartialFloats]
   float* fac1 = ws + kAttnWarps * kPartialFloats;  // [max(warps, splits)][16]
   float* fac2 = fac1 + kMaxCombine * kAttnRows;

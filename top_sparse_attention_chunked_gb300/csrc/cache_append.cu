@@ -142,9 +142,10 @@ __device__ __forceinline__ uint4 convert8(uint4 u, bool src_fp16) {
 
 // Grid: z = the sequence b, y = 0 (index keys), 1 (K) or 2 (V), x = tiles of
 // rows. For one sequence the new K (or V) rows of all heads are one
-// contiguous span of q_len * Hkv rows, and so are the cache rows they go to
-// (rows (T_b - q_len) * Hkv ...), whatever the head; a tile is kAppRowsK of
-// them. The tile is staged in shared memory with cp.async (eight 16-byte
+// contiguous span of q_len * Hkv rows, and in a dense cache so are the rows
+// they go to (rows (T_b - q_len) * Hkv ...), whatever the head; a tile is
+// kAppRowsK of them. In a paged cache each row's destination goes through the
+// block table, and a row whose entry lies outside the pool is not written. The tile is staged in shared memory with cp.async (eight 16-byte
 // copies per thread in flight, no registers held), then eight lanes take a
 // row: lane l reads bytes 16l and 128 + 16l of it (elements 8l..8l+7 and
 // 64+8l..64+8l+7), so each 8-lane phase of a shared load covers 128
@@ -177,9 +178,16 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(const AppendP
       if (r[i] < p.S) u[i] = ld_stream(src + (tok0 + r[i]) * DSA_IDX_DIM + part[i] * 8);
     }
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (r[i] < p.S)
-        *reinterpret_cast<uint4*>(dst + (dst0 + r[i]) * DSA_IDX_DIM + part[i] * 8) = u[i];
+    for (int i = 0; i < 2; ++i) {
+      if (r[i] >= p.S) continue;
+      long long row = dst0 + r[i];
+      if (p.pg.table != nullptr) {
+        bool bad = false;
+        row = cache_row(p.pg, b, p.cap, p.lens.T[b] - p.S + static_cast<int>(r[i]), &bad);
+        if (bad) continue;   // never write through an entry outside the pool
+      }
+      *reinterpret_cast<uint4*>(dst + row * DSA_IDX_DIM + part[i] * 8) = u[i];
+    }
     return;
   }
   const bool is_k = (kind == 1);
@@ -208,7 +216,13 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(const AppendP
     uint4 u[2];
     u[0] = *reinterpret_cast<const uint4*>(row + l8 * 16);
     u[1] = *reinterpret_cast<const uint4*>(row + 128 + l8 * 16);
-    const long long drow = drow0 + rr;
+    long long drow = drow0 + rr;
+    bool bad = false;
+    if (p.pg.table != nullptr && valid) {
+      const int rs = static_cast<int>(r0) + rr;      // row within the sequence's span
+      const int tok = rs / p.Hkv;
+      drow = cache_row(p.pg, b, p.cap, p.lens.T[b] - p.S + tok, &bad) * p.Hkv + (rs - tok * p.Hkv);
+    }
     if (p.kv_dtype == DSA_INT8) {
       float x[16];
       unpack16(u, src16, x);
@@ -223,13 +237,13 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(const AppendP
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       const float scale = __fdiv_rn(amax, 127.0f);   // 0 for an all-zero row
       const uint4 codes = quantize16(x, scale);
-      if (!valid) continue;
+      if (!valid || bad) continue;
       int8_t* dst = static_cast<int8_t*>(is_k ? p.k : p.v) + drow * DSA_HEAD_DIM;
       *reinterpret_cast<uint2*>(dst + l8 * 8) = make_uint2(codes.x, codes.y);
       *reinterpret_cast<uint2*>(dst + 64 + l8 * 8) = make_uint2(codes.z, codes.w);
       if (l8 == 0) (is_k ? p.k_scale : p.v_scale)[drow] = scale;
     } else {
-      if (!valid) continue;
+      if (!valid || bad) continue;
       uint4 o0 = u[0], o1 = u[1];   // same 16-bit type: a copy
       if (p.kv_dtype != p.q_dtype) {
         o0 = convert8(o0, src16);

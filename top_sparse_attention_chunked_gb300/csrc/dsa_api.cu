@@ -314,6 +314,37 @@ SeqLens lens_of(const dsa_problem* p) {
   return s;
 }
 
+// Cache rows (tokens) the kI / K / V arrays hold: the dense [B, cap] layout or
+// the paged pool.
+long long pool_tokens(const dsa_problem* p, const Paging& pg) {
+  return pg.table ? (static_cast<long long>(pg.num_blocks) << pg.shift)
+                  : static_cast<long long>(p->batch) * p->cache_capacity;
+}
+
+const Paging kDense = {nullptr, 0, 0, 0};
+
+// Validates a paged-cache descriptor against the problem and fills *pg.
+int check_pages(const dsa_problem* p, const dsa_kv_pages* pages, Paging* pg) {
+  if (!pages) return fail(DSA_ERR_INVALID_ARG, "pages is NULL");
+  const int bs = pages->block_size;
+  if (bs < 128 || bs > (1 << 20) || (bs & (bs - 1)) != 0)
+    return fail(DSA_ERR_UNSUPPORTED, "block_size %d must be a power of two from 128 to 2^20", bs);
+  if (pages->num_blocks < 1) return fail(DSA_ERR_INVALID_ARG, "num_blocks %d < 1", pages->num_blocks);
+  if (pages->blocks_per_seq < 1)
+    return fail(DSA_ERR_INVALID_ARG, "blocks_per_seq %d < 1", pages->blocks_per_seq);
+  if (static_cast<long long>(pages->blocks_per_seq) * bs != p->cache_capacity)
+    return fail(DSA_ERR_INVALID_ARG, "cache_capacity %d must equal blocks_per_seq * block_size (%lld)",
+                p->cache_capacity, static_cast<long long>(pages->blocks_per_seq) * bs);
+  if (!pages->block_table) return fail(DSA_ERR_INVALID_ARG, "block_table is NULL");
+  if (!aligned(pages->block_table, 4)) return fail(DSA_ERR_MISALIGNED, "block_table must be 4-byte aligned");
+  if ((static_cast<long long>(pages->num_blocks) * bs) * std::max(1, p->num_kv_heads) >= (1LL << 31))
+    return fail(DSA_ERR_UNSUPPORTED, "num_blocks * block_size * num_kv_heads must be below 2^31");
+  int shift = 0;
+  while ((1 << shift) < bs) ++shift;
+  *pg = Paging{pages->block_table, pages->blocks_per_seq, shift, pages->num_blocks};
+  return DSA_OK;
+}
+
 int pow2_at_least(int x) {
   int v = 1;
   while (v < x) v <<= 1;
@@ -321,10 +352,11 @@ int pow2_at_least(int x) {
 }
 
 // ------------------------------------------------------------------ stages
-int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const void* qI,
-                const float* w, const void* kI, float* scores, uint32_t* hist, uint32_t* status,
-                cudaStream_t st) {
+int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Paging& pg,
+                const void* qI, const float* w, const void* kI, float* scores, uint32_t* hist,
+                uint32_t* status, cudaStream_t st) {
   IndexerParams ip;
+  ip.pg = pg;
   ip.w = w;
   ip.scores = scores;
   ip.hist = hist;
@@ -349,7 +381,7 @@ int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, co
   }
   ip.total_units = total;
   CUtensorMap tm_kI, tm_qI;
-  int rc = make_map_rows64(&tm_kI, kI, static_cast<long long>(p->batch) * p->cache_capacity, kKeyTile);
+  int rc = make_map_rows64(&tm_kI, kI, pool_tokens(p, pg), kKeyTile);
   if (rc) return rc;
   rc = make_map_rows64(&tm_qI, qI, static_cast<long long>(d.rows) * DSA_IDX_HEADS, ip.QB * 16);
   if (rc) return rc;
@@ -438,9 +470,11 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
 }
 
 int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
-                  const void* q, const void* k, const void* v, const float* ks, const float* vs,
-                  const int32_t* idx, void* out, void* ws, bool prefill, cudaStream_t st) {
+                  const Paging& pg, const void* q, const void* k, const void* v, const float* ks,
+                  const float* vs, const int32_t* idx, void* out, void* ws, bool prefill,
+                  cudaStream_t st) {
   AttnParams ap;
+  ap.pg = pg;
   ap.q = q;
   ap.k = k;
   ap.v = v;
@@ -476,7 +510,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   timing_before(DSA_KERNEL_ATTENTION, st);
   if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin)) {
     CUtensorMap tm_k, tm_v;
-    const long long rows = static_cast<long long>(p->batch) * p->cache_capacity * p->num_kv_heads;
+    const long long rows = pool_tokens(p, pg) * p->num_kv_heads;
     int rc = make_map_kv_rows(&tm_k, k, rows);
     if (rc == DSA_OK) rc = make_map_kv_rows(&tm_v, v, rows);
     if (rc != DSA_OK) {
@@ -486,10 +520,10 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
     e = launch_prefill_tc(ap, p->kv_dtype, di.sms, tm_k, tm_v, at<uint32_t>(ws, 0), st);
   } else {
     // row gathers (16-bit caches) address rows with signed 32-bit coordinates
-    const long long rows = static_cast<long long>(p->batch) * p->cache_capacity * p->num_kv_heads;
+    const long long rows = pool_tokens(p, pg) * p->num_kv_heads;
     if (p->kv_dtype != DSA_INT8 && rows >= (1LL << 31)) {
       timing_after(DSA_KERNEL_ATTENTION, st);
-      return fail(DSA_ERR_UNSUPPORTED, "batch * cache_capacity * num_kv_heads must be below 2^31");
+      return fail(DSA_ERR_UNSUPPORTED, "cache rows * num_kv_heads must be below 2^31");
     }
     CUtensorMap tm_k{}, tm_v{};   // INT8 caches are gathered with cp.async
     int rc = DSA_OK;
@@ -508,8 +542,9 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   return DSA_OK;
 }
 
-bool prefill_tc_ok(const dsa_problem* p, const Derived& d, const DeviceInfo& di) {
+bool prefill_tc_ok(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Paging& pg) {
   AttnParams ap{};
+  ap.pg = pg;
   ap.topk = p->top_k;
   ap.B = p->batch;
   ap.cap = p->cache_capacity;
@@ -537,7 +572,7 @@ int check_attn_ptrs(const dsa_problem* p, const void* q, const void* qI, const f
   return DSA_OK;
 }
 
-int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const float* w,
+int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, const void* qI, const float* w,
               const void* kI, const void* k, const void* v, const float* ks, const float* vs,
               int32_t* idx_out, void* out, void* ws, size_t ws_bytes, void* stream) {
   reset_launches();
@@ -563,7 +598,7 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
   const bool hist_in_indexer = decode;
   int split_keys = 0, nsplit = 1;
   choose_split(p, d, di.sms, &split_keys, &nsplit);
-  const bool tc_prefill = !decode && p->attn_split_keys == 0 && prefill_tc_ok(p, d, di);
+  const bool tc_prefill = !decode && p->attn_split_keys == 0 && prefill_tc_ok(p, d, di, pg);
   const bool attn_tickets = !tc_prefill && nsplit > 1 && !attn_uses_cluster(nsplit);
   if (hist_in_indexer || attn_tickets) {
     // histograms, tickets and counters start at zero; the clearing kernel
@@ -574,12 +609,50 @@ int attn_call(const dsa_problem* p, int op, const void* q, const void* qI, const
   float* scores = at<float>(ws, L.scores);
   int32_t* idx = idx_out ? idx_out : at<int32_t>(ws, L.idx);
   uint32_t* status = at<uint32_t>(ws, 0);
-  rc = run_indexer(p, d, di, qI, w, kI, scores, hist_in_indexer ? at<uint32_t>(ws, L.hist) : nullptr,
+  rc = run_indexer(p, d, di, pg, qI, w, kI, scores, hist_in_indexer ? at<uint32_t>(ws, L.hist) : nullptr,
                    status, st);
   if (rc) return rc;
   rc = run_topk(p, d, di, L, scores, idx, ws, hist_in_indexer, topk_rows, true, st);
   if (rc) return rc;
-  return run_attention(p, d, di, L, q, k, v, ks, vs, idx, out, ws, !decode, st);
+  return run_attention(p, d, di, L, pg, q, k, v, ks, vs, idx, out, ws, !decode, st);
+}
+
+int index_call(const dsa_problem* p, const dsa_kv_pages* pages, const void* qI, const float* w,
+               const void* kI, float* scores, void* ws, size_t ws_bytes, void* stream) {
+  reset_launches();
+  Derived d;
+  int rc = check_problem(p, DSA_OP_INDEX_SCORES, &d);
+  if (rc) return rc;
+  Paging pg = kDense;
+  if (pages && (rc = check_pages(p, pages, &pg))) return rc;
+  if (!qI || !w || !kI || !scores) return fail(DSA_ERR_INVALID_ARG, "a tensor pointer is NULL");
+  if (!aligned(qI, 16) || !aligned(kI, 16) || !aligned(scores, 16) || !aligned(w, 4))
+    return fail(DSA_ERR_MISALIGNED, "qI, kI and scores must be 16-byte aligned, w 4-byte");
+  const Layout L = layout(p, DSA_OP_INDEX_SCORES, d);
+  rc = check_ws(ws, ws_bytes, L);
+  if (rc) return rc;
+  DeviceInfo di;
+  rc = device_info(&di);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  return run_indexer(p, d, di, pg, qI, w, kI, scores, nullptr, at<uint32_t>(ws, 0), st);
+}
+
+int attn_entry(const dsa_problem* p, int op, const dsa_kv_pages* pages, const void* q,
+               const void* qI, const float* w, const void* kI, const void* k, const void* v,
+               const float* ks, const float* vs, int32_t* idx_out, void* out, void* ws,
+               size_t ws_bytes, void* stream) {
+  Paging pg = kDense;
+  if (pages) {
+    reset_launches();
+    Derived d;
+    int rc = check_problem(p, op, &d);
+    if (rc) return rc;
+    if ((rc = check_pages(p, pages, &pg))) return rc;
+  }
+  return attn_call(p, op, pg, q, qI, w, kI, k, v, ks, vs, idx_out, out, ws, ws_bytes, stream);
 }
 
 }  // namespace
@@ -642,23 +715,17 @@ size_t dsa_workspace_size(const dsa_problem* p, int op) {
 
 int dsa_index_scores(const dsa_problem* p, const void* qI, const float* w, const void* kI,
                      float* scores, void* ws, size_t ws_bytes, void* stream) {
-  reset_launches();
-  Derived d;
-  int rc = check_problem(p, DSA_OP_INDEX_SCORES, &d);
-  if (rc) return rc;
-  if (!qI || !w || !kI || !scores) return fail(DSA_ERR_INVALID_ARG, "a tensor pointer is NULL");
-  if (!aligned(qI, 16) || !aligned(kI, 16) || !aligned(scores, 16) || !aligned(w, 4))
-    return fail(DSA_ERR_MISALIGNED, "qI, kI and scores must be 16-byte aligned, w 4-byte");
-  const Layout L = layout(p, DSA_OP_INDEX_SCORES, d);
-  rc = check_ws(ws, ws_bytes, L);
-  if (rc) return rc;
-  DeviceInfo di;
-  rc = device_info(&di);
-  if (rc) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
-  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
-  return run_indexer(p, d, di, qI, w, kI, scores, nullptr, at<uint32_t>(ws, 0), st);
+  return index_call(p, nullptr, qI, w, kI, scores, ws, ws_bytes, stream);
+}
+
+int dsa_index_scores_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* qI,
+                           const float* w, const void* kI, float* scores, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!pages) {
+    reset_launches();
+    return fail(DSA_ERR_INVALID_ARG, "pages is NULL");
+  }
+  return index_call(p, pages, qI, w, kI, scores, ws, ws_bytes, stream);
 }
 
 int dsa_topk(const dsa_problem* p, const float* scores, int32_t* idx, void* ws, size_t ws_bytes,
@@ -688,7 +755,7 @@ int dsa_sparse_attn_decode(const dsa_problem* p, const void* q, const void* qI, 
                            const void* kI, const void* k, const void* v, const float* k_scale,
                            const float* v_scale, int32_t* idx_out, void* out, void* ws,
                            size_t ws_bytes, void* stream) {
-  return attn_call(p, DSA_OP_DECODE, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
+  return attn_entry(p, DSA_OP_DECODE, nullptr, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
                    ws_bytes, stream);
 }
 
@@ -696,17 +763,19 @@ int dsa_sparse_attn_prefill(const dsa_problem* p, const void* q, const void* qI,
                             const void* kI, const void* k, const void* v, const float* k_scale,
                             const float* v_scale, int32_t* idx_out, void* out, void* ws,
                             size_t ws_bytes, void* stream) {
-  return attn_call(p, DSA_OP_PREFILL, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
+  return attn_entry(p, DSA_OP_PREFILL, nullptr, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
                    ws_bytes, stream);
 }
 
-int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new,
-                     const void* v_new, void* kI, void* k, void* v, float* k_scale,
-                     float* v_scale, void* stream) {
+static int append_call(const dsa_problem* p, const dsa_kv_pages* pages, const void* kI_new,
+                       const void* k_new, const void* v_new, void* kI, void* k, void* v,
+                       float* k_scale, float* v_scale, void* stream) {
   reset_launches();
   Derived d;
   int rc = check_problem(p, DSA_OP_PREFILL, &d);
   if (rc) return rc;
+  Paging pg = kDense;
+  if (pages && (rc = check_pages(p, pages, &pg))) return rc;
   if (!kI_new || !k_new || !v_new || !kI || !k || !v)
     return fail(DSA_ERR_INVALID_ARG, "a required tensor pointer is NULL");
   const bool int8 = (p->kv_dtype == DSA_INT8);
@@ -721,14 +790,15 @@ int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new
       !aligned(k, 16) || !aligned(v, 16))
     return fail(DSA_ERR_MISALIGNED, "kI_new, k_new, v_new, kI, k and v must be 16-byte aligned");
   // the new tokens are read while the caches are written: no input may overlap an output
-  const long long B = p->batch, S = p->q_len, H = p->num_kv_heads, cap = p->cache_capacity;
+  const long long B = p->batch, S = p->q_len, H = p->num_kv_heads;
+  const long long rows = pool_tokens(p, pg);   // cache rows (dense or the pool)
   struct Span { const void* p; long long n; };
   const Span in[3] = {{kI_new, B * S * DSA_IDX_DIM * 2}, {k_new, B * S * H * DSA_HEAD_DIM * 2},
                       {v_new, B * S * H * DSA_HEAD_DIM * 2}};
   const long long row_bytes = int8 ? DSA_HEAD_DIM : DSA_HEAD_DIM * 2;
-  const Span out[5] = {{kI, B * cap * DSA_IDX_DIM * 2}, {k, B * cap * H * row_bytes},
-                       {v, B * cap * H * row_bytes}, {k_scale, int8 ? B * cap * H * 4 : 0},
-                       {v_scale, int8 ? B * cap * H * 4 : 0}};
+  const Span out[5] = {{kI, rows * DSA_IDX_DIM * 2}, {k, rows * H * row_bytes},
+                       {v, rows * H * row_bytes}, {k_scale, int8 ? rows * H * 4 : 0},
+                       {v_scale, int8 ? rows * H * 4 : 0}};
   for (const Span& a : in)
     for (const Span& o : out) {
       const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), o0 = reinterpret_cast<uintptr_t>(o.p);
@@ -753,6 +823,7 @@ int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new
   ap.cap = p->cache_capacity;
   ap.q_dtype = p->q_dtype;
   ap.kv_dtype = p->kv_dtype;
+  ap.pg = pg;
   for (int b = 0; b < p->batch; ++b) ap.lens.T[b] = p->total_len[b];
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   timing_before(DSA_KERNEL_APPEND, st);
@@ -760,6 +831,48 @@ int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new
   if (e != cudaSuccess) return cuda_fail(e, "cache append launch");
   timing_after(DSA_KERNEL_APPEND, st);
   return DSA_OK;
+}
+
+int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new,
+                     const void* v_new, void* kI, void* k, void* v, float* k_scale,
+                     float* v_scale, void* stream) {
+  return append_call(p, nullptr, kI_new, k_new, v_new, kI, k, v, k_scale, v_scale, stream);
+}
+
+int dsa_cache_append_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* kI_new,
+                           const void* k_new, const void* v_new, void* kI, void* k, void* v,
+                           float* k_scale, float* v_scale, void* stream) {
+  if (!pages) {
+    reset_launches();
+    return fail(DSA_ERR_INVALID_ARG, "pages is NULL");
+  }
+  return append_call(p, pages, kI_new, k_new, v_new, kI, k, v, k_scale, v_scale, stream);
+}
+
+int dsa_sparse_attn_decode_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* q,
+                                 const void* qI, const float* w, const void* kI, const void* k,
+                                 const void* v, const float* k_scale, const float* v_scale,
+                                 int32_t* idx_out, void* out, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (!pages) {
+    reset_launches();
+    return fail(DSA_ERR_INVALID_ARG, "pages is NULL");
+  }
+  return attn_entry(p, DSA_OP_DECODE, pages, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
+                    ws, ws_bytes, stream);
+}
+
+int dsa_sparse_attn_prefill_paged(const dsa_problem* p, const dsa_kv_pages* pages, const void* q,
+                                  const void* qI, const float* w, const void* kI, const void* k,
+                                  const void* v, const float* k_scale, const float* v_scale,
+                                  int32_t* idx_out, void* out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!pages) {
+    reset_launches();
+    return fail(DSA_ERR_INVALID_ARG, "pages is NULL");
+  }
+  return attn_entry(p, DSA_OP_PREFILL, pages, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
+                    ws, ws_bytes, stream);
 }
 
 int dsa_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32_t* status_out) {
@@ -773,6 +886,8 @@ int dsa_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   *status_out = v;
   if (v & kDevTimeout) return fail(DSA_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+  if (v & kDevBadPage)
+    return fail(DSA_ERR_INVALID_ARG, "a gathered key's block-table entry lies outside the pool");
   return DSA_OK;
 }
 

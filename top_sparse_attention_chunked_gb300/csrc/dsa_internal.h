@@ -47,6 +47,30 @@ struct SeqLens {
   int32_t T[DSA_MAX_BATCH];
 };
 
+// Where a sequence's cached token lives. Dense: row b * cap + t of a
+// [B * cap] array. Paged: the caches are a pool of num_blocks blocks of
+// 2^shift tokens and block_table[b * per_seq + t >> shift] names the block
+// holding token t; an entry outside [0, num_blocks) is read as block 0 (no
+// memory outside the pool is touched) and reported as `bad`.
+struct Paging {
+  const int32_t* table;   // [B, per_seq] or nullptr (dense)
+  int per_seq;            // blocks per sequence (columns of the table)
+  int shift;              // log2(block size)
+  int num_blocks;         // blocks in the pool
+};
+
+constexpr uint32_t kDevBadPage = 2u;   // status bit: a block-table entry outside the pool
+
+__device__ __forceinline__ long long cache_row(const Paging& pg, int b, int cap, int t, bool* bad) {
+  if (pg.table == nullptr) return static_cast<long long>(b) * cap + t;
+  int blk = __ldg(pg.table + b * pg.per_seq + (t >> pg.shift));
+  if (blk < 0 || blk >= pg.num_blocks) {
+    *bad = true;
+    blk = 0;
+  }
+  return (static_cast<long long>(blk) << pg.shift) + (t & ((1 << pg.shift) - 1));
+}
+
 // ---------------------------------------------------------------- indexer
 struct IndexerParams {
   const float* w;        // [B, S, 16]
@@ -57,6 +81,7 @@ struct IndexerParams {
   int QB;                // query tokens per block (N = 16 * QB)
   int nqb;               // query blocks per sequence, ceil(S / QB)
   long long total_units; // (sequence, query block, key tile) triples
+  Paging pg;               // cache addressing (dense or paged)
   SeqLens lens;
 };
 
@@ -125,6 +150,7 @@ struct AttnParams {
   int q_dtype, out_dtype;
   float scale_log2;        // softmax_scale * log2(e)
   uint32_t* status;        // device status word (a bounded wait that ran out)
+  Paging pg;               // cache addressing (dense or paged)
   SeqLens lens;
 };
 
@@ -165,6 +191,7 @@ struct AppendParams {
   float* v_scale;
   int B, S, Hkv, cap;
   int q_dtype, kv_dtype;
+  Paging pg;               // cache addressing (dense or paged)
   SeqLens lens;
 };
 

@@ -208,7 +208,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           !mbar_wait_bounded(&bars->empty[s], static_cast<uint32_t>((r - 1) & 1), abort_flag))
         return;
       mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
-      tma_load_2d(sA + s * kATileBytes, &tm_kI, &bars->full[s], 0, c.b * p.cap + c.kt * kKeyTile);
+      // a 128-key tile never straddles a cache block (block sizes are
+      // multiples of 128); an entry outside the pool reads block 0 (the
+      // attention reports it when it gathers from that block)
+      bool bad = false;
+      const int row = static_cast<int>(cache_row(p.pg, c.b, p.cap, c.kt * kKeyTile, &bad));
+      tma_load_2d(sA + s * kATileBytes, &tm_kI, &bars->full[s], 0, row);
       ++ps.issued;
       advance_unit(p, c);
     }

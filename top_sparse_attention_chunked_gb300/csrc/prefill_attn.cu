@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
     const bool issuer = lane < 16;
     long long seq = 0;                   // position in the ring (tiles issued)
     bool ok = true;
+    bool bad_page = false;               // a block-table entry outside the pool was read
     for (long long it = my_first; it < n_items && ok; it += stride) {
       const PfItem w = pf_item(p, it);
       const int b = w.r / p.S;
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           const int j = t * kKeys + 4 * grp + e;
           int key = j < w.keff ? __ldg(idx_row + j) : 0;
           if (key < 0 || key >= T) key = 0;
-          y[e] = (b * p.cap + key) * p.Hkv + w.g;
+          y[e] = static_cast<int>(cache_row(p.pg, b, p.cap, key, &bad_page) * p.Hkv + w.g);
         }
       };
       for (int pass = 0; pass < 2 && ok; ++pass) {            // K tiles, then V tiles
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         }
       }
     }
+    if (bad_page) atomicOr(status, kDevBadPage);
     if (lane == 0) {
       // the ring's last copies may still be landing (the consumers may have
       // given up): wait, bounded, for them before the block can exit
@@ -448,7 +450,9 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
 
 bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin) {
   // gather row coordinates are signed 32-bit
-  const long long rows = static_cast<long long>(p.B) * p.cap * p.Hkv;
+  const long long tokens = p.pg.table ? (static_cast<long long>(p.pg.num_blocks) << p.pg.shift)
+                                      : static_cast<long long>(p.B) * p.cap;
+  const long long rows = tokens * p.Hkv;
   return (kv_dtype == DSA_BF16 || kv_dtype == DSA_FP16) && p.topk <= pf::kMaxTiles * pf::kKeys &&
          rows < (1LL << 31) && pf::kSmemBytes <= smem_optin;
 }

@@ -32,11 +32,23 @@ EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_sparse_attn_decode", "dsa_sparse_attn_prefill",
             "dsa_read_device_status", "dsa_last_error_string", "dsa_status_string",
             "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc",
-            "dsa_last_launches", "dsa_cache_append"]
+            "dsa_last_launches", "dsa_cache_append", "dsa_index_scores_paged",
+            "dsa_sparse_attn_decode_paged", "dsa_sparse_attn_prefill_paged",
+            "dsa_cache_append_paged"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
              DSA_FP32: torch.float32}
+
+
+class DsaKvPages(ctypes.Structure):
+    """dsa_kv_pages: a paged kI / K / V pool and its device block table."""
+    _fields_ = [
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("blocks_per_seq", ctypes.c_int32),
+        ("block_table", ctypes.c_void_p),
+    ]
 
 
 class DsaProblem(ctypes.Structure):
@@ -80,6 +92,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(p)
     vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     P = ctypes.POINTER(DsaProblem)
+    PG = ctypes.POINTER(DsaKvPages)
     sig = {
         "dsa_workspace_size": (sz, [P, i32]),
         "dsa_index_scores": (i32, [P, vp, vp, vp, vp, vp, sz, vp]),
@@ -95,6 +108,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_timing_read": (i32, [ctypes.POINTER(ctypes.c_float)]),
         "dsa_topk_noalloc": (i32, [P, vp, vp, vp]),
         "dsa_cache_append": (i32, [P] + [vp] * 9),
+        "dsa_index_scores_paged": (i32, [P, PG, vp, vp, vp, vp, vp, sz, vp]),
+        "dsa_sparse_attn_decode_paged": (i32, [P, PG] + [vp] * 11 + [sz, vp]),
+        "dsa_sparse_attn_prefill_paged": (i32, [P, PG] + [vp] * 11 + [sz, vp]),
+        "dsa_cache_append_paged": (i32, [P, PG] + [vp] * 9),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -182,14 +199,36 @@ def _ws(ws: torch.Tensor):
     return _ptr(ws, "workspace", torch.uint8), ws.numel()
 
 
-def dsa_index_scores(p: DsaProblem, qI, w, kI, scores, workspace, stream=None):
+def make_pages(block_table: torch.Tensor, block_size: int, num_blocks: int) -> DsaKvPages:
+    """A dsa_kv_pages for a device int32 block table [B, blocks_per_seq]
+    (the table tensor is kept alive by the returned object)."""
+    _ptr(block_table, "block_table", torch.int32)
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [B, blocks_per_seq]")
+    pg = DsaKvPages(block_size, num_blocks, block_table.shape[1], block_table.data_ptr())
+    pg._table = block_table
+    return pg
+
+
+def _cache_shapes(p: DsaProblem, pages: Optional[DsaKvPages]):
+    """Leading dims of the kI / K / V / scale arrays: [B, cap] or the pool."""
+    if pages is None:
+        return (p.batch, p.cache_capacity)
+    return (pages.num_blocks * pages.block_size,)
+
+
+def dsa_index_scores(p: DsaProblem, qI, w, kI, scores, workspace, stream=None, pages=None):
     B, S, cap = p.batch, p.q_len, p.cache_capacity
     lib = load_library()
     wp, wn = _ws(workspace)
-    _check(lib.dsa_index_scores(
-        ctypes.byref(p), _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
-        _ptr(w, "w", torch.float32, (B, S, 16)), _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)),
-        _ptr(scores, "scores", torch.float32, (B, S, cap)), wp, wn, _stream(stream)))
+    lead = _cache_shapes(p, pages)
+    args = [ctypes.byref(p), _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
+            _ptr(w, "w", torch.float32, (B, S, 16)), _ptr(kI, "kI", torch.bfloat16, lead + (64,)),
+            _ptr(scores, "scores", torch.float32, (B, S, cap)), wp, wn, _stream(stream)]
+    if pages is None:
+        _check(lib.dsa_index_scores(*args))
+    else:
+        _check(lib.dsa_index_scores_paged(args[0], ctypes.byref(pages), *args[1:]))
 
 
 def dsa_topk(p: DsaProblem, scores, idx, workspace, stream=None):
@@ -212,53 +251,62 @@ def dsa_topk_noalloc(p: DsaProblem, scores, idx, stream=None):
 
 
 def dsa_cache_append(p: DsaProblem, kI_new, k_new, v_new, kI, k, v, k_scale=None,
-                     v_scale=None, stream=None):
+                     v_scale=None, stream=None, pages=None):
     """Write the q_len new tokens of every sequence into cache rows
-    total_len[b]-q_len .. total_len[b]-1 (INT8 caches: quantised on write)."""
-    B, S, cap, Hkv = p.batch, p.q_len, p.cache_capacity, p.num_kv_heads
+    total_len[b]-q_len .. total_len[b]-1 (INT8 caches: quantised on write);
+    with `pages` (make_pages) the caches are paged pools."""
+    B, S, Hkv = p.batch, p.q_len, p.num_kv_heads
     lib = load_library()
     qdt, kvdt = _TORCH_DT[p.q_dtype], _TORCH_DT[p.kv_dtype]
-    _check(lib.dsa_cache_append(
-        ctypes.byref(p), _ptr(kI_new, "kI_new", torch.bfloat16, (B, S, 64)),
-        _ptr(k_new, "k_new", qdt, (B, S, Hkv, 128)), _ptr(v_new, "v_new", qdt, (B, S, Hkv, 128)),
-        _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)), _ptr(k, "k", kvdt, (B, cap, Hkv, 128)),
-        _ptr(v, "v", kvdt, (B, cap, Hkv, 128)),
-        _ptr(k_scale, "k_scale", torch.float32, (B, cap, Hkv)),
-        _ptr(v_scale, "v_scale", torch.float32, (B, cap, Hkv)), _stream(stream)))
+    lead = _cache_shapes(p, pages)
+    args = [_ptr(kI_new, "kI_new", torch.bfloat16, (B, S, 64)),
+            _ptr(k_new, "k_new", qdt, (B, S, Hkv, 128)), _ptr(v_new, "v_new", qdt, (B, S, Hkv, 128)),
+            _ptr(kI, "kI", torch.bfloat16, lead + (64,)), _ptr(k, "k", kvdt, lead + (Hkv, 128)),
+            _ptr(v, "v", kvdt, lead + (Hkv, 128)),
+            _ptr(k_scale, "k_scale", torch.float32, lead + (Hkv,)),
+            _ptr(v_scale, "v_scale", torch.float32, lead + (Hkv,)), _stream(stream)]
+    if pages is None:
+        _check(lib.dsa_cache_append(ctypes.byref(p), *args))
+    else:
+        _check(lib.dsa_cache_append_paged(ctypes.byref(p), ctypes.byref(pages), *args))
 
 
-def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream):
-    B, S, cap, Hq, Hkv = p.batch, p.q_len, p.cache_capacity, p.num_q_heads, p.num_kv_heads
+def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream,
+          pages=None):
+    B, S, Hq, Hkv = p.batch, p.q_len, p.num_q_heads, p.num_kv_heads
     lib = load_library()
     wp, wn = _ws(workspace)
     kvdt = _TORCH_DT[p.kv_dtype]
+    lead = _cache_shapes(p, pages)
     args = [
-        ctypes.byref(p),
         _ptr(q, "q", _TORCH_DT[p.q_dtype], (B, S, Hq, 128)),
         _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
         _ptr(w, "w", torch.float32, (B, S, 16)),
-        _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)),
-        _ptr(k, "k", kvdt, (B, cap, Hkv, 128)),
-        _ptr(v, "v", kvdt, (B, cap, Hkv, 128)),
-        _ptr(k_scale, "k_scale", torch.float32, (B, cap, Hkv)),
-        _ptr(v_scale, "v_scale", torch.float32, (B, cap, Hkv)),
+        _ptr(kI, "kI", torch.bfloat16, lead + (64,)),
+        _ptr(k, "k", kvdt, lead + (Hkv, 128)),
+        _ptr(v, "v", kvdt, lead + (Hkv, 128)),
+        _ptr(k_scale, "k_scale", torch.float32, lead + (Hkv,)),
+        _ptr(v_scale, "v_scale", torch.float32, lead + (Hkv,)),
         _ptr(idx_out, "idx_out", torch.int32, (B, S, p.top_k)),
         _ptr(out, "out", _TORCH_DT[p.out_dtype], (B, S, Hq, 128)),
         wp, wn, _stream(stream),
     ]
-    _check(getattr(lib, fn_name)(*args))
+    if pages is None:
+        _check(getattr(lib, fn_name)(ctypes.byref(p), *args))
+    else:
+        _check(getattr(lib, fn_name + "_paged")(ctypes.byref(p), ctypes.byref(pages), *args))
 
 
 def dsa_sparse_attn_decode(p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace,
-                           stream=None):
+                           stream=None, pages=None):
     _attn("dsa_sparse_attn_decode", p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
-          workspace, stream)
+          workspace, stream, pages)
 
 
 def dsa_sparse_attn_prefill(p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace,
-                            stream=None):
+                            stream=None, pages=None):
     _attn("dsa_sparse_attn_prefill", p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
-          workspace, stream)
+          workspace, stream, pages)
 
 
 def dsa_read_device_status(workspace, stream=None) -> int:

@@ -237,6 +237,37 @@ def config_of(wl, graph):
             "cuda_graph": bool(graph)}
 
 
+def to_paged(dev, wl, block_size, spare, seed):
+    """The workload's dense caches scattered over a shuffled pool of
+    block_size-token blocks (the blocks that hold visible tokens plus `spare`
+    unused ones), and the device block table [B, cap / block_size]."""
+    import torch
+    B, cap = wl.batch, wl.cap
+    if cap % block_size:
+        raise SystemExit(f"--paged {block_size}: the cache capacity {cap} is not a multiple")
+    per_seq = cap // block_size
+    used = -(-wl.total_len // block_size)
+    nblocks = B * used + spare
+    g = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(nblocks, generator=g)[:B * used].view(B, used)
+    table = torch.full((B, per_seq), -1, dtype=torch.int32)
+    table[:, :used] = perm.to(torch.int32)
+    table_d = table.cuda()
+    src = perm.reshape(-1).cuda()
+    pools = {}
+    for name in ("kI", "k", "v", "k_scale", "v_scale"):
+        d = dev.get(name)
+        if d is None:
+            pools[name] = None
+            continue
+        tail = tuple(d.shape[2:])
+        pool = torch.zeros((nblocks, block_size) + tail, dtype=d.dtype, device="cuda")
+        blocks = d[:, :used * block_size].reshape((B * used, block_size) + tail)
+        pool[src] = blocks
+        pools[name] = pool.view((nblocks * block_size,) + tail)
+    return pools, table_d, nblocks
+
+
 # ------------------------------------------------------------------ replicas
 # Multi-GPU runs are independent replicas of the workload (the method has no
 # exchange step): one process per GPU, each with its own seeded inputs; the
@@ -293,10 +324,21 @@ def run_libdsa(args, wl):
 
     prefill = wl.q_len > 16
     call = D.dsa_sparse_attn_prefill if prefill else D.dsa_sparse_attn_decode
+    caches = {k: dev[k] for k in ("kI", "k", "v", "k_scale", "v_scale")}
+    pages = None
+    if args.paged:
+        # the same caches in a paged pool (13 spare blocks: the 256K layout's
+        # 1,037 blocks of 256 tokens)
+        pools, table_d, nblocks = to_paged(dev, wl, args.paged, 13, seed=wl.seed)
+        pages = D.make_pages(table_d, args.paged, nblocks)
+        caches = pools
+        for k in ("kI", "k", "v", "k_scale", "v_scale"):
+            dev[k] = None   # only the pool stays resident
+        torch.cuda.empty_cache()
 
     def step():
-        call(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"], dev["k_scale"],
-             dev["v_scale"], idx, out, ws)
+        call(p, dev["q"], dev["qI"], dev["w"], caches["kI"], caches["k"], caches["v"],
+             caches["k_scale"], caches["v_scale"], idx, out, ws, pages=pages)
 
     if args.profile_calls:
         # untimed calls only, for an ncu capture of the step's kernels
@@ -452,7 +494,9 @@ def run_libdsa(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded N(0,1) / U(0,1) tensors, see dsa_inputs.py)",
-            "config": config_of(wl, graph is not None),
+            "config": dict(config_of(wl, graph is not None),
+                           **({"paged": {"block_size": args.paged, "num_blocks": pages.num_blocks}}
+                              if pages is not None else {})),
             "hbm_gbs_step": round(step_gbs, 1),
             "hbm_frac_step": round(step_gbs / hbm, 4),
             "hbm_frac_step_of_8tbs": round(step_gbs / 8000.0, 4),
@@ -599,6 +643,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="run this many untimed calls and exit (for ncu captures)")
+    ap.add_argument("--paged", type=int, default=0,
+                    help="run the step on a paged cache with blocks of this many tokens")
     ap.add_argument("--op", default="step", choices=["step", "append"],
                     help="append: time dsa_cache_append alone on the workload's shape")
     ap.add_argument("--q-len", type=int, default=0,

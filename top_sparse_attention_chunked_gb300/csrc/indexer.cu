@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     UnitCursor c;
     int pb, pqb, nblk;
     long long i, issued;
+    int s;         // stage of tile i (i % stages, kept as a running counter)
+    uint32_t r;    // round of tile i (i / stages)
   } ps{};
+  const bool paged = p.pg.table != nullptr;
   auto produce = [&](long long limit) {
     for (; ps.i < limit; ++ps.i) {
       UnitCursor& c = ps.c;
@@ -202,19 +205,21 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         ps.pb = c.b;
         ps.pqb = c.qb;
       }
-      const int s = static_cast<int>(ps.i % stages);
-      const long long r = ps.i / stages;
-      if (ps.i >= stages &&
-          !mbar_wait_bounded(&bars->empty[s], static_cast<uint32_t>((r - 1) & 1), abort_flag))
-        return;
+      const int s = ps.s;
+      if (ps.r > 0 && !mbar_wait_bounded(&bars->empty[s], (ps.r - 1) & 1u, abort_flag)) return;
       mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
       // a 128-key tile never straddles a cache block (block sizes are
       // multiples of 128); an entry outside the pool reads block 0 (the
       // attention reports it when it gathers from that block)
       bool bad = false;
-      const int row = static_cast<int>(cache_row(p.pg, c.b, p.cap, c.kt * kKeyTile, &bad));
+      const int row = !paged ? c.b * p.cap + c.kt * kKeyTile
+                             : static_cast<int>(cache_row(p.pg, c.b, p.cap, c.kt * kKeyTile, &bad));
       tma_load_2d(sA + s * kATileBytes, &tm_kI, &bars->full[s], 0, row);
       ++ps.issued;
+      if (++ps.s == stages) {
+        ps.s = 0;
+        ++ps.r;
+      }
       advance_unit(p, c);
     }
   };
@@ -254,6 +259,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       constexpr uint32_t idesc = idesc_bf16_f32(kKeyTile, N);
       UnitCursor c = locate_unit(p, u0);
       int pb = -1, pqb = -1, nblk = 0, bi = 0;
+      int s = 0;           // stage of tile i, running
+      uint32_t round = 0;  // i / stages, running
       for (long long i = 0; i < count; ++i) {
         if (c.b != pb || c.qb != pqb) {
           if (nblk > 0) tc_commit(&bars->bempty[bi]);
@@ -263,9 +270,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           pb = c.b;
           pqb = c.qb;
         }
-        const int s = static_cast<int>(i % stages);
-        if (!mbar_wait_bounded(&bars->full[s], static_cast<uint32_t>((i / stages) & 1), abort_flag))
-          break;
+        if (!mbar_wait_bounded(&bars->full[s], round & 1u, abort_flag)) break;
         const int a = static_cast<int>(i % C::NACC);
         if (i >= C::NACC &&
             !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag))
@@ -281,6 +286,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         tc_commit(&bars->empty[s]);
         tc_commit(&bars->accfull[a]);
         advance_unit(p, c);
+        if (++s == stages) {
+          s = 0;
+          ++round;
+        }
       }
       // every MMA this CTA issued must finish before tensor memory is freed
       tc_commit(&bars->done);

@@ -125,7 +125,7 @@ __device__ __forceinline__ PfItem pf_item(const AttnParams& p, long long it) {
 
 // tm_k / tm_v view the caches as [B * cap * Hkv rows, 128] 16-bit matrices
 // (row (b * cap + key) * Hkv + g), box 64 x 1, 128-byte swizzle.
-template <bool F16>
+template <bool F16, bool PAGED>
 __global__ void __launch_bounds__(pf::kThreads, 2)
     sparse_attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                   const __grid_constant__ CUtensorMap tm_v, const AttnParams p,
@@ -194,7 +194,12 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           const int j = t * kKeys + 4 * grp + e;
           int key = j < w.keff ? __ldg(idx_row + j) : 0;
           if (key < 0 || key >= T) key = 0;
-          y[e] = static_cast<int>(cache_row(p.pg, b, p.cap, key, &bad_page) * p.Hkv + w.g);
+          // dense rows in 32-bit arithmetic: the loaders' issue rate bounds
+          // this kernel, so the paged lookup is a separate instantiation
+          if constexpr (PAGED)
+            y[e] = static_cast<int>(cache_row(p.pg, b, p.cap, key, &bad_page) * p.Hkv + w.g);
+          else
+            y[e] = (b * p.cap + key) * p.Hkv + w.g;
         }
       };
       for (int pass = 0; pass < 2 && ok; ++pass) {            // K tiles, then V tiles
@@ -457,28 +462,29 @@ bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin) 
          rows < (1LL << 31) && pf::kSmemBytes <= smem_optin;
 }
 
+template <bool F16, bool PAGED>
+static cudaError_t launch_prefill_variant(const AttnParams& p, int grid, const CUtensorMap& tm_k,
+                                          const CUtensorMap& tm_v, long long n_items,
+                                          uint32_t* status, cudaStream_t stream) {
+  auto k = sparse_attn_prefill_tc_kernel<F16, PAGED>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(pf::kSmemBytes));
+  if (e != cudaSuccess) return e;
+  return launch_kernel("sparse_attn_prefill_tc_kernel", k, dim3(grid), dim3(pf::kThreads),
+                       pf::kSmemBytes, stream, true, tm_k, tm_v, p, n_items, status);
+}
+
 cudaError_t launch_prefill_tc(const AttnParams& p, int kv_dtype, int sms, const CUtensorMap& tm_k,
                               const CUtensorMap& tm_v, uint32_t* status, cudaStream_t stream) {
   const long long n_items = static_cast<long long>(p.B) * p.S * p.Hkv * p.HG;
   // two CTAs per SM: one gathers while the other computes
   const int grid = static_cast<int>(n_items < 2 * sms ? n_items : 2 * sms);
-  if (kv_dtype == DSA_FP16) {
-    auto k = sparse_attn_prefill_tc_kernel<true>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(pf::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    return launch_kernel("sparse_attn_prefill_tc_kernel", k, dim3(grid), dim3(pf::kThreads),
-                         pf::kSmemBytes, stream, true, tm_k, tm_v, p,
-                         n_items, status);
-  } else {
-    auto k = sparse_attn_prefill_tc_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(pf::kSmemBytes));
-    if (e != cudaSuccess) return e;
-    return launch_kernel("sparse_attn_prefill_tc_kernel", k, dim3(grid), dim3(pf::kThreads),
-                         pf::kSmemBytes, stream, true, tm_k, tm_v, p,
-                         n_items, status);
-  }
+  const bool paged = p.pg.table != nullptr;
+  if (kv_dtype == DSA_FP16)
+    return paged ? launch_prefill_variant<true, true>(p, grid, tm_k, tm_v, n_items, status, stream)
+                 : launch_prefill_variant<true, false>(p, grid, tm_k, tm_v, n_items, status, stream);
+  return paged ? launch_prefill_variant<false, true>(p, grid, tm_k, tm_v, n_items, status, stream)
+               : launch_prefill_variant<false, false>(p, grid, tm_k, tm_v, n_items, status, stream);
 }
 
 }  // namespace dsa

@@ -49,6 +49,14 @@ R12 paged caches (PR #33802's page, the companion 256K change: a pool of
     block_size-token blocks and a per-sequence block table): token t of
     sequence b is pool row table[b, t // block_size] * block_size
     + t % block_size; every result is the dense one on the gathered caches.
+R13 RMSNorm + rotary embedding (PR #33997 Description item 1, the exact FP32
+    RMSNormRotary): each head vector x (head_dim D) of a token at position p
+    becomes y = x * gamma / sqrt(mean(x^2) + eps), then its first r dims are
+    rotated in pairs (i, i + r/2), i < r/2, by the cache's angle for p:
+    out_i = y_i cos[p,i] - y_{i+r/2} sin[p,i],
+    out_{i+r/2} = y_{i+r/2} cos[p,i] + y_i sin[p,i]; dims r..D-1 stay y.
+    Computed here exactly (float64); the library computes in fp32 and rounds
+    once to the output type.
 
 Parity pins for every function live in tests/test_oracle_pins.py.
 """
@@ -277,4 +285,29 @@ def gather_pages(pool, table, block_size: int, total_len):
     for b in range(B):
         for t in range(int(total_len[b])):
             out[b, t] = pool[table[b, t // block_size] * block_size + t % block_size]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm + rotary embedding (R13)
+# ---------------------------------------------------------------------------
+def rmsnorm_rotary(x, gamma, eps: float, cos, sin, positions, rotary_dim: int):
+    """x [N, H, D] (exact values of the stored input), gamma [D], cos / sin
+    [max_pos, rotary_dim / 2], positions [N]. Returns float64 [N, H, D]:
+    per head vector, RMS normalisation with weight gamma, then the rotate-half
+    rotation of the first rotary_dim dims by the token's cached angle."""
+    x = np.asarray(x, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    y = x / np.sqrt(ms + eps) * gamma
+    out = y.copy()
+    h = rotary_dim // 2
+    if h == 0:
+        return out
+    pos = np.asarray(positions, dtype=np.int64)
+    c = np.asarray(cos, dtype=np.float64)[pos][:, None, :]     # [N, 1, h]
+    s = np.asarray(sin, dtype=np.float64)[pos][:, None, :]
+    a, b = y[..., :h], y[..., h:rotary_dim]
+    out[..., :h] = a * c - b * s
+    out[..., h:rotary_dim] = b * c + a * s
     return out

@@ -429,6 +429,62 @@ def test_gather_pages_hand_case():
 
 
 # ---------------------------------------------------------------------------
+# RMSNorm + rotary embedding (R13)
+# ---------------------------------------------------------------------------
+def check_rope_fixture(mod):
+    for c in _load("rmsnorm_rotary_tiny.json")["cases"]:
+        out = mod.rmsnorm_rotary(np.array([c["x"]], dtype=np.float64), c["gamma"], c["eps"],
+                                 np.array(c["cos"]), np.array(c["sin"]), [c["position"]],
+                                 c["rotary_dim"])
+        assert np.allclose(out[0], np.array(c["out"]), rtol=0, atol=1e-12), (c, out)
+
+
+def check_rope_complex(mod):
+    """The rotation as a complex product: (y_i + i y_{i+h}) * exp(i theta_{p,i}),
+    with y from the vector norm (||x|| / sqrt(D)) instead of the mean square."""
+    rng = np.random.default_rng(5)
+    N, H, D, r = 6, 3, 16, 12
+    x = rng.standard_normal((N, H, D))
+    gamma = rng.uniform(0.5, 1.5, D)
+    theta = rng.uniform(-np.pi, np.pi, (9, r // 2))
+    pos = rng.integers(0, 9, N)
+    eps = 1e-3
+    out = mod.rmsnorm_rotary(x, gamma, eps, np.cos(theta), np.sin(theta), pos, r)
+    rms = np.sqrt(np.linalg.norm(x, axis=-1, keepdims=True) ** 2 / D + eps)
+    y = gamma * x / rms
+    h = r // 2
+    z = (y[..., :h] + 1j * y[..., h:r]) * np.exp(1j * theta[pos])[:, None, :]
+    assert np.allclose(out[..., :h], z.real, atol=1e-12)
+    assert np.allclose(out[..., h:r], z.imag, atol=1e-12)
+    assert np.allclose(out[..., r:], y[..., r:], atol=1e-12)
+
+
+def check_rope_scale_invariance(mod):
+    """With eps = 0 the output does not depend on the input's scale, and at an
+    angle of zero it is x * gamma / rms(x)."""
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((4, 2, 8))
+    g = rng.uniform(0.5, 2.0, 8)
+    ones, zeros = np.ones((3, 4)), np.zeros((3, 4))
+    a = mod.rmsnorm_rotary(x, g, 0.0, ones, zeros, [0, 1, 2, 0], 8)
+    b = mod.rmsnorm_rotary(37.5 * x, g, 0.0, ones, zeros, [0, 1, 2, 0], 8)
+    assert np.allclose(a, b, atol=1e-12)
+    assert np.allclose(a, x * g / np.sqrt(np.mean(x * x, axis=-1, keepdims=True)), atol=1e-12)
+
+
+def test_rope_golden_fixture():
+    check_rope_fixture(O)
+
+
+def test_rope_complex_rotation():
+    check_rope_complex(O)
+
+
+def test_rope_scale_invariance():
+    check_rope_scale_invariance(O)
+
+
+# ---------------------------------------------------------------------------
 # mutation tests: plant a mistake in a copy of the oracle, a pin must fail
 # ---------------------------------------------------------------------------
 class _Mutant:
@@ -568,3 +624,41 @@ def test_mutant_page_index_swapped_is_caught():
                 out[b, t] = pool[table[b, t % per_seq] * block_size + t // per_seq]
         return out
     assert _fails(check_gather_pages, _Mutant(gather_pages=bad))
+
+
+def _rope_variant(pairs="half", sin_sign=1.0, eps_outside=False, norm_all_heads=False):
+    def f(x, gamma, eps, cos, sin, positions, rotary_dim):
+        x = np.asarray(x, dtype=np.float64)
+        axis = (-2, -1) if norm_all_heads else -1
+        ms = np.mean(x * x, axis=axis, keepdims=True)
+        y = x / (np.sqrt(ms) + eps if eps_outside else np.sqrt(ms + eps)) * np.asarray(gamma)
+        out = y.copy()
+        h = rotary_dim // 2
+        pos = np.asarray(positions)
+        c = np.asarray(cos)[pos][:, None, :]
+        s = sin_sign * np.asarray(sin)[pos][:, None, :]
+        if pairs == "half":
+            ia, ib = np.arange(h), np.arange(h) + h
+        else:
+            ia, ib = 2 * np.arange(h), 2 * np.arange(h) + 1
+        a, b = y[..., ia], y[..., ib]
+        out[..., ia] = a * c - b * s
+        out[..., ib] = b * c + a * s
+        return out
+    return f
+
+
+def test_mutant_rope_interleaved_pairs_is_caught():
+    assert _fails(check_rope_fixture, _Mutant(rmsnorm_rotary=_rope_variant(pairs="interleaved")))
+
+
+def test_mutant_rope_sin_sign_is_caught():
+    assert _fails(check_rope_fixture, _Mutant(rmsnorm_rotary=_rope_variant(sin_sign=-1.0)))
+
+
+def test_mutant_rope_eps_outside_sqrt_is_caught():
+    assert _fails(check_rope_complex, _Mutant(rmsnorm_rotary=_rope_variant(eps_outside=True)))
+
+
+def test_mutant_rope_norm_over_all_heads_is_caught():
+    assert _fails(check_rope_complex, _Mutant(rmsnorm_rotary=_rope_variant(norm_all_heads=True)))

@@ -3,7 +3,7 @@ sparse attention step (indexer -> radix top-k -> sparse GQA attention) at a
 131,072-token context with top_k = 2,048, on synthetic data.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libdsa|reference]
-                    [--workload NAME] [--no-graph] [--op step|append [--q-len S]]
+                    [--workload NAME] [--no-graph] [--op step|append|rope [--q-len S]]
 
 One JSON line on stdout (rank 0). A step is one call of the whole decode path
 (dsa_sparse_attn_decode) over one batch of query tokens with inputs resident
@@ -16,7 +16,8 @@ replica of the workload (the path shards by sequence with no exchange:
 weak scaling); the slowest rank's time is reported.
 
 --op append times dsa_cache_append alone (the cache write before the step) on
-the workload's shape and reports its HBM GB/s.
+the workload's shape and reports its HBM GB/s; --op rope does the same for
+dsa_rmsnorm_rotary on the workload's query and key heads.
 
 --impl reference times the float64 CPU oracle on the same workload (rank 0
 only) -- a deliberately slow baseline, not the optimisation target.
@@ -632,6 +633,88 @@ def run_append_bench(args, wl):
         "clocks": clk}), flush=True)
 
 
+def run_rope_bench(args, wl):
+    """--op rope: dsa_rmsnorm_rotary alone on the query and key heads of the
+    workload's new tokens (--q-len tokens, default the workload's; head dim
+    128, full rotary width, FP32 cos / sin cache), timed per call."""
+    import torch
+
+    from dsa_inputs import make_rope_inputs
+    from top_sparse_attention_chunked_gb300 import build_lib
+    from top_sparse_attention_chunked_gb300 import dsa as D
+
+    build_lib.build()
+    D.load_library()
+    N = args.q_len or wl.q_len
+    H = wl.num_q_heads + wl.num_kv_heads
+    r = 128
+    max_pos = wl.total_len
+    inp = make_rope_inputs(N, H, 128, r, max_pos, wl.q_dtype, "fp32", seed=wl.seed,
+                           first_pos=max(0, wl.total_len - N))
+    x = inp["x"].cuda()
+    y = torch.empty_like(x)
+    g, c, sn, pos = (inp[k].cuda() for k in ("gamma", "cos", "sin", "positions"))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        D.dsa_rmsnorm_rotary(x, g, y, eps=1e-6, cos_cache=c, sin_cache=sn, positions=pos,
+                             rotary_dim=r)
+
+    if args.profile_calls:
+        for _ in range(args.profile_calls):
+            step()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_calls": args.profile_calls, "op": "rope",
+                          "kernels_per_step": D.dsa_last_launches()}), flush=True)
+        return
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    kernels = D.dsa_last_launches()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        graph.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # every x element read and every y element written once, plus each
+    # token's cos / sin row
+    nbytes = N * H * 128 * 2 * 2 + N * (r // 2) * 4 * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm, _, peak_kind = peaks()
+    print(json.dumps({
+        "metric": "RMSNorm + rotary embedding achieved HBM GB/s", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 arithmetic, bf16 in/out",
+        "data": "synthetic (seeded, see dsa_inputs.make_rope_inputs)",
+        "config": {"workload": f"RMSNorm + RoPE of {N} tokens x {H} heads x 128 "
+                               f"(query and key heads of {wl.name})",
+                   "l2": "flushed (256 MiB write) before every step", "graph": True},
+        "roofline": {"kernel": "rmsnorm_rotary_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes": nbytes},
+        "gpu_launches": len(kernels) * args.steps, "kernels_per_step": kernels,
+        "clocks": clk}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -645,8 +728,9 @@ def main():
                     help="run this many untimed calls and exit (for ncu captures)")
     ap.add_argument("--paged", type=int, default=0,
                     help="run the step on a paged cache with blocks of this many tokens")
-    ap.add_argument("--op", default="step", choices=["step", "append"],
-                    help="append: time dsa_cache_append alone on the workload's shape")
+    ap.add_argument("--op", default="step", choices=["step", "append", "rope"],
+                    help="append: time dsa_cache_append alone on the workload's shape; "
+                         "rope: time dsa_rmsnorm_rotary on its query and key heads")
     ap.add_argument("--q-len", type=int, default=0,
                     help="with --profile-calls: query tokens per sequence of a reduced case; "
                          "with --op append: new tokens per sequence")
@@ -659,6 +743,9 @@ def main():
     wl = WORKLOADS[args.workload]
     if args.op == "append":
         run_append_bench(args, wl)
+        return
+    if args.op == "rope":
+        run_rope_bench(args, wl)
         return
     if args.profile_calls and (args.q_len or args.context):
         # a reduced case of the same structure (heads, top_k, dtypes)

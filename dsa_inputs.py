@@ -182,6 +182,30 @@ def make_append_inputs(batch: int, q_len: int, num_kv_heads: int, capacity: int,
     return out
 
 
+def make_rope_inputs(tokens: int, heads: int, head_dim: int, rotary_dim: int, max_pos: int,
+                     x_dtype: str, cos_dtype: str, seed: int = 0, first_pos: int = 0,
+                     base: float = 1.0e6) -> Dict[str, torch.Tensor]:
+    """CPU tensors for RMSNorm + rotary embedding: x [N, H, D] ~ N(0,1) times
+    a per-vector magnitude 10^U(-2,2), gamma [D] ~ U(0.5, 1.5), the standard
+    rotary angle table theta[p, i] = p * base^(-2i / rotary_dim) as cos / sin
+    caches [max_pos, rotary_dim / 2] (computed in float64, stored in
+    cos_dtype), and consecutive positions first_pos .. first_pos + N - 1."""
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(tokens, heads, head_dim, generator=g, dtype=torch.float64)
+    x = x * 10.0 ** (torch.rand(tokens, heads, 1, generator=g, dtype=torch.float64) * 4 - 2)
+    gamma = (torch.rand(head_dim, generator=g) + 0.5).float()
+    h = rotary_dim // 2
+    out = {"x": x.to(DTYPES[x_dtype]).contiguous(), "gamma": gamma,
+           "positions": torch.arange(first_pos, first_pos + tokens, dtype=torch.int32),
+           "cos": None, "sin": None}
+    if h > 0:
+        inv = base ** (-2.0 * torch.arange(h, dtype=torch.float64) / rotary_dim)
+        theta = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv[None, :]
+        out["cos"] = torch.cos(theta).to(DTYPES[cos_dtype]).contiguous()
+        out["sin"] = torch.sin(theta).to(DTYPES[cos_dtype]).contiguous()
+    return out
+
+
 def small_workload(name="small", batch=2, q_len=3, total_len=1000, num_q_heads=8,
                    num_kv_heads=2, top_k=64, q_dtype="bf16", kv_dtype="bf16",
                    capacity=None, bias_frac=0.0, seed=7) -> Workload:

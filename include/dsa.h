@@ -233,6 +233,55 @@ int dsa_cache_append(const dsa_problem* p, const void* kI_new, const void* k_new
                      float* v_scale, void* stream);
 
 /*
+ * dsa_rmsnorm_rotary -- RMSNorm + rotary position embedding in fp32, the step
+ * that produces q, k, qI and kI before the cache append and the attention.
+ * PR #33997 Description item 1 (RMSNormRotary computed in exact FP32 with no
+ * intermediate BF16 rounding, from a BF16 or FP32 cos/sin cache, to a BF16 or
+ * FP16 output). For every head vector x (head_dim D) of token n:
+ *     y = x * gamma / sqrt(mean(x^2) + eps)
+ *     out_i       = y_i * cos[p, i] - y_{i+r/2} * sin[p, i]    (i < r/2)
+ *     out_{i+r/2} = y_{i+r/2} * cos[p, i] + y_i * sin[p, i]
+ *     out_i       = y_i                                        (i >= r)
+ * with p = positions[n] (clamped to 0 .. max_pos - 1) and r = rotary_dim,
+ * every step in fp32 and one round-to-nearest-even conversion at the end.
+ * Vectors whose absmax lies outside [2^-60, 2^60] are rescaled by an exact
+ * power of two first, so the fp32 sum of squares cannot overflow or vanish.
+ * With eps = 0 an all-zero vector gives NaN, as the formula does.
+ *
+ *   tokens      N >= 0 (0: nothing is launched)
+ *   heads       H >= 1
+ *   head_dim    D: 64 or 128
+ *   rotary_dim  r: even, 0 .. D (0: RMSNorm only)
+ *   max_pos     rows of the cos / sin caches (>= 1 when r > 0)
+ *   eps         finite, >= 0
+ *   x_dtype, y_dtype   DSA_BF16 or DSA_FP16
+ *   cos_dtype   DSA_FP32 or DSA_BF16
+ *
+ *   x           [N, H, D] x_dtype, 16-byte aligned
+ *   gamma       [D] fp32 channel weights
+ *   cos_cache, sin_cache  [max_pos, r/2] cos_dtype (NULL allowed when r = 0)
+ *   positions   [N] int32 (NULL allowed when r = 0)
+ *   y           [N, H, D] y_dtype, 16-byte aligned; may be x itself (in
+ *               place), must not overlap it otherwise
+ * All DEVICE pointers owned by the caller; no workspace; one kernel.
+ */
+typedef struct dsa_rope_problem {
+  int64_t tokens;
+  int32_t heads;
+  int32_t head_dim;
+  int32_t rotary_dim;
+  int32_t max_pos;
+  float eps;
+  int32_t x_dtype;
+  int32_t cos_dtype;
+  int32_t y_dtype;
+} dsa_rope_problem;
+
+int dsa_rmsnorm_rotary(const dsa_rope_problem* rp, const void* x, const float* gamma,
+                       const void* cos_cache, const void* sin_cache, const int32_t* positions,
+                       void* y, void* stream);
+
+/*
  * dsa_topk_noalloc -- dsa_topk for callers that cannot give the library any
  * device memory. Some callers cannot allocate: an operator plugin whose host
  * framework hands it only its input and output tensors, a serving engine that
@@ -350,8 +399,8 @@ int dsa_version(void);
 
 /*
  * dsa_last_launches -- the kernels that the last dsa_index_scores, dsa_topk,
- * dsa_topk_noalloc, dsa_cache_append, dsa_sparse_attn_decode or
- * dsa_sparse_attn_prefill call on
+ * dsa_topk_noalloc, dsa_cache_append, dsa_rmsnorm_rotary, dsa_sparse_attn_decode or
+ * dsa_sparse_attn_prefill call (or its _paged form) on
  * this host thread enqueued. Returns how many (0 after a call that failed
  * before launching); when buf is not NULL, writes their names in launch order,
  * comma-separated and NUL-terminated, truncated to fit buflen bytes. No

@@ -660,6 +660,9 @@ int attn_entry(const dsa_problem* p, int op, const dsa_kv_pages* pages, const vo
 // ------------------------------------------------------------------ no-alloc top-k helpers
 int noalloc_fail(int status, const char* msg) { return fail(status, "%s", msg); }
 
+// Records a failure of a call implemented in another translation unit.
+int report_error(int status, const char* msg) { return fail(status, "%s", msg); }
+
 int noalloc_check_topk(const dsa_problem* p, int* rows, int* max_n) {
   reset_launches();
   Derived d;

@@ -34,7 +34,7 @@ EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc",
             "dsa_last_launches", "dsa_cache_append", "dsa_index_scores_paged",
             "dsa_sparse_attn_decode_paged", "dsa_sparse_attn_prefill_paged",
-            "dsa_cache_append_paged"]
+            "dsa_cache_append_paged", "dsa_rmsnorm_rotary"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -48,6 +48,21 @@ class DsaKvPages(ctypes.Structure):
         ("num_blocks", ctypes.c_int32),
         ("blocks_per_seq", ctypes.c_int32),
         ("block_table", ctypes.c_void_p),
+    ]
+
+
+class DsaRopeProblem(ctypes.Structure):
+    """dsa_rope_problem (RMSNorm + rotary embedding)."""
+    _fields_ = [
+        ("tokens", ctypes.c_int64),
+        ("heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("rotary_dim", ctypes.c_int32),
+        ("max_pos", ctypes.c_int32),
+        ("eps", ctypes.c_float),
+        ("x_dtype", ctypes.c_int32),
+        ("cos_dtype", ctypes.c_int32),
+        ("y_dtype", ctypes.c_int32),
     ]
 
 
@@ -112,6 +127,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_sparse_attn_decode_paged": (i32, [P, PG] + [vp] * 11 + [sz, vp]),
         "dsa_sparse_attn_prefill_paged": (i32, [P, PG] + [vp] * 11 + [sz, vp]),
         "dsa_cache_append_paged": (i32, [P, PG] + [vp] * 9),
+        "dsa_rmsnorm_rotary": (i32, [ctypes.POINTER(DsaRopeProblem)] + [vp] * 7),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -269,6 +285,30 @@ def dsa_cache_append(p: DsaProblem, kI_new, k_new, v_new, kI, k, v, k_scale=None
         _check(lib.dsa_cache_append(ctypes.byref(p), *args))
     else:
         _check(lib.dsa_cache_append_paged(ctypes.byref(p), ctypes.byref(pages), *args))
+
+
+def dsa_rmsnorm_rotary(x, gamma, y, eps=1e-6, cos_cache=None, sin_cache=None, positions=None,
+                       rotary_dim=None, stream=None):
+    """RMSNorm + rotary embedding of x [N, H, D] (BF16/FP16) into y (BF16/FP16,
+    may be x); gamma [D] fp32; cos / sin caches [max_pos, rotary_dim / 2] in
+    fp32 or bf16 with positions [N] int32 (omit all three for RMSNorm only)."""
+    lib = load_library()
+    if x.dim() != 3:
+        raise ValueError("x must be [tokens, heads, head_dim]")
+    N, H, D = x.shape
+    r = 0 if cos_cache is None else (rotary_dim if rotary_dim is not None else 2 * cos_cache.shape[1])
+    inv = {v: k for k, v in _TORCH_DT.items()}
+    rp = DsaRopeProblem(N, H, D, r, 0 if cos_cache is None else cos_cache.shape[0], eps,
+                        inv[x.dtype], inv[cos_cache.dtype] if cos_cache is not None else DSA_FP32,
+                        inv[y.dtype])
+    if cos_cache is not None and tuple(cos_cache.shape) != (cos_cache.shape[0], r // 2):
+        raise ValueError("cos_cache must be [max_pos, rotary_dim / 2]")
+    _check(lib.dsa_rmsnorm_rotary(
+        ctypes.byref(rp), _ptr(x, "x", None, (N, H, D)), _ptr(gamma, "gamma", torch.float32, (D,)),
+        _ptr(cos_cache, "cos_cache"), _ptr(sin_cache, "sin_cache", cos_cache.dtype if cos_cache is not None else None,
+                                         tuple(cos_cache.shape) if cos_cache is not None else None),
+        _ptr(positions, "positions", torch.int32, (N,)), _ptr(y, "y", None, (N, H, D)),
+        _stream(stream)))
 
 
 def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream,

@@ -715,6 +715,89 @@ def run_rope_bench(args, wl):
         "clocks": clk}), flush=True)
 
 
+def run_layer_bench(args, wl):
+    """--op layer: one decoding layer's step built from the library's calls,
+    replayed from one CUDA graph: RMSNorm + RoPE of q, qI, the new k and kI
+    (positions T - S + s), the cache append of kI, k, v, then the decode."""
+    import torch
+
+    from dsa_inputs import make_append_inputs, make_inputs, make_rope_inputs
+    from top_sparse_attention_chunked_gb300 import build_lib
+    from top_sparse_attention_chunked_gb300 import dsa as D
+
+    build_lib.build()
+    D.load_library()
+    B, S, Hq, Hkv, cap = wl.batch, wl.q_len, wl.num_q_heads, wl.num_kv_heads, wl.cap
+    cpu = make_inputs(wl)
+    app = make_append_inputs(B, S, Hkv, 1, [1] * B, wl.q_dtype, wl.kv_dtype, seed=wl.seed + 1,
+                             specials=False)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    new = {k: app[k].cuda() for k in ("kI_new", "k_new", "v_new")}
+    p = D.problem_for(wl)
+    ws = D.alloc_workspace(p, D.DSA_OP_DECODE)
+    out = torch.empty(B, S, Hq, 128, dtype=D._TORCH_DT[p.out_dtype], device="cuda")
+    idx = torch.empty(B, S, wl.top_k, dtype=torch.int32, device="cuda")
+    rope = {}
+    for name, H, Dh in (("q", Hq, 128), ("qI", 16, 64), ("k", Hkv, 128), ("kI", 1, 64)):
+        r = make_rope_inputs(B * S, H, Dh, Dh, cap, wl.q_dtype, "fp32", seed=wl.seed + H)
+        r["positions"] = torch.tensor([wl.total_len - S + s for _ in range(B) for s in range(S)],
+                                      dtype=torch.int32)
+        rope[name] = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in r.items()}
+    views = {"q": dev["q"].view(B * S, Hq, 128), "qI": dev["qI"].view(B * S, 16, 64),
+             "k": new["k_new"].view(B * S, Hkv, 128), "kI": new["kI_new"].view(B * S, 1, 64)}
+    raw = {n: views[n].clone() for n in views}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for n in ("q", "qI", "k", "kI"):
+            r = rope[n]
+            D.dsa_rmsnorm_rotary(raw[n], r["gamma"], views[n], eps=1e-6, cos_cache=r["cos"],
+                                 sin_cache=r["sin"], positions=r["positions"])
+        D.dsa_cache_append(p, new["kI_new"], new["k_new"], new["v_new"], dev["kI"], dev["k"],
+                           dev["v"], dev["k_scale"], dev["v_scale"])
+        D.dsa_sparse_attn_decode(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"],
+                                 dev["k_scale"], dev["v_scale"], idx, out, ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert D.dsa_read_device_status(ws) == 0
+    # four RMSNorm + RoPE launches, the append, then the decode's kernels
+    kernels = ["rmsnorm_rotary_kernel"] * 4 + ["cache_append_kernel"] + D.dsa_last_launches()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        graph.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    print(json.dumps({
+        "metric": "decoding layer step (RMSNorm+RoPE, cache append, sparse attention) query-tokens/s",
+        "value": wl.query_tokens / (ms * 1e-3), "unit": "query-tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic (seeded, see dsa_inputs.py)",
+        "config": dict(config_of(wl, True), op="layer"),
+        "gpu_launches": len(kernels) * args.steps, "kernels_per_step": kernels,
+        "clocks": clk}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -728,9 +811,10 @@ def main():
                     help="run this many untimed calls and exit (for ncu captures)")
     ap.add_argument("--paged", type=int, default=0,
                     help="run the step on a paged cache with blocks of this many tokens")
-    ap.add_argument("--op", default="step", choices=["step", "append", "rope"],
+    ap.add_argument("--op", default="step", choices=["step", "append", "rope", "layer"],
                     help="append: time dsa_cache_append alone on the workload's shape; "
-                         "rope: time dsa_rmsnorm_rotary on its query and key heads")
+                         "rope: time dsa_rmsnorm_rotary on its query and key heads; "
+                         "layer: RMSNorm+RoPE, append and decode as one graph")
     ap.add_argument("--q-len", type=int, default=0,
                     help="with --profile-calls: query tokens per sequence of a reduced case; "
                          "with --op append: new tokens per sequence")
@@ -746,6 +830,9 @@ def main():
         return
     if args.op == "rope":
         run_rope_bench(args, wl)
+        return
+    if args.op == "layer":
+        run_layer_bench(args, wl)
         return
     if args.profile_calls and (args.q_len or args.context):
         # a reduced case of the same structure (heads, top_k, dtypes)

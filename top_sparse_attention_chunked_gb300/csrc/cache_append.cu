@@ -154,6 +154,7 @@ constexpr int kAppRowsK = 128;                               // K/V rows per til
 constexpr int kAppSmem = kAppRowsK * DSA_HEAD_DIM * 2;        // 32 KB (no opt-in needed)
 constexpr int kAppRowsI = 2 * kAppThreads / 8;               // index-key rows per tile (64)
 
+template <bool PAGED>
 __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(const AppendParams p) {
   extern __shared__ __align__(16) uint8_t tile[];
   const int b = blockIdx.z;
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(const AppendP
     for (int i = 0; i < 2; ++i) {
       if (r[i] >= p.S) continue;
       long long row = dst0 + r[i];
-      if (p.pg.table != nullptr) {
+      if constexpr (PAGED) {
         bool bad = false;
         row = cache_row(p.pg, b, p.cap, p.lens.T[b] - p.S + static_cast<int>(r[i]), &bad);
         if (bad) continue;   // never write through an entry outside the pool
@@ -218,10 +219,12 @@ __global__ void __launch_bounds__(kAppThreads) cache_append_kernel(const AppendP
     u[1] = *reinterpret_cast<const uint4*>(row + 128 + l8 * 16);
     long long drow = drow0 + rr;
     bool bad = false;
-    if (p.pg.table != nullptr && valid) {
-      const int rs = static_cast<int>(r0) + rr;      // row within the sequence's span
-      const int tok = rs / p.Hkv;
-      drow = cache_row(p.pg, b, p.cap, p.lens.T[b] - p.S + tok, &bad) * p.Hkv + (rs - tok * p.Hkv);
+    if constexpr (PAGED) {
+      if (valid) {   // (no early exit: every lane takes part in the INT8 warp vote)
+        const int rs = static_cast<int>(r0) + rr;    // row within the sequence's span
+        const int tok = rs / p.Hkv;
+        drow = cache_row(p.pg, b, p.cap, p.lens.T[b] - p.S + tok, &bad) * p.Hkv + (rs - tok * p.Hkv);
+      }
     }
     if (p.kv_dtype == DSA_INT8) {
       float x[16];
@@ -264,9 +267,12 @@ cudaError_t launch_cache_append(const AppendParams& p, int sms, cudaStream_t str
   const long long kI_tiles = (static_cast<long long>(p.S) + kAppRowsI - 1) / kAppRowsI;
   const long long tiles = kv_tiles > kI_tiles ? kv_tiles : kI_tiles;
   if (tiles > 0x7fffffffll) return cudaErrorInvalidValue;
-  return launch_kernel("cache_append_kernel", cache_append_kernel,
-                       dim3(static_cast<unsigned>(tiles), 3, p.B), dim3(kAppThreads), kAppSmem,
-                       stream, false, p);
+  const dim3 grid(static_cast<unsigned>(tiles), 3, p.B);
+  if (p.pg.table != nullptr)
+    return launch_kernel("cache_append_kernel", cache_append_kernel<true>, grid, dim3(kAppThreads),
+                         kAppSmem, stream, false, p);
+  return launch_kernel("cache_append_kernel", cache_append_kernel<false>, grid, dim3(kAppThreads),
+                       kAppSmem, stream, false, p);
 }
 
 }  // namespace dsa

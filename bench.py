@@ -749,7 +749,7 @@ def run_layer_bench(args, wl):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step_chain():
         for n in ("q", "qI", "k", "kI"):
             r = rope[n]
             D.dsa_rmsnorm_rotary(raw[n], r["gamma"], views[n], eps=1e-6, cos_cache=r["cos"],
@@ -759,12 +759,26 @@ def run_layer_bench(args, wl):
         D.dsa_sparse_attn_decode(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"],
                                  dev["k_scale"], dev["v_scale"], idx, out, ws)
 
+    def step_fused():
+        # (q and qI are rotated in place: each replay renormalises them again)
+        D.dsa_rope_append(p, dev["q"], dev["qI"], new["k_new"], new["kI_new"], new["v_new"],
+                          dev["kI"], dev["k"], dev["v"], dev["k_scale"], dev["v_scale"],
+                          rope["q"]["gamma"], rope["k"]["gamma"], rope["qI"]["gamma"],
+                          rope["kI"]["gamma"], eps=1e-6, cos=rope["q"]["cos"], sin=rope["q"]["sin"],
+                          cos_index=rope["qI"]["cos"], sin_index=rope["qI"]["sin"])
+        D.dsa_sparse_attn_decode(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"],
+                                 dev["k_scale"], dev["v_scale"], idx, out, ws)
+
+    step = step_fused if args.fused else step_chain
+
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     assert D.dsa_read_device_status(ws) == 0
-    # four RMSNorm + RoPE launches, the append, then the decode's kernels
-    kernels = ["rmsnorm_rotary_kernel"] * 4 + ["cache_append_kernel"] + D.dsa_last_launches()
+    # four RMSNorm + RoPE launches and the append (or the one fused launch),
+    # then the decode's kernels
+    kernels = ((["rope_append_kernel"] if args.fused
+                else ["rmsnorm_rotary_kernel"] * 4 + ["cache_append_kernel"]) + D.dsa_last_launches())
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
@@ -793,7 +807,7 @@ def run_layer_bench(args, wl):
         "value": wl.query_tokens / (ms * 1e-3), "unit": "query-tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "dtype": "bf16", "data": "synthetic (seeded, see dsa_inputs.py)",
-        "config": dict(config_of(wl, True), op="layer"),
+        "config": dict(config_of(wl, True), op="layer", fused_prologue=bool(args.fused)),
         "gpu_launches": len(kernels) * args.steps, "kernels_per_step": kernels,
         "clocks": clk}), flush=True)
 
@@ -809,6 +823,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="run this many untimed calls and exit (for ncu captures)")
+    ap.add_argument("--fused", action="store_true",
+                    help="with --op layer: RMSNorm+RoPE and the append as one launch")
     ap.add_argument("--paged", type=int, default=0,
                     help="run the step on a paged cache with blocks of this many tokens")
     ap.add_argument("--op", default="step", choices=["step", "append", "rope", "layer"],

@@ -282,6 +282,51 @@ int dsa_rmsnorm_rotary(const dsa_rope_problem* rp, const void* x, const float* g
                        void* y, void* stream);
 
 /*
+ * dsa_rope_append -- the work before the indexer in one launch: RMSNorm +
+ * rotary embedding of the step's new q and qI (in place), of k_new and
+ * kI_new, and the cache append of the rotated kI and k and of v_new. Equal,
+ * bit for bit, to dsa_rmsnorm_rotary on q (q dtype), qI (BF16), k_new (into
+ * the q dtype) and kI_new (into BF16), all at positions total_len[b] - q_len
+ * + s, followed by dsa_cache_append. PR #33997 Description item 1 and its
+ * Files changed table (the cache writes beside the attention kernels).
+ * Dense caches only.
+ *
+ *   q        [B, S, Hq, 128] q_dtype, rotated in place
+ *   qI       [B, S, 16, 64] bf16, rotated in place
+ *   k_new, v_new  [B, S, Hkv, 128] q_dtype (not modified)
+ *   kI_new   [B, S, 64] bf16 (not modified)
+ *   kI, k, v, k_scale, v_scale  the caches, as for dsa_cache_append
+ * All 16-byte aligned DEVICE pointers; the new-token tensors must not overlap
+ * a cache. The rope parameters:
+ *   eps          finite, >= 0 (all four tensors)
+ *   max_pos      rows of the cos / sin caches (>= 1 if any rotary width > 0)
+ *   cos_dtype    DSA_FP32 or DSA_BF16 (both caches)
+ *   rotary_dim, cos, sin              q and k: even width <= 128, caches
+ *                                     [max_pos, rotary_dim / 2]
+ *   rotary_dim_index, cos_index, sin_index   qI and kI: even width <= 64
+ *   gamma_q, gamma_k [128], gamma_qI, gamma_kI [64]   fp32 channel weights
+ */
+typedef struct dsa_rope_params {
+  float eps;
+  int32_t max_pos;
+  int32_t cos_dtype;
+  int32_t rotary_dim;
+  int32_t rotary_dim_index;
+  const void* cos;
+  const void* sin;
+  const void* cos_index;
+  const void* sin_index;
+  const float* gamma_q;
+  const float* gamma_k;
+  const float* gamma_qI;
+  const float* gamma_kI;
+} dsa_rope_params;
+
+int dsa_rope_append(const dsa_problem* p, const dsa_rope_params* rope, void* q, void* qI,
+                    const void* k_new, const void* kI_new, const void* v_new, void* kI, void* k,
+                    void* v, float* k_scale, float* v_scale, void* stream);
+
+/*
  * dsa_topk_noalloc -- dsa_topk for callers that cannot give the library any
  * device memory. Some callers cannot allocate: an operator plugin whose host
  * framework hands it only its input and output tensors, a serving engine that
@@ -399,7 +444,8 @@ int dsa_version(void);
 
 /*
  * dsa_last_launches -- the kernels that the last dsa_index_scores, dsa_topk,
- * dsa_topk_noalloc, dsa_cache_append, dsa_rmsnorm_rotary, dsa_sparse_attn_decode or
+ * dsa_topk_noalloc, dsa_cache_append, dsa_rmsnorm_rotary, dsa_rope_append,
+ * dsa_sparse_attn_decode or
  * dsa_sparse_attn_prefill call (or its _paged form) on
  * this host thread enqueued. Returns how many (0 after a call that failed
  * before launching); when buf is not NULL, writes their names in launch order,

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdsa.so")
 SOURCES = ["dsa_api.cu", "indexer.cu", "topk.cu", "attention.cu", "prefill_attn.cu",
-           "topk_noalloc.cu", "cache_append.cu", "rmsnorm_rotary.cu"]
+           "topk_noalloc.cu", "cache_append.cu", "rmsnorm_rotary.cu",
+           "rope_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -663,6 +663,12 @@ int noalloc_fail(int status, const char* msg) { return fail(status, "%s", msg); 
 // Records a failure of a call implemented in another translation unit.
 int report_error(int status, const char* msg) { return fail(status, "%s", msg); }
 
+// Problem validation for calls that write caches (any q_len, as for prefill).
+int problem_check_for_append(const dsa_problem* p) {
+  Derived d;
+  return check_problem(p, DSA_OP_PREFILL, &d);
+}
+
 int noalloc_check_topk(const dsa_problem* p, int* rows, int* max_n) {
   reset_launches();
   Derived d;

@@ -14,12 +14,10 @@
 //   out_i       = y_i                                   (i >= r)
 //
 // One warp per token and group of up to four heads (D/32 elements a lane);
-// the token's cos / sin values are loaded once per group. The sum of squares
-// is a shuffle butterfly in fp32; 1/sqrt uses the IEEE square root and
-// division. When that sum leaves [2^-100, 2^100], the vector is first scaled
-// by 2^-+64 (exact, chosen from its absmax) so that the fp32 sum of squares
-// neither overflows nor underflows; the scale cancels in y (eps is scaled by
-// the square of it). The normalised
+// the token's cos / sin values are loaded once per group. The per-vector
+// arithmetic (rope_math.cuh) is a shuffle-butterfly sum of squares in fp32,
+// the IEEE square root and division, and an exact 2^-+64 rescale when that
+// sum leaves [2^-100, 2^100], all in explicit round-to-nearest operations. The normalised
 // vector is staged in shared memory so that each lane can read its rotation
 // partner for any even rotary width.
 #include <cuda_bf16.h>
@@ -29,6 +27,7 @@
 #include <cstdio>
 
 #include "dsa_internal.h"
+#include "rope_math.cuh"
 
 namespace dsa {
 
@@ -169,43 +168,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
       const long long base = base0 + static_cast<long long>(hh) * D;
       float x[E];
       to_floats<E>(raw[hh], xf16, x);
-      float ss = 0.0f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      float eps = p.eps;
-      if (!(ss >= 0x1p-100f && ss <= 0x1p100f)) {
-        // out of the comfortable range (or zero): rescale by an exact power
-        // of two chosen from the absmax so that the fp32 sum of squares
-        // neither overflows nor underflows; the scale cancels in y (eps takes
-        // its square, in two steps: 2^128 is not an fp32 value)
-        float amax = 0.0f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        float sc = 1.0f;
-        if (amax > 0x1p60f) {
-          sc = 0x1p-64f;
-          eps = p.eps * 0x1p-64f * 0x1p-64f;
-        } else if (amax > 0.0f && amax < 0x1p-60f) {
-          sc = 0x1p64f;
-          eps = p.eps * 0x1p64f * 0x1p64f;
-        }
-        ss = 0.0f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          x[e] *= sc;
-          ss = fmaf(x[e], x[e], ss);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      }
-      const float inv = 1.0f / sqrtf(ss * (1.0f / D) + eps);
       float y[E];
-#pragma unroll
-      for (int e = 0; e < E; ++e) y[e] = x[e] * inv * g[e];
+      rms_normalize<E, D>(x, g, p.eps, y);
       if (h > 0) {
 #pragma unroll
         for (int e = 0; e < E; ++e) s_y[warp][i0 + e] = y[e];
@@ -218,7 +182,7 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
         float v = y[e];
         if (i < p.rotary_dim) {
           const float partner = s_y[warp][i < h ? i + h : i - h];
-          v = i < h ? v * c[e] - partner * sn[e] : v * c[e] + partner * sn[e];
+          v = rope_rotate(v, partner, c[e], sn[e], i < h);
         }
         o[e] = to_out(v, yf16);
       }

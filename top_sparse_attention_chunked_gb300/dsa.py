@@ -34,7 +34,7 @@ EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc",
             "dsa_last_launches", "dsa_cache_append", "dsa_index_scores_paged",
             "dsa_sparse_attn_decode_paged", "dsa_sparse_attn_prefill_paged",
-            "dsa_cache_append_paged", "dsa_rmsnorm_rotary"]
+            "dsa_cache_append_paged", "dsa_rmsnorm_rotary", "dsa_rope_append"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -63,6 +63,25 @@ class DsaRopeProblem(ctypes.Structure):
         ("x_dtype", ctypes.c_int32),
         ("cos_dtype", ctypes.c_int32),
         ("y_dtype", ctypes.c_int32),
+    ]
+
+
+class DsaRopeParams(ctypes.Structure):
+    """dsa_rope_params (the rope half of dsa_rope_append)."""
+    _fields_ = [
+        ("eps", ctypes.c_float),
+        ("max_pos", ctypes.c_int32),
+        ("cos_dtype", ctypes.c_int32),
+        ("rotary_dim", ctypes.c_int32),
+        ("rotary_dim_index", ctypes.c_int32),
+        ("cos", ctypes.c_void_p),
+        ("sin", ctypes.c_void_p),
+        ("cos_index", ctypes.c_void_p),
+        ("sin_index", ctypes.c_void_p),
+        ("gamma_q", ctypes.c_void_p),
+        ("gamma_k", ctypes.c_void_p),
+        ("gamma_qI", ctypes.c_void_p),
+        ("gamma_kI", ctypes.c_void_p),
     ]
 
 
@@ -128,6 +147,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_sparse_attn_prefill_paged": (i32, [P, PG] + [vp] * 11 + [sz, vp]),
         "dsa_cache_append_paged": (i32, [P, PG] + [vp] * 9),
         "dsa_rmsnorm_rotary": (i32, [ctypes.POINTER(DsaRopeProblem)] + [vp] * 7),
+        "dsa_rope_append": (i32, [P, ctypes.POINTER(DsaRopeParams)] + [vp] * 11),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -309,6 +329,37 @@ def dsa_rmsnorm_rotary(x, gamma, y, eps=1e-6, cos_cache=None, sin_cache=None, po
                                          tuple(cos_cache.shape) if cos_cache is not None else None),
         _ptr(positions, "positions", torch.int32, (N,)), _ptr(y, "y", None, (N, H, D)),
         _stream(stream)))
+
+
+def dsa_rope_append(p: DsaProblem, q, qI, k_new, kI_new, v_new, kI, k, v, k_scale, v_scale,
+                    gamma_q, gamma_k, gamma_qI, gamma_kI, eps=1e-6, cos=None, sin=None,
+                    cos_index=None, sin_index=None, stream=None):
+    """RMSNorm + RoPE of q, qI (in place), k_new, kI_new and the cache append
+    of kI, k, v in one launch (positions total_len[b] - q_len + s)."""
+    B, S, Hq, Hkv, cap = p.batch, p.q_len, p.num_q_heads, p.num_kv_heads, p.cache_capacity
+    lib = load_library()
+    qdt, kvdt = _TORCH_DT[p.q_dtype], _TORCH_DT[p.kv_dtype]
+    caches = [c for c in (cos, cos_index) if c is not None]
+    cdt = {torch.float32: DSA_FP32, torch.bfloat16: DSA_BF16}[caches[0].dtype] if caches else DSA_FP32
+    rp = DsaRopeParams(eps, caches[0].shape[0] if caches else 0, cdt,
+                       0 if cos is None else 2 * cos.shape[1],
+                       0 if cos_index is None else 2 * cos_index.shape[1],
+                       None if cos is None else cos.data_ptr(), None if sin is None else sin.data_ptr(),
+                       None if cos_index is None else cos_index.data_ptr(),
+                       None if sin_index is None else sin_index.data_ptr(),
+                       _ptr(gamma_q, "gamma_q", torch.float32, (128,)).value,
+                       _ptr(gamma_k, "gamma_k", torch.float32, (128,)).value,
+                       _ptr(gamma_qI, "gamma_qI", torch.float32, (64,)).value,
+                       _ptr(gamma_kI, "gamma_kI", torch.float32, (64,)).value)
+    for t, n in ((cos, "cos"), (sin, "sin"), (cos_index, "cos_index"), (sin_index, "sin_index")):
+        _ptr(t, n)
+    _check(lib.dsa_rope_append(
+        ctypes.byref(p), ctypes.byref(rp), _ptr(q, "q", qdt, (B, S, Hq, 128)),
+        _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)), _ptr(k_new, "k_new", qdt, (B, S, Hkv, 128)),
+        _ptr(kI_new, "kI_new", torch.bfloat16, (B, S, 64)), _ptr(v_new, "v_new", qdt, (B, S, Hkv, 128)),
+        _ptr(kI, "kI", torch.bfloat16, (B, cap, 64)), _ptr(k, "k", kvdt, (B, cap, Hkv, 128)),
+        _ptr(v, "v", kvdt, (B, cap, Hkv, 128)), _ptr(k_scale, "k_scale", torch.float32, (B, cap, Hkv)),
+        _ptr(v_scale, "v_scale", torch.float32, (B, cap, Hkv)), _stream(stream)))
 
 
 def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace, stream,

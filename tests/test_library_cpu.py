@@ -216,3 +216,81 @@ def test_paged_valid_call_without_gpu_reports_no_device(lib):
                                           ctypes.c_void_p(0x2000), ctypes.c_void_p(0x10000), need,
                                           None)
     assert rc == DSA_ERR_NO_DEVICE
+
+
+def _rope(**kw):
+    from top_sparse_attention_chunked_gb300.dsa import DsaRopeProblem
+    base = dict(tokens=16, heads=4, head_dim=128, rotary_dim=128, max_pos=64, eps=1e-6,
+                x_dtype=0, cos_dtype=3, y_dtype=0)
+    base.update(kw)
+    return DsaRopeProblem(**base)
+
+
+def _call_rope(lib, rp, x=0x10000, y=0x20000):
+    vp = ctypes.c_void_p
+    return lib.dsa_rmsnorm_rotary(ctypes.byref(rp) if rp is not None else None, vp(x), vp(0x3000),
+                                  vp(0x4000), vp(0x5000), vp(0x6000), vp(y), None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), 2), (dict(rotary_dim=7), 1), (dict(rotary_dim=130), 1),
+    (dict(eps=-1.0), 1), (dict(heads=0), 1), (dict(tokens=-1), 1), (dict(max_pos=0), 1),
+    (dict(x_dtype=2), 2), (dict(cos_dtype=1), 2),
+])
+def test_rmsnorm_rotary_rejects_bad_problems(lib, kw, status):
+    assert _call_rope(lib, _rope(**kw)) == status
+
+
+def test_rmsnorm_rotary_pointer_rules(lib):
+    from top_sparse_attention_chunked_gb300.dsa import (DSA_ERR_INVALID_ARG, DSA_ERR_MISALIGNED)
+    assert _call_rope(lib, None) == DSA_ERR_INVALID_ARG
+    assert _call_rope(lib, _rope(), x=0x10008) == DSA_ERR_MISALIGNED
+    # 16 x 4 x 128 bf16 = 16 KiB: y starting inside x overlaps it
+    assert _call_rope(lib, _rope(), y=0x10000 + 0x2000) == DSA_ERR_INVALID_ARG
+    assert "overlaps" in lib.dsa_last_error_string().decode()
+
+
+def test_rmsnorm_rotary_in_place_and_empty_pass_host_checks(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_NO_DEVICE
+    assert _call_rope(lib, _rope(), y=0x10000) == DSA_ERR_NO_DEVICE      # in place is allowed
+    assert _call_rope(lib, _rope(tokens=0)) == DSA_ERR_NO_DEVICE
+
+
+def _rope_params(**kw):
+    from top_sparse_attention_chunked_gb300.dsa import DsaRopeParams
+    base = dict(eps=1e-6, max_pos=64, cos_dtype=3, rotary_dim=128, rotary_dim_index=64,
+                cos=0x7000, sin=0x7100, cos_index=0x7200, sin_index=0x7300, gamma_q=0x7400,
+                gamma_k=0x7500, gamma_qI=0x7600, gamma_kI=0x7700)
+    base.update(kw)
+    return DsaRopeParams(**base)
+
+
+def _call_rope_append(lib, p, rp, ks=None, vs=None):
+    vp = ctypes.c_void_p
+    ptrs = [0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x1000000, 0x2000000, 0x3000000]
+    return lib.dsa_rope_append(ctypes.byref(p), ctypes.byref(rp) if rp is not None else None,
+                               *[vp(x) for x in ptrs], vp(ks), vp(vs), None)
+
+
+@pytest.mark.parametrize("kw", [dict(rotary_dim=130), dict(rotary_dim_index=66), dict(rotary_dim=3),
+                                dict(gamma_k=0), dict(cos=0), dict(sin_index=0), dict(eps=-1.0),
+                                dict(max_pos=0)])
+def test_rope_append_rejects_bad_parameters(lib, kw):
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_INVALID_ARG
+    p = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8)
+    assert _call_rope_append(lib, p, _rope_params(**kw)) == DSA_ERR_INVALID_ARG
+
+
+def test_rope_append_host_rules(lib):
+    import torch
+    from top_sparse_attention_chunked_gb300.dsa import DSA_ERR_INVALID_ARG, DSA_ERR_NO_DEVICE
+    p = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8)
+    assert _call_rope_append(lib, p, None) == DSA_ERR_INVALID_ARG
+    assert _call_rope_append(lib, p, _rope_params(), ks=0x4000000) == DSA_ERR_INVALID_ARG  # FP16 cache
+    p8 = _prob(q_len=4, total_len=64, cache_capacity=64, top_k=8, kv_dtype="int8")
+    assert _call_rope_append(lib, p8, _rope_params()) == DSA_ERR_INVALID_ARG              # scales missing
+    if not torch.cuda.is_available():
+        assert _call_rope_append(lib, p, _rope_params()) == DSA_ERR_NO_DEVICE

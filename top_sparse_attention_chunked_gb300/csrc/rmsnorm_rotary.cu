@@ -170,20 +170,30 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
       to_floats<E>(raw[hh], xf16, x);
       float y[E];
       rms_normalize<E, D>(x, g, p.eps, y);
-      if (h > 0) {
+      float partner[E];
+      if (vec_cs) {
+        // r/2 is a multiple of E: element i's partner i +- r/2 sits in lane
+        // lane +- r/(2E) at the same slot, one shuffle away
+        const int src = !rot ? lane : (i0 < h ? lane + h / E : lane - h / E);
+#pragma unroll
+        for (int e = 0; e < E; ++e) partner[e] = __shfl_sync(0xffffffffu, y[e], src);
+      } else if (h > 0) {
 #pragma unroll
         for (int e = 0; e < E; ++e) s_y[warp][i0 + e] = y[e];
         __syncwarp();
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = i0 + e;
+          partner[e] = i < p.rotary_dim ? s_y[warp][i < h ? i + h : i - h] : 0.0f;
+        }
+        __syncwarp();   // partner reads done before the next vector's writes
       }
       uint16_t o[E];
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const int i = i0 + e;
         float v = y[e];
-        if (i < p.rotary_dim) {
-          const float partner = s_y[warp][i < h ? i + h : i - h];
-          v = rope_rotate(v, partner, c[e], sn[e], i < h);
-        }
+        if (i < p.rotary_dim) v = rope_rotate(v, partner[e], c[e], sn[e], i < h);
         o[e] = to_out(v, yf16);
       }
       uint16_t* out = static_cast<uint16_t*>(p.y) + base;
@@ -193,7 +203,6 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
       } else {
         *reinterpret_cast<uint32_t*>(out) = o[0] | (static_cast<uint32_t>(o[1]) << 16);
       }
-      if (h > 0) __syncwarp();   // partner reads done before the next vector's writes
     }
   }
 }

@@ -9,11 +9,12 @@
 
 namespace dsa {
 
-// y = x * g / sqrt(mean(x^2) + eps) for the warp's vector. When the fp32 sum of
-// squares leaves [2^-100, 2^100] (or is zero) the vector is first scaled by
-// 2^-+64 (exact, chosen from its absmax) so that the sum neither overflows nor
-// vanishes; the scale cancels in y, and eps takes its square (in two steps:
-// 2^128 is not an fp32 value). x is overwritten by the scaled copy.
+// y = x * g / sqrt(mean(x^2) + eps) for the warp's vector, 1/sqrt taken in one
+// correctly rounded step. When the fp32 sum of squares leaves [2^-100, 2^100]
+// (or is zero) the vector is first scaled by 2^-+64 (exact, chosen from its
+// absmax) so that the sum neither overflows nor vanishes; the scale cancels in
+// y, and eps takes its square (in two steps: 2^128 is not an fp32 value). x is
+// overwritten by the scaled copy.
 template <int E, int D>
 __device__ __forceinline__ void rms_normalize(float* x, const float* g, float eps_in, float* y) {
   float ss = 0.0f;
@@ -45,7 +46,7 @@ __device__ __forceinline__ void rms_normalize(float* x, const float* g, float ep
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
   }
-  const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / D), eps)));
+  const float inv = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / D), eps));   // one rounding
 #pragma unroll
   for (int e = 0; e < E; ++e) y[e] = __fmul_rn(__fmul_rn(x[e], inv), g[e]);
 }

@@ -389,6 +389,30 @@ def check_append_positions(mod):
                 assert (kI2[b, t] == -9).all() and (k2[b, t] == -9).all() and (v2[b, t] == -9).all()
 
 
+def check_round_to(mod):
+    """Round-to-nearest-even into the 16-bit formats, worked from their
+    definitions: FP16 has 10 fraction bits, largest finite 65,504, subnormal
+    step 2^-24; BF16 has 7 fraction bits and FP32's exponent range."""
+    f16 = mod.round_to(np.array([65504.0, 65519.0, 65520.0, 1e-6, 2.0 ** -25, 3 * 2.0 ** -25,
+                                 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11]), "fp16")
+    assert f16[0] == 65504.0
+    assert f16[1] == 65504.0                      # below the midpoint to 2^16
+    assert np.isposinf(f16[2])                    # the midpoint: ties to even = 2^16, overflow
+    assert f16[3] == 17 * 2.0 ** -24              # 1e-6 / 2^-24 = 16.78
+    assert f16[4] == 0.0                          # half the smallest step: ties to even (0)
+    assert f16[5] == 2 * 2.0 ** -24               # 1.5 steps: ties to even (2)
+    assert f16[6] == 1.0                          # 1 + half an ulp: ties to even
+    assert f16[7] == 1.0 + 2.0 ** -9              # 1 + 1.5 ulp: ties to even (2 ulp)
+    bf = mod.round_to(np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 70000.0, 3.0e38]), "bf16")
+    assert bf[0] == 1.0 and bf[1] == 1.0 + 2.0 ** -6
+    assert bf[2] == 70144.0                       # 70000 = 1.068 * 2^16: steps of 2^9
+    assert bf[3] == 226 * 2.0 ** 120               # 3e38 / 2^120 = 225.7: the nearest step
+
+
+def test_round_to_ieee_cases():
+    check_round_to(O)
+
+
 def test_quantize_golden_fixture():
     check_quantize_fixture(O)
 
@@ -662,3 +686,13 @@ def test_mutant_rope_eps_outside_sqrt_is_caught():
 
 def test_mutant_rope_norm_over_all_heads_is_caught():
     assert _fails(check_rope_complex, _Mutant(rmsnorm_rotary=_rope_variant(norm_all_heads=True)))
+
+
+def test_mutant_round_toward_zero_is_caught():
+    def bad(values, dtype):
+        import torch
+        t = torch.as_tensor(np.asarray(values, dtype=np.float64)).to(torch.float32)
+        bits = {"bf16": 7, "fp16": 10, "fp32": 23}[dtype]
+        m, e = np.frexp(t.numpy().astype(np.float64))
+        return np.ldexp(np.trunc(m * 2.0 ** (bits + 1)) / 2.0 ** (bits + 1), e)
+    assert _fails(check_round_to, _Mutant(round_to=bad))

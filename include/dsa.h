@@ -19,6 +19,11 @@
  *                online-softmax combine (follow-up PR #33847: the rescale never
  *                flushes the earlier tiles).
  *
+ * Around the step: the cache append of the new tokens (with INT8
+ * quantise-on-write), fp32 RMSNorm + rotary embedding, both in one launch
+ * (dsa_rope_append), and _paged forms of the calls for caches kept in a pool
+ * of token blocks with a block table.
+ *
  * Conventions (all calls):
  *  - Positions: a sequence's cache holds T_b = total_len[b] rows and its
  *    q_len new query tokens are the LAST q_len rows, so query s sits at

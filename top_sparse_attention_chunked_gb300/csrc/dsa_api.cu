@@ -916,7 +916,7 @@ const char* dsa_status_string(int s) {
   }
 }
 
-int dsa_version(void) { return 100; }
+int dsa_version(void) { return 200; }
 
 int dsa_last_launches(char* buf, size_t buflen) {
   if (buf && buflen > 0) {

@@ -49,12 +49,31 @@ constexpr int kTile8 = kTileKeys * kD;           // 2 KB: one 16-key tile, INT8
 constexpr int kWarpSmem = 4 * kTile16;
 // the split combine merges up to kAttnMaxSplits partial states
 constexpr int kMaxCombine = kAttnMaxSplits;
-constexpr int kMergeFloats = kAttnWarps * kPartialFloats + 2 * kMaxCombine * kAttnRows + 2 * kAttnRows;
-constexpr int kAttnSmem = ((kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnWarps * kWarpSmem
-                                                                        : kMergeFloats * 4) +
-                          1024;   // slack to align the base to 1024 bytes
+// per-warp partial state in shared memory: m[16], l[16], o[16][kORow] (rows
+// padded to 136 floats so the fragment stores of a half-warp hit distinct banks)
+constexpr int kORow = DSA_HEAD_DIM + 8;
+constexpr int kWarpState = 2 * kAttnRows + kAttnRows * kORow;
+constexpr int kMergeFloats = kAttnWarps * kWarpState + 2 * kMaxCombine * kAttnRows + 2 * kAttnRows;
+constexpr int kStageBytes = (kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnWarps * kWarpSmem
+                                                                       : kMergeFloats * 4;
+// Cluster combine: every CTA receives from each peer q its M, L (32 floats at
+// q * 32) and, for the output columns this CTA owns, q's unnormalised rows
+// (column-major, 16 rows per column, at 512 + (q * cols + c) * 16): at most
+// 16 * 32 + 2,048 floats, written by the peers with st.async while this CTA
+// may still be gathering, so it has its own region.
+constexpr int kRecvFloats = 16 * 2 * kAttnRows + kAttnRows * DSA_HEAD_DIM;
+constexpr int kAttnSmem = kStageBytes + kRecvFloats * 4 + 1024;   // + slack to align the base
 
 enum { KV_BF16 = 0, KV_FP16 = 1, KV_INT8 = 2 };
+
+// 16-bit K/V rows are gathered with 16-byte cp.async (each warp instruction
+// moves two whole 256-byte rows) unless built with DSA_ATTN_TMA_GATHER, which
+// selects TMA tile::gather4 row gathers.
+#ifdef DSA_ATTN_TMA_GATHER
+constexpr bool kTmaGather16 = true;
+#else
+constexpr bool kTmaGather16 = false;
+#endif
 
 // Byte offset of 16-byte chunk c (0..15) of row r in a 16-row 16-bit tile:
 // two 64-column blocks of 16 x 128 B, chunk positions XOR-swizzled by the row
@@ -181,8 +200,13 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   __shared__ uint64_t s_bar[kAttnWarps][2];     // per warp and stage: the tile's rows landed
   __shared__ int s_abort;
   __shared__ float s_sc[kAttnWarps][64];        // INT8: [stage][k 16 | v 16] scales per warp
+  __shared__ uint64_t s_merge_bar;              // cluster combine: every peer's slice landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    DSA_TRACE_MIN(p.status, 15);
+    DSA_TRACE_MAX(p.status, 22);
+  }
   const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates
   const int r = blockIdx.z;                  // query row = b * S + s
   const int b = r / p.S, s = r % p.S;
@@ -212,6 +236,19 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     fence_mbar_init();
   }
   if (threadIdx.x == 0) s_abort = 0;
+  float* recv = reinterpret_cast<float*>(smem + kStageBytes);
+  if (p.cluster) {
+    // the combine's receive barrier expects every peer's M, L and column
+    // slice; peers push into it only after the cluster barrier below, which
+    // every CTA arrives at once its barrier is armed
+    if (threadIdx.x == 0) {
+      mbar_init(&s_merge_bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&s_merge_bar,
+                            static_cast<uint32_t>((p.nsplit * 2 * kAttnRows + kAttnRows * kD) * 4));
+    }
+    cluster_arrive();
+  }
 
   const int32_t* idx_row = p.idx + static_cast<size_t>(r) * p.topk + split_begin;
   bool bad_page = false;   // a gathered key's block-table entry lay outside the pool
@@ -249,6 +286,22 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       const size_t so = static_cast<size_t>(cr) * p.Hkv + g;
       if (lane < 16) cp_async4(sSc + st * 32 + lane, p.k_scale + so, kr >= 0);
       else cp_async4(sSc + st * 32 + lane, p.v_scale + so, kr >= 0);
+    } else if constexpr (!kTmaGather16) {
+      // 16-bit rows (256 B): lanes 0-15 copy chunk `lane` of row 2i, lanes
+      // 16-31 of row 2i + 1, into the swizzled layout ldmatrix reads; invalid
+      // keys land as zeros (their logits are masked)
+      const uint8_t* kb = static_cast<const uint8_t*>(p.k);
+      const uint8_t* vb = static_cast<const uint8_t*>(p.v);
+      const int c = lane & 15;
+#pragma unroll
+      for (int i = 0; i < kTileKeys / 2; ++i) {
+        const int row = 2 * i + (lane >> 4);
+        const int kr = __shfl_sync(0xffffffffu, key, row);
+        const long long cr = __shfl_sync(0xffffffffu, crow, row);
+        const size_t off = ((static_cast<size_t>(cr) * p.Hkv + g) * kD) * 2 + c * 16;
+        cp_async16(sK[st] + swz(row, c), kb + off, kr >= 0);
+        cp_async16(sV[st] + swz(row, c), vb + off, kr >= 0);
+      }
     } else {
       // 16-bit rows (256 B): TMA row gathers, lane l of the first 16 issuing
       // one for 4 rows (grp) of one column block (blk) of K or V (tsr)
@@ -294,10 +347,12 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     tma_prefetch_desc(&tm_v);
   }
   pdl_wait();       // the selected indices come from the previous kernel
+  if (threadIdx.x == 0) DSA_TRACE_MIN(p.status, 16);
   pdl_trigger();
   // the split's selected indices, loaded once (all loads in flight together)
   for (int i = threadIdx.x; i < split_len; i += kAttnThreads) s_idx[i] = __ldcg(idx_row + i);
   __syncthreads();
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 17);
   if (my_tiles > 0) issue_tile(0, 0);
   cp_async_commit();
   int issued = my_tiles > 0 ? 1 : 0, landed = 0;
@@ -309,13 +364,14 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       ++issued;
     }
     cp_async_commit();
-    cp_async_wait<1>();   // INT8 tiles
-    if constexpr (KV != KV_INT8) {
+    cp_async_wait<1>();   // cp.async tiles
+    if constexpr (KV != KV_INT8 && kTmaGather16) {
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_bar[warp][st],
                                                       static_cast<uint32_t>((it >> 1) & 1), &s_abort)))
         break;
     }
     landed = it + 1;
+    if (it == 0 && lane == 0) DSA_TRACE_MAX(p.status, 18);
     __syncwarp();
     const int tile = warp + it * kAttnWarps;
     const int nvalid = min(kTileKeys, split_len - tile * kTileKeys);
@@ -461,10 +517,14 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   cp_async_wait<0>();
   // after a wait that gave up, let this warp's copies land before the
   // buffers are reused
-  if (KV != KV_INT8 && landed < issued && lane == 0)
+  if (KV != KV_INT8 && kTmaGather16 && landed < issued && lane == 0)
     for (int t = landed; t < issued; ++t)
       mbar_drain_attn(&s_bar[warp][t & 1], static_cast<uint32_t>((t >> 1) & 1));
 
+  if (lane == 0) {
+    DSA_TRACE_MAX(p.status, 19);
+    DSA_TRACE_MIN(p.status, 27);
+  }
   // ---- merge the warps of this CTA
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -474,11 +534,11 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   __syncthreads();   // stage buffers become the merge area
   if (threadIdx.x == 0 && s_abort && p.status) atomicOr(p.status, kDevTimeout);
   if (__any_sync(0xffffffffu, bad_page) && lane == 0 && p.status) atomicOr(p.status, kDevBadPage);
-  float* ws = reinterpret_cast<float*>(smem);      // [warps][kPartialFloats]
-  float* fac1 = ws + kAttnWarps * kPartialFloats;  // [max(warps, splits)][16]
+  float* ws = reinterpret_cast<float*>(smem);      // [warps][kWarpState]
+  float* fac1 = ws + kAttnWarps * kWarpState;      // [max(warps, splits)][16]
   float* fac2 = fac1 + kMaxCombine * kAttnRows;
   float* sML = fac2 + kMaxCombine * kAttnRows;     // M[16], L[16]
-  float* mine = ws + warp * kPartialFloats;
+  float* mine = ws + warp * kWarpState;
   if (tq == 0) {
     mine[gq] = m_run[0];
     mine[gq + 8] = m_run[1];
@@ -488,14 +548,16 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
 #pragma unroll
   for (int nd = 0; nd < kD / 8; ++nd)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int row = gq + 8 * (e >> 1), col = nd * 8 + 2 * tq + (e & 1);
-      mine[2 * kAttnRows + row * kD + col] = o_acc[nd][e];
+    for (int h = 0; h < 2; ++h) {
+      const int row = gq + 8 * h, col = nd * 8 + 2 * tq;
+      *reinterpret_cast<float2*>(mine + 2 * kAttnRows + row * kORow + col) =
+          make_float2(o_acc[nd][2 * h], o_acc[nd][2 * h + 1]);
     }
   __syncthreads();
   if (threadIdx.x < kAttnRows)
-    combine_factors(ws, kPartialFloats, kAttnWarps, fac1, fac2, sML);
+    combine_factors(ws, kWarpState, kAttnWarps, fac1, fac2, sML);
   __syncthreads();
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 24);
 
   const int d = threadIdx.x;   // one output column per thread
   const bool single = (p.nsplit == 1);
@@ -507,7 +569,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   for (int w = 0; w < kAttnWarps; ++w)
 #pragma unroll
     for (int row = 0; row < kAttnRows; ++row)
-      acc[row] += ws[w * kPartialFloats + 2 * kAttnRows + row * kD + d] *
+      acc[row] += ws[w * kWarpState + 2 * kAttnRows + row * kORow + d] *
                   fac1[w * kAttnRows + row] * fac2[w * kAttnRows + row];
   if (single) {
 #pragma unroll
@@ -516,74 +578,68 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     return;
   }
   if (p.cluster) {
-    // ---- split combine inside the thread-block cluster: every split CTA
-    // publishes its state in its own shared memory, then each CTA merges one
-    // slice of the output columns from all peers' shared memory.
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    __syncthreads();   // ws reads above are done
-    float* pubO = ws;  // [16][128]
-#pragma unroll
-    for (int row = 0; row < kAttnRows; ++row) pubO[row * kD + d] = acc[row];
-    cluster.sync();
+    // ---- split combine inside the thread-block cluster. CTA q owns output
+    // columns [q * cols, (q + 1) * cols). Every CTA pushes, with st.async into
+    // the owners' shared memory, each column's 16 rows and its M, L; the
+    // owner's barrier completes when all peers' bytes have landed. Nothing is
+    // read from a peer, so no CTA waits for another to leave.
     const int ns = p.nsplit;
-    const int rank = static_cast<int>(cluster.block_rank());
-    float* cf = pubO + kAttnRows * kD;   // [16 peers][16 rows] factors f1, f2; M, L
-    float* cm = cf + 2 * 16 * kAttnRows;   // [16 peers][16 rows] peer m, then l
-    // every (peer, row) pair in parallel: peer m and l into local shared memory
-    for (int pr = threadIdx.x; pr < 16 * kAttnRows; pr += kAttnThreads) {
-      const int q = pr / kAttnRows, row = pr % kAttnRows;
-      float mq = -INFINITY, lq = 0.0f;
-      if (q < ns) {
-        const float* peerML = cluster.map_shared_rank(sML, q);
-        mq = peerML[row];
-        lq = peerML[kAttnRows + row];
-      }
-      cm[pr] = mq;
-      cm[16 * kAttnRows + pr] = lq;
-    }
-    __syncthreads();
-    float* sMrow = cm + 2 * 16 * kAttnRows;   // M[16], L[16]
-    if (threadIdx.x < kAttnRows) {
-      float M = -INFINITY;
+    const int cols = kD / ns;                      // ns divides 128 (power of two)
+    const uint32_t rank = cluster_ctarank();
+    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 28);
+    cluster_wait();                                // every peer's barrier is armed
+    {
+      const uint32_t q = static_cast<uint32_t>(d / cols), c = static_cast<uint32_t>(d % cols);
+      const uint32_t bar_q = cluster_map(&s_merge_bar, q);
+      const uint32_t dst = cluster_map(recv + 16 * 2 * kAttnRows + (rank * cols + c) * kAttnRows, q);
 #pragma unroll
-      for (int q = 0; q < 16; ++q) M = fmaxf(M, cm[q * kAttnRows + threadIdx.x]);
-      sMrow[threadIdx.x] = M;
+      for (int j = 0; j < kAttnRows / 4; ++j)
+        st_async_v4(dst + 16u * j, acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3], bar_q);
+      if (threadIdx.x < static_cast<unsigned>(ns)) {
+        const uint32_t q2 = threadIdx.x;
+        const uint32_t bar2 = cluster_map(&s_merge_bar, q2);
+        const uint32_t dml = cluster_map(recv + rank * 2 * kAttnRows, q2);
+#pragma unroll
+        for (int j = 0; j < 2 * kAttnRows / 4; ++j)
+          st_async_v4(dml + 16u * j, sML[4 * j], sML[4 * j + 1], sML[4 * j + 2], sML[4 * j + 3], bar2);
+      }
     }
-    __syncthreads();
-    for (int pr = threadIdx.x; pr < 16 * kAttnRows; pr += kAttnThreads) {
-      const int row = pr % kAttnRows;
-      float f1, f2;
-      exp2_pair(cm[pr] - sMrow[row], &f1, &f2);
-      cf[pr] = f1;
-      cf[16 * kAttnRows + pr] = f2;
+    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 25);
+    // every peer pushes, even one whose gathers gave up, so this wait ignores
+    // the abort flag (a CTA must not leave while peers may still write to it)
+    bool landed_all = mbar_try_wait(&s_merge_bar, 0u);
+    for (const long long t0 = clock64(); !landed_all && clock64() - t0 <= kWaitBudgetCycles;)
+      landed_all = mbar_try_wait(&s_merge_bar, 0u);
+    if (!landed_all) {
+      if (threadIdx.x == 0 && p.status) atomicOr(p.status, kDevTimeout);
+      return;
     }
-    __syncthreads();
-    if (threadIdx.x < kAttnRows) {   // row sums in a fixed order (deterministic)
-      float L = 0.0f;
+    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 26);
+    for (int o = threadIdx.x; o < kAttnRows * cols; o += kAttnThreads) {
+      const int row = o % kAttnRows, c = o / kAttnRows;
+      float mq[16], lq[16], ov[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
-        const int pr = q * kAttnRows + threadIdx.x;
-        L += cm[16 * kAttnRows + pr] * cf[pr] * cf[16 * kAttnRows + pr];
+        const bool in = q < ns;
+        mq[q] = in ? recv[q * 2 * kAttnRows + row] : -INFINITY;
+        lq[q] = in ? recv[q * 2 * kAttnRows + kAttnRows + row] : 0.0f;
+        ov[q] = in ? recv[16 * 2 * kAttnRows + (q * cols + c) * kAttnRows + row] : 0.0f;
       }
-      sMrow[kAttnRows + threadIdx.x] = L;
-    }
-    __syncthreads();
-    const int cols = kD / ns;                      // ns divides 128 (power of two)
-    for (int o = threadIdx.x; o < kAttnRows * cols; o += kAttnThreads) {
-      const int row = o / cols, col = rank * cols + o % cols;
-      if (row >= nh) continue;
-      float ov[16];
+      float M = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        ov[q] = q < ns ? cluster.map_shared_rank(pubO, q)[row * kD + col] : 0.0f;
-      float O = 0.0f;
+      for (int q = 0; q < 16; ++q) M = fmaxf(M, mq[q]);
+      // the peers' weights 2^(m_q - M), summed in a fixed order (deterministic)
+      float L = 0.0f, O = 0.0f;
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        O += ov[q] * cf[q * kAttnRows + row] * cf[16 * kAttnRows + q * kAttnRows + row];
-      store_out<OUT>(p.out, (out_row + row) * kD + col, O / sMrow[kAttnRows + row]);
+      for (int q = 0; q < 16; ++q) {
+        float f1, f2;
+        exp2_pair(mq[q] - M, &f1, &f2);
+        L += lq[q] * f1 * f2;
+        O += ov[q] * f1 * f2;
+      }
+      if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + rank * cols + c, O / L);
     }
-    cluster.sync();    // peers may still be reading this CTA's shared memory
+    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 20);
     return;
   }
   float* part = p.partial + ((static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit + blockIdx.x) *

@@ -203,16 +203,23 @@ int check_problem(const dsa_problem* p, int op, Derived* d) {
   return DSA_OK;
 }
 
+// Automatic split count before rounding: enough CTAs for two per SM, and,
+// while the grid stays within one wave of three CTAs per SM, at most 128 keys
+// (two 16-key tiles per warp) per split; up to the 16 CTAs a cluster merges,
+// never splits of fewer than 16 keys.
+int auto_splits(const Derived& d, int units, int sms) {
+  int s = std::max(ceil_div(2 * sms, units), std::min(ceil_div(d.kmax, 128), 3 * sms / units));
+  s = std::min(s, 16);
+  s = std::min(s, ceil_div(d.kmax, 16));
+  return s < 1 ? 1 : s;
+}
+
 // Upper bound of the automatic split count (any GPU with <= 256 SMs).
 int splits_bound(const dsa_problem* p, const Derived& d) {
   if (p->attn_split_keys > 0) return ceil_div(d.kmax, p->attn_split_keys);
-  if (ceil_div(d.kmax, 64) > kAttnMaxSplits) return kAttnMaxSplits;
+  if (ceil_div(d.kmax, kAttnMaxSplitKeys) > 16) return kAttnMaxSplits;
   const int units = d.rows * p->num_kv_heads * d.HG;
-  int s = ceil_div(2 * 256, units);
-  s = s < 16 ? s : 16;
-  const int cap = ceil_div(d.kmax, 64);
-  s = s < cap ? s : cap;
-  return s < 1 ? 1 : s;
+  return auto_splits(d, units, 256);
 }
 
 // Actual split of the selected keys for the attention kernel.
@@ -222,11 +229,7 @@ void choose_split(const dsa_problem* p, const Derived& d, int sms, int* split_ke
     sk = p->attn_split_keys;
   } else {
     const int units = d.rows * p->num_kv_heads * d.HG;
-    int s = ceil_div(2 * sms, units);
-    s = s < 16 ? s : 16;
-    const int cap = ceil_div(d.kmax, 64);
-    s = s < cap ? s : cap;
-    if (s < 1) s = 1;
+    int s = auto_splits(d, units, sms);
     if (s > attn_max_cluster()) s = attn_max_cluster();
     // a power of two (so the cluster combine splits the 128 columns evenly),
     // and no split longer than kAttnMaxSplitKeys
@@ -406,10 +409,30 @@ int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, co
   return DSA_OK;
 }
 
+// The decode's caches, for the top-k's L2 prefetch of the selected rows.
+struct KvPrefetch {
+  const void* k;
+  const void* v;
+  const float* ks;
+  const float* vs;
+  Paging pg;
+};
+
 int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
              const float* scores, int32_t* idx, void* ws, bool hist_ready, bool prefer_rows,
-             bool after_kernel, cudaStream_t st) {
-  TopkParams tp;
+             bool after_kernel, cudaStream_t st, const KvPrefetch* pf = nullptr) {
+  TopkParams tp{};
+  tp.status = at<uint32_t>(ws, 0);
+  if (pf) {
+    const int elem = p->kv_dtype == DSA_INT8 ? 1 : 2;
+    tp.pf_k = static_cast<const uint8_t*>(pf->k);
+    tp.pf_v = static_cast<const uint8_t*>(pf->v);
+    tp.pf_ks = pf->ks;
+    tp.pf_vs = pf->vs;
+    tp.pf_row_bytes = p->num_kv_heads * DSA_HEAD_DIM * elem;
+    tp.pf_heads = p->num_kv_heads;
+    tp.pg = pf->pg;
+  }
   tp.scores = scores;
   tp.idx = idx;
   tp.hist = at<uint32_t>(ws, L.hist);
@@ -603,7 +626,7 @@ int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, con
   if (hist_in_indexer || attn_tickets) {
     // histograms, tickets and counters start at zero; the clearing kernel
     // overlaps the indexer, which waits for it only before its final flush
-    cudaError_t e = launch_zero_scratch(ws, L.zero_end, st);
+    cudaError_t e = launch_zero_scratch(at<uint8_t>(ws, L.zero_begin), L.zero_end - L.zero_begin, st);
     if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
   }
   float* scores = at<float>(ws, L.scores);
@@ -612,7 +635,9 @@ int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, con
   rc = run_indexer(p, d, di, pg, qI, w, kI, scores, hist_in_indexer ? at<uint32_t>(ws, L.hist) : nullptr,
                    status, st);
   if (rc) return rc;
-  rc = run_topk(p, d, di, L, scores, idx, ws, hist_in_indexer, topk_rows, true, st);
+  const KvPrefetch pf{k, v, ks, vs, pg};
+  rc = run_topk(p, d, di, L, scores, idx, ws, hist_in_indexer, topk_rows, true, st,
+                decode ? &pf : nullptr);
   if (rc) return rc;
   return run_attention(p, d, di, L, pg, q, k, v, ks, vs, idx, out, ws, !decode, st);
 }

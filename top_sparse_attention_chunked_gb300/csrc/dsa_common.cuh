@@ -100,4 +100,28 @@ __device__ __forceinline__ void find_threshold_digit(const uint32_t* h, int nb, 
   __syncthreads();
 }
 
+// ----------------------------------------------------------- phase stamps
+// For latency studies only: compiled with -DDSA_TRACE, a kernel keeps in 64-bit
+// slot `slot` (0..30, at byte 8 of the workspace's status block) the
+// earliest (DSA_TRACE_MIN) or latest (DSA_TRACE_MAX) %globaltimer reading seen
+// at that point of the step. Without the define both expand to nothing.
+#ifdef DSA_TRACE
+__device__ __forceinline__ unsigned long long trace_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define DSA_TRACE_MIN(status, slot)                                                           \
+  do {                                                                                        \
+    if (status) atomicMin(reinterpret_cast<unsigned long long*>(status) + 1 + (slot), ::dsa::trace_now()); \
+  } while (0)
+#define DSA_TRACE_MAX(status, slot)                                                           \
+  do {                                                                                        \
+    if (status) atomicMax(reinterpret_cast<unsigned long long*>(status) + 1 + (slot), ::dsa::trace_now()); \
+  } while (0)
+#else
+#define DSA_TRACE_MIN(status, slot) ((void)0)
+#define DSA_TRACE_MAX(status, slot) ((void)0)
+#endif
+
 }  // namespace dsa

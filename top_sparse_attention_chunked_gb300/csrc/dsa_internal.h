@@ -112,6 +112,17 @@ struct TopkParams {
   int nchunks;                  // chunks of the longest row
   int row0, nrows;              // rows handled by this launch (workspace rows are local)
   int hist_ready;               // cluster select: the row histograms are in `hist`
+  uint32_t* status;             // device status word (nullptr: none)
+  // Decode: as the cluster select emits a key it prefetches that token's K
+  // and V rows (all KV heads) and INT8 scales into L2 for the attention that
+  // follows. pf_k == nullptr: no prefetch.
+  const uint8_t* pf_k;
+  const uint8_t* pf_v;
+  const float* pf_ks;           // INT8 scales [.., Hkv] or nullptr
+  const float* pf_vs;
+  int pf_row_bytes;             // bytes of one token's K (or V) over all KV heads
+  int pf_heads;                 // KV heads
+  Paging pg;                    // cache addressing of the prefetched rows
   SeqLens lens;
 };
 

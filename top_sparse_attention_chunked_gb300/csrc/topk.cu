@@ -655,7 +655,12 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
   const int rank = static_cast<int>(cluster.block_rank());
   const int ncta = static_cast<int>(cluster.num_blocks());
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    DSA_TRACE_MIN(p.status, 8);
+    DSA_TRACE_MAX(p.status, 21);
+  }
   pdl_wait();      // scores and the histogram come from the previous kernel
+  if (threadIdx.x == 0) DSA_TRACE_MIN(p.status, 9);
   pdl_trigger();
   const RowInfo ri = row_info(p, r);
   const int t0 = rank * kSlice;
@@ -714,9 +719,11 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
     __syncthreads();
   }
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 10);
   // ---- threshold bin: a block-wide scan of the histogram
   find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
                                    &s_above, &s_cnt);
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 11);
   const uint32_t bin = static_cast<uint32_t>(s_d);
   uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
   const bool all0 = (need == s_cnt);             // the whole threshold bin is selected
@@ -764,6 +771,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
   // same path
   const bool gather = all || s_cnt <= static_cast<uint32_t>(kClGatherMax);
   cluster.sync();                                // candidates and counts are published
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 12);
 
   uint32_t pos = 0;                              // this CTA's first output slot
   int off_mine = 0;                              // gathered candidates of lower ranks
@@ -771,8 +779,8 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     // ---- every CTA gathers all candidates and counts, then resolves locally
     unsigned long long* sg = scand + PER * kClThreads;   // gathered candidates
     if (threadIdx.x < ncta) {
-      s_pc[threadIdx.x] = *cluster.map_shared_rank(&s_ncand, threadIdx.x);
-      s_ps[threadIdx.x] = *cluster.map_shared_rank(&s_nsure, threadIdx.x);
+      s_pc[threadIdx.x] = ld_cluster_u32(cluster_map(&s_ncand, threadIdx.x));
+      s_ps[threadIdx.x] = ld_cluster_u32(cluster_map(&s_nsure, threadIdx.x));
     }
     __syncthreads();
     int off = 0;
@@ -788,13 +796,13 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
         int base = 0;
         for (int q = 0; q < warp; ++q) base += static_cast<int>(s_pc[q]);
         const int cnt = static_cast<int>(s_pc[warp]);
-        const unsigned long long* peer = cluster.map_shared_rank(scand, warp);
+        const uint32_t peer = cluster_map(scand, warp);
         for (int i0 = 0; i0 < cnt; i0 += 128) {
           unsigned long long v[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int i = i0 + u * 32 + lane;
-            v[u] = i < cnt ? peer[i] : 0ull;
+            v[u] = i < cnt ? ld_cluster_u64(peer + 8u * i) : 0ull;
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -807,6 +815,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
     // this CTA is done reading its peers: arrive now, wait before exiting
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 29);
     if (!all0)
       resolve_composites<kClThreads>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
                                      &s_cnt, 52);
@@ -848,6 +857,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
   }
 
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 13);
   // ---- selection bits: bins above the threshold bin, or in it with the
   // determined composite bits at or above the threshold prefix; one block
   // scan gives both the in-CTA positions (low half) and, on the gather path,
@@ -876,6 +886,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
   }
   uint32_t total;
   const uint32_t packed = block_exclusive_scan<kClThreads>(mine | (lower << 16), warp_tot, &total);
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 30);
   pos += (packed & 0xFFFFu) + (total >> 16);
   if (!gather) {
     if (threadIdx.x == 0) s_count = total & 0xFFFFu;
@@ -883,12 +894,27 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     for (int q = 0; q < rank; ++q) pos += *cluster.map_shared_rank(&s_count, q);
   }
 #pragma unroll
+  const int seq = r / p.S;
   for (int wd = 0; wd < (PER + 31) / 32; ++wd) {
     uint32_t bits = selm[wd];
     while (bits) {
       const int j = __ffs(bits) - 1;
       bits &= bits - 1;
-      if (pos < static_cast<uint32_t>(ri.keff)) out[pos] = t0 + tb + wd * 32 + j;
+      if (pos < static_cast<uint32_t>(ri.keff)) {
+        const int t = t0 + tb + wd * 32 + j;
+        out[pos] = t;
+        if (p.pf_k) {
+          // the attention gathers this token's rows next: start them into L2
+          bool bad = false;
+          const long long row = cache_row(p.pg, seq, p.cap, t, &bad);
+          prefetch_l2_bulk(p.pf_k + row * p.pf_row_bytes, p.pf_row_bytes);
+          prefetch_l2_bulk(p.pf_v + row * p.pf_row_bytes, p.pf_row_bytes);
+          if (p.pf_ks) {
+            prefetch_l2_line(p.pf_ks + row * p.pf_heads);
+            prefetch_l2_line(p.pf_vs + row * p.pf_heads);
+          }
+        }
+      }
       ++pos;
     }
   }
@@ -896,6 +922,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     for (int i = ri.keff + threadIdx.x; i < p.k; i += kClThreads) out[i] = -1;
   if (gather) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   else cluster.sync();                           // peers may still read this CTA's s_count
+  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 14);
 }
 
 // Cluster shape for rows of up to max_n keys: keys per thread and CTAs per

@@ -86,7 +86,7 @@ extern "C" int dsa_topk_noalloc(const dsa_problem* p, const float* scores, int32
   cudaError_t e = cudaMemsetAsync(base, 0, kNaZeroEnd, st);
   if (e != cudaSuccess) return noalloc_fail(DSA_ERR_CUDA, "clearing the top-k scratch failed");
 
-  TopkParams tp;
+  TopkParams tp{};
   tp.scores = scores;
   tp.idx = idx;
   tp.hist = reinterpret_cast<uint32_t*>(base + kNaHist);

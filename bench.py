@@ -56,7 +56,7 @@ def peaks():
 # profiles/). They hold for the indexer source they were taken on: when any of
 # these files changes, the figure is dropped (null) until it is measured again.
 TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh", "dsa_internal.h"]
-TRAFFIC_SOURCE_SHA = "3576e237dfdf92c1"
+TRAFFIC_SOURCE_SHA = "638f37ae5c0ec876"
 INDEXER_TRAFFIC = {
     "decode_4k": 572672,
     "grouped_decode_32k": 16906496,

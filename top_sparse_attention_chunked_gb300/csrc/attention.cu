@@ -203,10 +203,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   __shared__ uint64_t s_merge_bar;              // cluster combine: every peer's slice landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    DSA_TRACE_MIN(p.status, 15);
-    DSA_TRACE_MAX(p.status, 22);
-  }
+  DSA_TS_DECL;
+  if (threadIdx.x == 0) DSA_TS(0);
   const int gq = lane >> 2, tq = lane & 3;   // MMA fragment coordinates
   const int r = blockIdx.z;                  // query row = b * S + s
   const int b = r / p.S, s = r % p.S;
@@ -347,12 +345,12 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     tma_prefetch_desc(&tm_v);
   }
   pdl_wait();       // the selected indices come from the previous kernel
-  if (threadIdx.x == 0) DSA_TRACE_MIN(p.status, 16);
+  if (threadIdx.x == 0) DSA_TS(1);
   pdl_trigger();
   // the split's selected indices, loaded once (all loads in flight together)
   for (int i = threadIdx.x; i < split_len; i += kAttnThreads) s_idx[i] = __ldcg(idx_row + i);
   __syncthreads();
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 17);
+  if (threadIdx.x == 0) DSA_TS(2);
   if (my_tiles > 0) issue_tile(0, 0);
   cp_async_commit();
   int issued = my_tiles > 0 ? 1 : 0, landed = 0;
@@ -371,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
         break;
     }
     landed = it + 1;
-    if (it == 0 && lane == 0) DSA_TRACE_MAX(p.status, 18);
+    if (it == 0 && lane == 0) DSA_TS(3);
     __syncwarp();
     const int tile = warp + it * kAttnWarps;
     const int nvalid = min(kTileKeys, split_len - tile * kTileKeys);
@@ -521,10 +519,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     for (int t = landed; t < issued; ++t)
       mbar_drain_attn(&s_bar[warp][t & 1], static_cast<uint32_t>((t >> 1) & 1));
 
-  if (lane == 0) {
-    DSA_TRACE_MAX(p.status, 19);
-    DSA_TRACE_MIN(p.status, 27);
-  }
+  if (lane == 0) DSA_TS(4);
   // ---- merge the warps of this CTA
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -557,7 +552,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   if (threadIdx.x < kAttnRows)
     combine_factors(ws, kWarpState, kAttnWarps, fac1, fac2, sML);
   __syncthreads();
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 24);
+  if (threadIdx.x == 0) DSA_TS(5);
 
   const int d = threadIdx.x;   // one output column per thread
   const bool single = (p.nsplit == 1);
@@ -586,7 +581,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     const int ns = p.nsplit;
     const int cols = kD / ns;                      // ns divides 128 (power of two)
     const uint32_t rank = cluster_ctarank();
-    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 28);
+    if (threadIdx.x == 0) DSA_TS(6);
     cluster_wait();                                // every peer's barrier is armed
     {
       const uint32_t q = static_cast<uint32_t>(d / cols), c = static_cast<uint32_t>(d % cols);
@@ -604,7 +599,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
           st_async_v4(dml + 16u * j, sML[4 * j], sML[4 * j + 1], sML[4 * j + 2], sML[4 * j + 3], bar2);
       }
     }
-    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 25);
+    if (threadIdx.x == 0) DSA_TS(7);
     // every peer pushes, even one whose gathers gave up, so this wait ignores
     // the abort flag (a CTA must not leave while peers may still write to it)
     bool landed_all = mbar_try_wait(&s_merge_bar, 0u);
@@ -614,7 +609,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       if (threadIdx.x == 0 && p.status) atomicOr(p.status, kDevTimeout);
       return;
     }
-    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 26);
+    if (threadIdx.x == 0) DSA_TS(8);
     for (int o = threadIdx.x; o < kAttnRows * cols; o += kAttnThreads) {
       const int row = o % kAttnRows, c = o / kAttnRows;
       float mq[16], lq[16], ov[16];
@@ -639,7 +634,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       }
       if (row < nh) store_out<OUT>(p.out, (out_row + row) * kD + rank * cols + c, O / L);
     }
-    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 20);
+    if (threadIdx.x == 0) DSA_TS(9);
+    DSA_TS_FLUSH(p.status, 2);
     return;
   }
   float* part = p.partial + ((static_cast<size_t>(r) * gridDim.y + gh) * p.nsplit + blockIdx.x) *

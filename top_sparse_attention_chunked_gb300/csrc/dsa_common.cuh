@@ -101,27 +101,38 @@ __device__ __forceinline__ void find_threshold_digit(const uint32_t* h, int nb, 
 }
 
 // ----------------------------------------------------------- phase stamps
-// For latency studies only: compiled with -DDSA_TRACE, a kernel keeps in 64-bit
-// slot `slot` (0..30, at byte 8 of the workspace's status block) the
-// earliest (DSA_TRACE_MIN) or latest (DSA_TRACE_MAX) %globaltimer reading seen
-// at that point of the step. Without the define both expand to nothing.
+// For latency studies only, compiled with -DDSA_TRACE: a kernel keeps per CTA
+// the latest %globaltimer reading at up to 16 points (DSA_TS, from any
+// thread, into shared memory) and at its end thread 0 writes them to
+// buf[((kid * 4096) + cta) * 16 + i], where buf is the device pointer stored
+// at byte 8 of the workspace's status block (null: nothing is written).
+// Nothing reaches global memory before the kernel's end, so the stamps do not
+// delay its barriers. Without the define all three expand to nothing.
 #ifdef DSA_TRACE
 __device__ __forceinline__ unsigned long long trace_now() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-#define DSA_TRACE_MIN(status, slot)                                                           \
-  do {                                                                                        \
-    if (status) atomicMin(reinterpret_cast<unsigned long long*>(status) + 1 + (slot), ::dsa::trace_now()); \
-  } while (0)
-#define DSA_TRACE_MAX(status, slot)                                                           \
-  do {                                                                                        \
-    if (status) atomicMax(reinterpret_cast<unsigned long long*>(status) + 1 + (slot), ::dsa::trace_now()); \
+#define DSA_TS_DECL                                   \
+  __shared__ unsigned long long dsa_ts[16];           \
+  if (threadIdx.x == 0)                               \
+    for (int i_ = 0; i_ < 16; ++i_) dsa_ts[i_] = 0ull
+#define DSA_TS(i) atomicMax(&dsa_ts[i], ::dsa::trace_now())
+#define DSA_TS_FLUSH(status, kid)                                                               \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && (status)) {                                                         \
+      unsigned long long* b_ = *reinterpret_cast<unsigned long long* const*>(                   \
+          reinterpret_cast<const uint8_t*>(status) + 8);                                        \
+      const unsigned c_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);       \
+      if (b_ && c_ < 4096u)                                                                     \
+        for (int i_ = 0; i_ < 16; ++i_) b_[((kid) * 4096u + c_) * 16u + i_] = dsa_ts[i_];     \
+    }                                                                                           \
   } while (0)
 #else
-#define DSA_TRACE_MIN(status, slot) ((void)0)
-#define DSA_TRACE_MAX(status, slot) ((void)0)
+#define DSA_TS_DECL ((void)0)
+#define DSA_TS(i) ((void)0)
+#define DSA_TS_FLUSH(status, kid) ((void)0)
 #endif
 
 }  // namespace dsa

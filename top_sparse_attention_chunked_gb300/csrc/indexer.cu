@@ -162,10 +162,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
   const long long count = u1 - u0;
 
-  if (threadIdx.x == 0) {
-    DSA_TRACE_MIN(p.status, 2);
-    DSA_TRACE_MAX(p.status, 3);
-  }
+  DSA_TS_DECL;
+  if (threadIdx.x == 0) DSA_TS(0);
   // the first block resets the call's device status word (no memset needed)
   if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) *p.status = 0u;
   if (threadIdx.x == 0) {
@@ -275,8 +273,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           pqb = c.qb;
         }
         if (!mbar_wait_bounded(&bars->full[s], round & 1u, abort_flag)) break;
-        if (i == 0) DSA_TRACE_MAX(p.status, 4);
-        if (i == count - 1) DSA_TRACE_MAX(p.status, 5);
+        if (i == 0) DSA_TS(1);
+        if (i == count - 1) DSA_TS(2);
         const int a = static_cast<int>(i % C::NACC);
         if (i >= C::NACC &&
             !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag))
@@ -394,12 +392,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (lane == 0) mbar_arrive(&bars->accempty[a]);
       advance_unit(p, c);
     }
-    if (et == 0) DSA_TRACE_MAX(p.status, 6);
+    if (et == 0) DSA_TS(3);
     if constexpr (HIST) {
       // one query block per CTA here (see the unit ranges above); the global
       // histograms were cleared by the previous kernel of the call
       pdl_wait();
-      if (et == 0) DSA_TRACE_MAX(p.status, 23);
+      if (et == 0) DSA_TS(4);
       named_bar_sync(1, kIdxEpiThreads);
       if (count > 0) {
         for (int j = 0; j < QB; ++j) {
@@ -420,18 +418,21 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
   if (threadIdx.x == 0 && bars->abort_flag) atomicOr(p.status, kDevTimeout);
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 7);
+  if (threadIdx.x == 0) DSA_TS(5);
+  DSA_TS_FLUSH(p.status, 0);
 }
 
 // Clears call scratch (histograms, tickets, counters). It lets the next
 // kernel launch at once; that kernel waits for it only where it needs zeros.
 __global__ void zero_scratch_kernel(uint4* base, long long n16) {
-  if (threadIdx.x == 0) DSA_TRACE_MIN(reinterpret_cast<uint8_t*>(base) - 256, 0);
+  DSA_TS_DECL;
+  if (threadIdx.x == 0) DSA_TS(0);
   pdl_trigger();
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<long long>(gridDim.x) * blockDim.x)
     base[i] = make_uint4(0u, 0u, 0u, 0u);
-  if (threadIdx.x == 0) DSA_TRACE_MAX(reinterpret_cast<uint8_t*>(base) - 256, 1);
+  if (threadIdx.x == 0) DSA_TS(1);
+  DSA_TS_FLUSH(reinterpret_cast<uint8_t*>(base) - 256, 3);
 }
 
 cudaError_t launch_zero_scratch(void* base, size_t bytes, cudaStream_t stream) {

@@ -355,7 +355,10 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
 }
 
 constexpr int kClThreads = 512;
-constexpr int kClGatherMax = 8192;   // candidates gathered into every CTA of the cluster
+// Candidates gathered into every CTA of the cluster: 8,192, or 4,096 for the
+// shortest slices, whose CTAs then fit two to an SM (many short rows, as in
+// grouped decode, run in one wave).
+__host__ __device__ constexpr int cl_gather_max(int per) { return per <= 8 ? 4096 : 8192; }
 
 // Exact threshold over a list of candidate composites held by this CTA:
 // refines (prefix, mask) until `need` candidates are at or above it.
@@ -635,7 +638,7 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
 // shared-memory bank conflicts arise; the threshold-bin candidates go to
 // shared memory.
 template <int PER>
-__global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_select_kernel(const TopkParams p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int kSlice = PER * kClThreads;
@@ -655,12 +658,10 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
   const int rank = static_cast<int>(cluster.block_rank());
   const int ncta = static_cast<int>(cluster.num_blocks());
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    DSA_TRACE_MIN(p.status, 8);
-    DSA_TRACE_MAX(p.status, 21);
-  }
+  DSA_TS_DECL;
+  if (threadIdx.x == 0) DSA_TS(0);
   pdl_wait();      // scores and the histogram come from the previous kernel
-  if (threadIdx.x == 0) DSA_TRACE_MIN(p.status, 9);
+  if (threadIdx.x == 0) DSA_TS(1);
   pdl_trigger();
   const RowInfo ri = row_info(p, r);
   const int t0 = rank * kSlice;
@@ -719,11 +720,11 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 10);
+  if (threadIdx.x == 0) DSA_TS(2);
   // ---- threshold bin: a block-wide scan of the histogram
   find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
                                    &s_above, &s_cnt);
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 11);
+  if (threadIdx.x == 0) DSA_TS(3);
   const uint32_t bin = static_cast<uint32_t>(s_d);
   uint32_t need = static_cast<uint32_t>(ri.keff) - s_above;
   const bool all0 = (need == s_cnt);             // the whole threshold bin is selected
@@ -769,9 +770,9 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
   int32_t* out = p.idx + static_cast<size_t>(r) * p.k;
   // the threshold bin's total (s_cnt) is the same in every CTA: all take the
   // same path
-  const bool gather = all || s_cnt <= static_cast<uint32_t>(kClGatherMax);
+  const bool gather = all || s_cnt <= static_cast<uint32_t>(cl_gather_max(PER));
   cluster.sync();                                // candidates and counts are published
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 12);
+  if (threadIdx.x == 0) DSA_TS(4);
 
   uint32_t pos = 0;                              // this CTA's first output slot
   int off_mine = 0;                              // gathered candidates of lower ranks
@@ -815,7 +816,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
     // this CTA is done reading its peers: arrive now, wait before exiting
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 29);
+    if (threadIdx.x == 0) DSA_TS(5);
     if (!all0)
       resolve_composites<kClThreads>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
                                      &s_cnt, 52);
@@ -857,7 +858,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     }
   }
 
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 13);
+  if (threadIdx.x == 0) DSA_TS(6);
   // ---- selection bits: bins above the threshold bin, or in it with the
   // determined composite bits at or above the threshold prefix; one block
   // scan gives both the in-CTA positions (low half) and, on the gather path,
@@ -886,7 +887,7 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
   }
   uint32_t total;
   const uint32_t packed = block_exclusive_scan<kClThreads>(mine | (lower << 16), warp_tot, &total);
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 30);
+  if (threadIdx.x == 0) DSA_TS(7);
   pos += (packed & 0xFFFFu) + (total >> 16);
   if (!gather) {
     if (threadIdx.x == 0) s_count = total & 0xFFFFu;
@@ -922,7 +923,8 @@ __global__ void __launch_bounds__(kClThreads, 1) topk_cluster_select_kernel(cons
     for (int i = ri.keff + threadIdx.x; i < p.k; i += kClThreads) out[i] = -1;
   if (gather) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   else cluster.sync();                           // peers may still read this CTA's s_count
-  if (threadIdx.x == 0) DSA_TRACE_MAX(p.status, 14);
+  if (threadIdx.x == 0) DSA_TS(8);
+  DSA_TS_FLUSH(p.status, 1);
 }
 
 // Cluster shape for rows of up to max_n keys: keys per thread and CTAs per
@@ -944,7 +946,7 @@ bool topk_cluster_feasible(int max_n) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   const int pi = per == 8 ? 0 : per == 16 ? 1 : 2;
   if (cached[dev][pi]) return cached[dev][pi] == 1;
-  const size_t smem = (static_cast<size_t>(per) * kClThreads + kClGatherMax) * sizeof(unsigned long long);
+  const size_t smem = (static_cast<size_t>(per) * kClThreads + cl_gather_max(per)) * sizeof(unsigned long long);
   auto kern = per == 8 ? topk_cluster_select_kernel<8>
             : per == 16 ? topk_cluster_select_kernel<16> : topk_cluster_select_kernel<32>;
   bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -983,7 +985,7 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   cluster_shape(max_n, &per, &ctas);
   if (ctas == 0) return cudaErrorInvalidValue;
   // worst case every key of the slice is a candidate; then the gathered list
-  const size_t smem = (static_cast<size_t>(per) * kClThreads + kClGatherMax) * sizeof(unsigned long long);
+  const size_t smem = (static_cast<size_t>(per) * kClThreads + cl_gather_max(per)) * sizeof(unsigned long long);
   auto kern = per == 8 ? topk_cluster_select_kernel<8>
             : per == 16 ? topk_cluster_select_kernel<16> : topk_cluster_select_kernel<32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,

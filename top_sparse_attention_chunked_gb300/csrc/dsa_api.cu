@@ -452,6 +452,13 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
   tp.nrows = d.rows;
   cudaError_t e;
   const int row_max = topk_row_max_len(di.smem_optin);
+  if (!hist_ready && prefer_rows && d.max_n <= topk_row_stream_max_len()) {
+    timing_before(DSA_KERNEL_TOPK_ROW, st);
+    e = launch_topk_row_stream(tp, d.max_n, after_kernel, st);
+    timing_after(DSA_KERNEL_TOPK_ROW, st);
+    if (e != cudaSuccess) return cuda_fail(e, "top-k row launch");
+    return DSA_OK;
+  }
   if (!hist_ready && prefer_rows && d.max_n <= row_max) {
     timing_before(DSA_KERNEL_TOPK_ROW, st);
     if (topk_row_reg_per(d.max_n) > 0)
@@ -616,7 +623,8 @@ int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, con
   // top-k needs its histograms, tickets and counters cleared, the split-K
   // attention outside a cluster its tickets. Otherwise nothing is cleared
   // (the indexer resets the status word itself).
-  const bool topk_rows = !decode && d.max_n <= topk_row_max_len(di.smem_optin);
+  const bool topk_rows = !decode && (d.max_n <= topk_row_stream_max_len() ||
+                                     d.max_n <= topk_row_max_len(di.smem_optin));
   // decode: the indexer epilogue builds the top-k's row histograms
   const bool hist_in_indexer = decode;
   int split_keys = 0, nsplit = 1;

@@ -137,6 +137,10 @@ constexpr int kTopkClusterMax = 16;
 int topk_cluster_ctas(int max_n);   // 0 if the row is too long for it
 cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
                                        cudaStream_t stream);
+// Streaming whole-row select (one CTA per row, several rows per SM): rows of
+// up to topk_row_stream_max_len() keys; needs no zeroed scratch.
+int topk_row_stream_max_len();
+cudaError_t launch_topk_row_stream(const TopkParams& p, int max_n, bool pdl, cudaStream_t stream);
 // Whole-row select with the keys in registers: keys per thread for rows of
 // up to max_n keys (0 if too long).
 int topk_row_reg_per(int max_n);

@@ -585,6 +585,362 @@ __global__ void __launch_bounds__(kRrThreads, 1) topk_row_reg_kernel(const TopkP
   for (int i = keff + threadIdx.x; i < p.k; i += kRrThreads) out[i] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// 3c. streaming whole-row select (many rows: prefill). One CTA of 512 threads
+// per row keeps no keys in registers:
+//   1. a sample of the row (every 16th 128-byte line, so no extra DRAM
+//      sectors) gives a provisional threshold theta a little below the k-th
+//      key: its share of keff plus 25 % and 16 keys of slack, resolved on 22
+//      key bits of the sample;
+//   2. one pass over the row lists the keys at or above theta (composites
+//      key << 32 | ~index) in shared memory -- its reads of the sampled lines
+//      hit L2;
+//   3. the exact keff-th composite among the listed keys is resolved in
+//      11-bit rounds (equal keys go to the lower index) and the selected ones
+//      are marked in a bitmap of the row in shared memory;
+//   4. the bitmap is emitted in index order.
+// If the sample misleads (fewer than keff keys at or above theta, or more
+// than kRsCandMax), an exact path takes over: a histogram of the row's top 11
+// key bits, a pass that marks the keys above the threshold bin and lists the
+// bin's keys, and the same resolve (for a bin of more than kRsCandMax keys,
+// rounds that re-read the row). With ~40 KB of shared memory and few
+// registers several rows are in flight per SM, so one row's reads overlap
+// another's resolve.
+// ---------------------------------------------------------------------------
+constexpr int kRsThreads = 512;
+constexpr int kRsCandMax = 4096;
+constexpr int kRsMaxLen = 262144;
+#ifndef RS_UNROLL
+#define RS_UNROLL 4
+#endif
+
+// Exact threshold among n listed composites whose bits above `hi` are fixed by
+// (prefix, mask): refines 11 bits a round until `need` composites are at or
+// above the prefix; returns the prefix (zero below its determined bits).
+__device__ unsigned long long rs_resolve(const unsigned long long* list, uint32_t n, uint32_t need,
+                                         unsigned long long prefix, unsigned long long mask, int hi,
+                                         uint32_t* h, uint32_t* warp_tot, int* sd, uint32_t* sabove,
+                                         uint32_t* scnt) {
+  bool all = false;
+  while (!all && hi >= 0) {
+    const int w = hi + 1 < 11 ? hi + 1 : 11;
+    const int sh = hi - w + 1;
+    const uint32_t dm = (1u << w) - 1u;
+    for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
+    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < n; i += kRsThreads) {
+      const unsigned long long cc = list[i];
+      if ((cc & mask) == prefix) atomicAdd(&h[static_cast<uint32_t>(cc >> sh) & dm], 1u);
+    }
+    __syncthreads();
+    find_threshold_digit<kRsThreads>(h, 1 << w, need, warp_tot, sd, sabove, scnt);
+    need -= *sabove;
+    prefix |= static_cast<unsigned long long>(*sd) << sh;
+    mask |= static_cast<unsigned long long>(dm) << sh;
+    all = (*scnt == need);
+    hi -= w;
+  }
+  return prefix;
+}
+
+__global__ void __launch_bounds__(kRsThreads) topk_row_stream_kernel(const TopkParams p) {
+  extern __shared__ uint32_t rs_bm[];                  // [ceil(n / 32)] selection bits
+  __shared__ unsigned long long rs_c[kRsCandMax];      // listed composites
+  __shared__ __align__(16) uint32_t h[kHistBins];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ int s_d;
+  __shared__ uint32_t s_above, s_cnt, s_nc;
+  const int rl = blockIdx.x, r = p.row0 + rl;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kWarps = kRsThreads / 32;
+  DSA_TS_DECL;
+  if (threadIdx.x == 0) DSA_TS(0);
+  pdl_wait();      // scores come from the previous kernel
+  if (threadIdx.x == 0) DSA_TS(1);
+  pdl_trigger();
+  const RowInfo ri = row_info(p, r);
+  const int n = ri.n, keff = ri.keff;
+  const int nw = (n + 31) >> 5;
+  const float* row = p.scores + static_cast<size_t>(r) * p.cap;
+  if (threadIdx.x < 32) {
+    // the whole row into L2 at once (the 16-byte-aligned part of it, in
+    // 16 KB pieces): the passes below then read at L2 latency
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(row) + 15) & ~uintptr_t(15);
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(row + n) & ~uintptr_t(15);
+    for (uintptr_t a = a0 + static_cast<uintptr_t>(threadIdx.x) * 16384u; a < a1; a += 32u * 16384u)
+      prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(a1 - a < 16384u ? a1 - a : 16384u));
+  }
+  for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
+  for (int i = threadIdx.x; i < nw; i += kRsThreads) rs_bm[i] = 0u;
+  if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; s_nc = 0; }
+  __syncthreads();
+  constexpr int U = RS_UNROLL;                         // loads in flight per thread
+  auto composite = [](uint32_t k, int t) {
+    return (static_cast<unsigned long long>(k) << 32) | (0xFFFFFFFFull - static_cast<uint32_t>(t));
+  };
+
+  // ---- 1. provisional threshold from every 16th line (warp w reads lines
+  // 16 (w + kWarps j), lane l key l of the line); the first kRsSmpReg sampled
+  // keys stay in registers for the second level
+  constexpr int kRsSmpReg = 8;
+  uint32_t ks[kRsSmpReg];
+  uint32_t nsmp = 0;
+  const int nlines = nw;
+  {
+#pragma unroll
+    for (int j = 0; j < kRsSmpReg; ++j) {
+      const int t = 32 * 16 * (warp + kWarps * j) + lane;
+      ks[j] = t < n ? float_key(__ldcg(row + t)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kRsSmpReg; ++j) {
+      const int t = 32 * 16 * (warp + kWarps * j) + lane;
+      if (t < n) {
+        atomicAdd(&h[ks[j] >> (32 - kHistBits)], 1u);
+        ++nsmp;
+      }
+    }
+    for (int j = kRsSmpReg; 16 * (warp + kWarps * j) < nlines; ++j) {
+      const int t = 32 * 16 * (warp + kWarps * j) + lane;
+      if (t < n) {
+        atomicAdd(&h[float_key(__ldcg(row + t)) >> (32 - kHistBits)], 1u);
+        ++nsmp;
+      }
+    }
+  }
+  uint32_t ns;
+  block_exclusive_scan<kRsThreads>(nsmp, warp_tot, &ns);
+  uint32_t rs = static_cast<uint32_t>((static_cast<unsigned long long>(keff) * ns * 5 + 4ull * n - 1) /
+                                      (4ull * n)) + 16u;
+  if (rs > ns) rs = ns;
+  uint32_t theta = 0;
+  if (rs > 0) {
+    find_threshold_digit<kRsThreads>(h, kHistBins, rs, warp_tot, &s_d, &s_above, &s_cnt);
+    const uint32_t sb = static_cast<uint32_t>(s_d);
+    const uint32_t need2 = rs - s_above;
+    for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRsSmpReg; ++j) {
+      const int t = 32 * 16 * (warp + kWarps * j) + lane;
+      if (t < n && (ks[j] >> (32 - kHistBits)) == sb)
+        atomicAdd(&h[(ks[j] >> (32 - 2 * kHistBits)) & (kHistBins - 1)], 1u);
+    }
+    for (int j = kRsSmpReg; 16 * (warp + kWarps * j) < nlines; ++j) {
+      const int t = 32 * 16 * (warp + kWarps * j) + lane;
+      if (t < n) {
+        const uint32_t k = float_key(__ldcg(row + t));   // an L2 hit: read just above
+        if ((k >> (32 - kHistBits)) == sb) atomicAdd(&h[(k >> (32 - 2 * kHistBits)) & (kHistBins - 1)], 1u);
+      }
+    }
+    __syncthreads();
+    find_threshold_digit<kRsThreads>(h, kHistBins, need2, warp_tot, &s_d, &s_above, &s_cnt);
+    theta = (sb << (32 - kHistBits)) | (static_cast<uint32_t>(s_d) << (32 - 2 * kHistBits));
+  }
+  if (threadIdx.x == 0) DSA_TS(2);
+
+  // ---- 2. the keys at or above theta into the list: warp w appends to its
+  // own region [w * kRsWarpCand, (w + 1) * kRsWarpCand) (count in a register);
+  // the next batch's loads are issued before the current batch is examined
+  constexpr int kRsWarpCand = kRsCandMax / kWarps;
+  unsigned long long* wlist = rs_c + warp * kRsWarpCand;
+  uint32_t wcount = 0;
+  {
+    uint32_t k[U], kn[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = u * kRsThreads + threadIdx.x;
+      k[u] = t < n ? float_key(__ldcg(row + t)) : 0u;
+    }
+    for (int base = 0; base < n; base += U * kRsThreads) {
+      const int nb = base + U * kRsThreads;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = nb + u * kRsThreads + threadIdx.x;
+        kn[u] = t < n ? float_key(__ldcg(row + t)) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = base + u * kRsThreads + threadIdx.x;
+        const bool cand = t < n && k[u] >= theta;
+        const uint32_t cb = __ballot_sync(0xffffffffu, cand);
+        const uint32_t at = wcount + __popc(cb & ((1u << lane) - 1u));
+        if (cand && at < static_cast<uint32_t>(kRsWarpCand)) wlist[at] = composite(k[u], t);
+        wcount += __popc(cb);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) k[u] = kn[u];
+    }
+  }
+  if (lane == 0) atomicAdd(&s_nc, wcount);
+  __syncthreads();
+  if (threadIdx.x == 0) DSA_TS(3);
+  const uint32_t nc = s_nc;
+  // every warp region held its keys; then keys that are not listed are below theta
+  const bool fits = __syncthreads_and(wcount <= static_cast<uint32_t>(kRsWarpCand));
+  if (fits && nc >= static_cast<uint32_t>(keff)) {
+    // ---- 3. compact the regions, resolve the exact threshold among the
+    // listed keys and mark those at or above it
+    __shared__ uint32_t s_wc[kWarps];
+    if (lane == 0) s_wc[warp] = wcount;
+    __syncthreads();
+    uint32_t off = 0;
+    for (int w = 0; w < warp; ++w) off += s_wc[w];
+    // move regions left in order: region w lands at off >= w * kRsWarpCand
+    // never below; copy through registers one warp at a time
+    for (int w = 1; w < kWarps; ++w) {
+      if (warp == w) {
+        // batches of 32 (wcount is the same in every lane), every lane in
+        // every batch: the reads of a batch land before its writes
+        for (uint32_t i0 = 0; i0 < wcount; i0 += 32) {
+          const uint32_t i = i0 + lane;
+          const unsigned long long v = i < wcount ? wlist[i] : 0ull;
+          __syncwarp();
+          if (i < wcount) rs_c[off + i] = v;
+          __syncwarp();
+        }
+      }
+      __syncthreads();
+    }
+    const unsigned long long T = rs_resolve(rs_c, nc, static_cast<uint32_t>(keff), 0ull, 0ull, 63, h,
+                                            warp_tot, &s_d, &s_above, &s_cnt);
+    if (threadIdx.x == 0) DSA_TS(4);
+    for (uint32_t i = threadIdx.x; i < nc; i += kRsThreads) {
+      const unsigned long long cc = rs_c[i];
+      if (cc >= T) {
+        const uint32_t t = 0xFFFFFFFFu - static_cast<uint32_t>(cc & 0xFFFFFFFFull);
+        atomicOr(&rs_bm[t >> 5], 1u << (t & 31));
+      }
+    }
+  } else {
+    // ---- the sample misled: exact path. Histogram of the row's top 11 bits,
+    for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; s_nc = 0; }
+    __syncthreads();
+    for (int base = 0; base < n; base += kRsThreads) {
+      const int t = base + threadIdx.x;
+      hist_add_warp(h, t < n ? float_key(__ldcg(row + t)) >> (32 - kHistBits) : 0xFFFFFFFFu);
+    }
+    __syncthreads();
+    find_threshold_digit<kRsThreads>(h, kHistBins, static_cast<uint32_t>(keff), warp_tot, &s_d,
+                                     &s_above, &s_cnt);
+    const uint32_t b1 = static_cast<uint32_t>(s_d);
+    const uint32_t need = static_cast<uint32_t>(keff) - s_above;
+    const uint32_t n1 = s_cnt;
+    const uint32_t lo1 = b1 << (32 - kHistBits);
+    const uint32_t hi1 = lo1 + (1u << (32 - kHistBits)) - 1u;
+    const bool listed = n1 <= static_cast<uint32_t>(kRsCandMax);
+    // keys above bin b1 into the bitmap (warp w of a round: one word), the
+    // bin's keys into the list
+    for (int base = 0; base < n; base += kRsThreads) {
+      const int t = base + threadIdx.x;
+      const uint32_t k = t < n ? float_key(__ldcg(row + t)) : 0u;
+      const uint32_t word = __ballot_sync(0xffffffffu, t < n && k > hi1);
+      if (lane == 0 && t < n) rs_bm[t >> 5] = word;
+      if (listed) {
+        const bool cand = t < n && k >= lo1 && k <= hi1;
+        const uint32_t cb = __ballot_sync(0xffffffffu, cand);
+        if (cb) {
+          uint32_t slot = 0;
+          if (lane == 0) slot = atomicAdd(&s_nc, static_cast<uint32_t>(__popc(cb)));
+          slot = __shfl_sync(0xffffffffu, slot, 0);
+          if (cand) rs_c[slot + __popc(cb & ((1u << lane) - 1u))] = composite(k, t);
+        }
+      }
+    }
+    __syncthreads();
+    unsigned long long T = static_cast<unsigned long long>(b1) << 53;   // need == n1: the whole bin
+    if (need < n1) {
+      if (listed) {
+        T = rs_resolve(rs_c, n1, need, T, ~0ull << 53, 52, h, warp_tot, &s_d, &s_above, &s_cnt);
+      } else {
+        // a heavy tie: rounds that re-read the row
+        unsigned long long mask = ~0ull << 53;
+        uint32_t nd = need;
+        bool all = false;
+        int hi = 52;
+        while (!all && hi >= 0) {
+          const int w = hi + 1 < 11 ? hi + 1 : 11;
+          const int sh = hi - w + 1;
+          const uint32_t dm = (1u << w) - 1u;
+          for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
+          if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+          __syncthreads();
+          for (int base = 0; base < n; base += kRsThreads) {
+            const int t = base + threadIdx.x;
+            uint32_t dg = 0xFFFFFFFFu;
+            if (t < n) {
+              const unsigned long long cc = composite(float_key(__ldcg(row + t)), t);
+              if ((cc & mask) == T) dg = static_cast<uint32_t>(cc >> sh) & dm;
+            }
+            hist_add_warp(h, dg);
+          }
+          __syncthreads();
+          find_threshold_digit<kRsThreads>(h, 1 << w, nd, warp_tot, &s_d, &s_above, &s_cnt);
+          nd -= s_above;
+          T |= static_cast<unsigned long long>(s_d) << sh;
+          mask |= static_cast<unsigned long long>(dm) << sh;
+          all = (s_cnt == nd);
+          hi -= w;
+        }
+      }
+    }
+    if (listed) {
+      for (uint32_t i = threadIdx.x; i < n1; i += kRsThreads) {
+        const unsigned long long cc = rs_c[i];
+        if (cc >= T) {
+          const uint32_t t = 0xFFFFFFFFu - static_cast<uint32_t>(cc & 0xFFFFFFFFull);
+          atomicOr(&rs_bm[t >> 5], 1u << (t & 31));
+        }
+      }
+    } else {
+      for (int t = threadIdx.x; t < n; t += kRsThreads) {
+        const uint32_t k = float_key(__ldcg(row + t));
+        if (k >= lo1 && k <= hi1 && composite(k, t) >= T) atomicOr(&rs_bm[t >> 5], 1u << (t & 31));
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) DSA_TS(5);
+  // ---- 4. emit in index order: thread i owns words [i * wpt, (i + 1) * wpt)
+  const int wpt = (nw + kRsThreads - 1) / kRsThreads;
+  const int w0 = threadIdx.x * wpt;
+  uint32_t cnt = 0;
+  for (int j = 0; j < wpt; ++j)
+    if (w0 + j < nw) cnt += __popc(rs_bm[w0 + j]);
+  uint32_t tot;
+  uint32_t pos = block_exclusive_scan<kRsThreads>(cnt, warp_tot, &tot);
+  int32_t* out = p.idx + static_cast<size_t>(r) * p.k;
+  for (int j = 0; j < wpt; ++j) {
+    if (w0 + j >= nw) break;
+    uint32_t bits = rs_bm[w0 + j];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (pos < static_cast<uint32_t>(keff)) out[pos] = (w0 + j) * 32 + b;
+      ++pos;
+    }
+  }
+  for (int i = keff + threadIdx.x; i < p.k; i += kRsThreads) out[i] = -1;
+  if (threadIdx.x == 0) DSA_TS(6);
+  DSA_TS_FLUSH(p.status, 1);
+}
+
+int topk_row_stream_max_len() { return kRsMaxLen; }
+
+cudaError_t launch_topk_row_stream(const TopkParams& p, int max_n, bool pdl, cudaStream_t stream) {
+  if (max_n > kRsMaxLen) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>((max_n + 31) / 32) * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(topk_row_stream_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_kernel("topk_row_stream_kernel", topk_row_stream_kernel, dim3(p.nrows),
+                       dim3(kRsThreads), smem, stream, pdl, p);
+}
+
 int topk_row_reg_per(int max_n) {
   const int per = (max_n + kRrThreads - 1) / kRrThreads;
   const int per16 = ((per + 15) / 16) * 16;

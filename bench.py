@@ -15,6 +15,13 @@ memory and its output copied back. Under torchrun every rank runs its own
 replica of the workload (the path shards by sequence with no exchange:
 weak scaling); the slowest rank's time is reported.
 
+By default the run also measures, in the same process and the same way, the
+other four workloads (decode_4k, grouped_decode_32k, prefill_8k_on_32k,
+decode_256k_int8) and reports each under "configs" with its own step time,
+throughput, e2e, roofline (prefill: the indexer and the attention against the
+bf16 tensor peak, with the attention's gather rate), per-kernel split, CPU
+oracle baseline and clocks (--no-all-configs: the named workload only).
+
 --op append times dsa_cache_append alone (the cache write before the step) on
 the workload's shape and reports its HBM GB/s; --op rope does the same for
 dsa_rmsnorm_rotary on the workload's query and key heads.
@@ -56,12 +63,12 @@ def peaks():
 # profiles/). They hold for the indexer source they were taken on: when any of
 # these files changes, the figure is dropped (null) until it is measured again.
 TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh", "dsa_internal.h"]
-TRAFFIC_SOURCE_SHA = "638f37ae5c0ec876"
+TRAFFIC_SOURCE_SHA = "50175b152edd17f4"
 INDEXER_TRAFFIC = {
-    "decode_4k": 572672,
-    "grouped_decode_32k": 16906496,
+    "decode_4k": 573184,
+    "grouped_decode_32k": 16906240,
     "decode_128k": 16826112,
-    "decode_256k_int8": 33628672,
+    "decode_256k_int8": 33627392,
 }
 
 
@@ -294,24 +301,34 @@ def whole_job_value(world, query_tokens, ms):
 
 
 # ------------------------------------------------------------------ libdsa arm
-def run_libdsa(args, wl):
+# The four workloads reported beside the headline (decode_128k) in the same
+# JSON line, under "configs".
+OTHER_WORKLOADS = ["decode_4k", "grouped_decode_32k", "prefill_8k_on_32k", "decode_256k_int8"]
+
+
+def attention_flops_bytes(wl, idx_np):
+    """Prefill attention's algorithmic work: 2 * 2 * Hq * 128 flop (QK^T and
+    PV) per (query row, selected key), and its gather traffic (the selected K
+    and V rows of every query row, Hkv * 128 16-bit values each)."""
+    import numpy as np
+    sel = int((idx_np >= 0).sum())
+    flops = sel * 2 * 2 * wl.num_q_heads * 128
+    elem = 1 if wl.kv_dtype == "int8" else 2
+    gather = sel * wl.num_kv_heads * 128 * elem * 2
+    return flops, gather
+
+
+def measure_workload(args, wl, world, rank, dev_index, cpu_budget):
+    """One workload: the graph-replayed step (L2 flushed before each), the
+    roofline of its dominant kernels, the per-kernel split, the end-to-end
+    call with host copies and (rank 0, N = 1) the CPU oracle. Returns the
+    fields of its JSON entry."""
     import numpy as np
     import torch
     import torch.distributed as dist
 
     from dsa_inputs import make_inputs
-    from top_sparse_attention_chunked_gb300 import build_lib
     from top_sparse_attention_chunked_gb300 import dsa as D
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    build_lib.build()
-    D.load_library()
-    dev_index = torch.cuda.current_device()
 
     cpu = make_inputs(wl, seed=replica_seed(wl, rank))   # an independent replica per rank
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
@@ -341,16 +358,6 @@ def run_libdsa(args, wl):
         call(p, dev["q"], dev["qI"], dev["w"], caches["kI"], caches["k"], caches["v"],
              caches["k_scale"], caches["v_scale"], idx, out, ws, pages=pages)
 
-    if args.profile_calls:
-        # untimed calls only, for an ncu capture of the step's kernels
-        for _ in range(args.profile_calls):
-            step()
-        torch.cuda.synchronize()
-        assert D.dsa_read_device_status(ws) == 0
-        if rank == 0:
-            print(json.dumps({"profile_calls": args.profile_calls, "workload": wl.name,
-                              "kernels_per_step": D.dsa_last_launches()}), flush=True)
-        return
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -381,7 +388,8 @@ def run_libdsa(args, wl):
 
     def timed_loop(kernel_timing):
         """K steps, L2 flushed before each, CUDA events on the launching stream
-        around every step (and, with kernel_timing, around the indexer launch)."""
+        around every step (and, with kernel_timing, the library's events
+        around one kernel launch)."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         kern_ms = []
@@ -410,11 +418,18 @@ def run_libdsa(args, wl):
     step_ms, _ = timed_loop(False)
     clk = clocks.stop()
     ms = slowest_rank_ms(statistics.mean(step_ms), world, device="cuda")
-    # the roofline loop: same steps with events recorded around the indexer
+    # the roofline loops: the same steps with events recorded around the
+    # indexer launch (and, for prefill, around the attention launch)
     D.dsa_timing_select(D.DSA_KERNEL_INDEXER)
     graph = capture() if args.graph else None
     step_ms_t, idx_ms = timed_loop(True)
+    attn_ms = []
+    if prefill:
+        D.dsa_timing_select(D.DSA_KERNEL_ATTENTION)
+        graph = capture() if args.graph else None
+        _, attn_ms = timed_loop(True)
     D.dsa_timing_select(-1)
+    graph = None
     idx_np = idx.cpu().numpy()
     ab = algorithmic_bytes(wl, idx_np)
     hbm, bf16, peak_kind = peaks()
@@ -465,12 +480,14 @@ def run_libdsa(args, wl):
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu_base = None
     if rank == 0 and world == 1:
-        times, ntok = oracle_step_time(wl, cpu, budget_s=args.cpu_budget)
+        times, ntok = oracle_step_time(wl, cpu, budget_s=cpu_budget)
         what = (f"{ntok} sampled query rows of" if ntok < wl.query_tokens else "full")
         cpu_base = {"value": ntok / statistics.mean(times), "unit": UNIT,
                     "cores": cores(), "kind": "oracle",
                     "sample": f"{len(times)} x {what} {wl.name} step ({ntok} query "
                               f"token(s) each) in float64 NumPy"}
+        if ntok < wl.query_tokens:
+            cpu_base["extrapolated_step_s"] = round(statistics.mean(times) * wl.query_tokens / ntok, 3)
 
     idx_us = 1e3 * statistics.mean(idx_ms)
     step_gbs = ab["step"] / (ms * 1e-3) / 1e9
@@ -481,39 +498,114 @@ def run_libdsa(args, wl):
         roof = {"kernel": "indexer_tc_kernel", "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": bf16, "unit": "TFLOP/s", "frac": round(achieved / bf16, 4),
                 "peak_kind": peak_kind, "traffic": None, "algorithmic_flops": flops,
-                "launch_us": round(idx_us, 2)}
+                "launch_us_events": round(idx_us, 2)}
+        attn_us = 1e3 * statistics.mean(attn_ms)
+        aflops, gbytes = attention_flops_bytes(wl, idx_np)
+        a_tf = aflops / (attn_us * 1e-6) / 1e12
+        roof_attn = {"kernel": "sparse_attn_prefill_tc_kernel", "bound": "tensor",
+                     "achieved": round(a_tf, 1), "peak": bf16, "unit": "TFLOP/s",
+                     "frac": round(a_tf / bf16, 4), "peak_kind": peak_kind,
+                     "algorithmic_flops": aflops, "launch_us_events": round(attn_us, 2),
+                     # the selected rows are gathered from the L2-resident cache:
+                     # the rate it moves them at is the kernel's practical bound
+                     "gather_bytes": gbytes,
+                     "gather_gbs": round(gbytes / (attn_us * 1e-6) / 1e9, 1)}
     else:
         achieved = ab["indexer"] / (idx_us * 1e-6) / 1e9
         roof = {"kernel": "indexer_tc_kernel", "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_kind": peak_kind, "traffic": indexer_traffic(wl.name),
                 "algorithmic_bytes": ab["indexer"],
-                "launch_us": round(idx_us, 2)}
+                # events around the launch inside the graph break its overlap with
+                # the kernel before it, so this time includes that gap
+                "launch_us_events": round(idx_us, 2)}
+        roof_attn = None
+    res = {
+        "ms_per_step": ms, "value": value,
+        "config": dict(config_of(wl, args.graph),
+                       **({"paged": {"block_size": args.paged, "num_blocks": pages.num_blocks}}
+                          if pages is not None else {})),
+        "hbm_gbs_step": round(step_gbs, 1),
+        "hbm_frac_step": round(step_gbs / hbm, 4),
+        "hbm_frac_step_of_8tbs": round(step_gbs / 8000.0, 4),
+        "algorithmic_bytes_step": ab["step"],
+        "roofline": roof,
+        "per_kernel_us": per_kernel,
+        "ms_per_step_with_indexer_events": statistics.mean(step_ms_t),
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+        # the library's own count of the kernels one call enqueues, times the
+        # timed steps of the headline loop
+        "gpu_launches": len(kernels_per_step) * args.steps,
+        "kernels_per_step": kernels_per_step,
+        "clocks": clk,
+    }
+    if roof_attn is not None:
+        res["roofline_attention"] = roof_attn
+    del dev, caches, ws, out, idx, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_libdsa(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    from dsa_inputs import WORKLOADS, make_inputs
+    from top_sparse_attention_chunked_gb300 import build_lib
+    from top_sparse_attention_chunked_gb300 import dsa as D
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build_lib.build()
+    D.load_library()
+    dev_index = torch.cuda.current_device()
+
+    if args.profile_calls:
+        # untimed calls only, for an ncu capture of the step's kernels
+        cpu = make_inputs(wl, seed=replica_seed(wl, rank))
+        dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+        p = D.problem_for(wl)
+        ws = D.alloc_workspace(p, D.DSA_OP_PREFILL if wl.q_len > 16 else D.DSA_OP_DECODE)
+        out = torch.empty(wl.batch, wl.q_len, wl.num_q_heads, 128, dtype=D._TORCH_DT[p.out_dtype],
+                          device="cuda")
+        idx = torch.empty(wl.batch, wl.q_len, wl.top_k, dtype=torch.int32, device="cuda")
+        call = D.dsa_sparse_attn_prefill if wl.q_len > 16 else D.dsa_sparse_attn_decode
+        for _ in range(args.profile_calls):
+            call(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"],
+                 dev["k_scale"], dev["v_scale"], idx, out, ws)
+        torch.cuda.synchronize()
+        assert D.dsa_read_device_status(ws) == 0
+        if rank == 0:
+            print(json.dumps({"profile_calls": args.profile_calls, "workload": wl.name,
+                              "kernels_per_step": D.dsa_last_launches()}), flush=True)
+        return
+
+    head = measure_workload(args, wl, world, rank, dev_index, args.cpu_budget)
+    others = {}
+    if args.all_configs:
+        for name in OTHER_WORKLOADS:
+            if name == wl.name:
+                continue
+            r = measure_workload(args, WORKLOADS[name], world, rank, dev_index,
+                                 min(args.cpu_budget, 5.0))
+            others[name] = r
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic (seeded N(0,1) / U(0,1) tensors, see dsa_inputs.py)",
-            "config": dict(config_of(wl, graph is not None),
-                           **({"paged": {"block_size": args.paged, "num_blocks": pages.num_blocks}}
-                              if pages is not None else {})),
-            "hbm_gbs_step": round(step_gbs, 1),
-            "hbm_frac_step": round(step_gbs / hbm, 4),
-            "hbm_frac_step_of_8tbs": round(step_gbs / 8000.0, 4),
-            "algorithmic_bytes_step": ab["step"],
-            "roofline": roof,
-            "per_kernel_us": per_kernel,
-            "ms_per_step_with_indexer_events": statistics.mean(step_ms_t),
-            "cpu_baseline": cpu_base,
-            "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
-            # the library's own count of the kernels one call enqueues, times
-            # the timed steps of the headline loop
-            "gpu_launches": len(kernels_per_step) * args.steps,
-            "kernels_per_step": kernels_per_step,
-            "clocks": clk,
-        }
+        line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16",
+                "data": "synthetic (seeded N(0,1) / U(0,1) tensors, see dsa_inputs.py)"}
+        line.update({k: v for k, v in head.items() if k not in ("value", "ms_per_step")})
+        # every launch of the measured runs counts, the other workloads' included
+        line["gpu_launches"] = head["gpu_launches"] + sum(r["gpu_launches"] for r in others.values())
+        if others:
+            line["configs"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -819,6 +911,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="libdsa", choices=["libdsa", "reference"])
     ap.add_argument("--workload", default="decode_128k")
+    ap.add_argument("--no-all-configs", dest="all_configs", action="store_false",
+                    help="measure only --workload (by default the headline run also measures "
+                         "the other four workloads and reports them under \"configs\")")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--profile-calls", type=int, default=0,
@@ -837,6 +932,8 @@ def main():
     ap.add_argument("--context", type=int, default=0,
                     help="with --profile-calls: cache length of a reduced case")
     args = ap.parse_args()
+    if args.workload != "decode_128k" or args.paged:
+        args.all_configs = False
     if args.warmup < 3:
         args.warmup = 3
     from dsa_inputs import WORKLOADS

@@ -57,6 +57,16 @@ R13 RMSNorm + rotary embedding (PR #33997 Description item 1, the exact FP32
     out_{i+r/2} = y_{i+r/2} cos[p,i] + y_i sin[p,i]; dims r..D-1 stay y.
     Computed here exactly (float64); the library computes in fp32 and rounds
     once to the output type.
+R14 floating auxiliary K/V (PR #33997: the op takes the step's own key and
+    value as inputs beside the caches; its review notes that grouped attention
+    can overflow BF16 auxiliary values when converting them to an FP16 cache's
+    type, and the fix keeps floating auxiliary K/V with FP16 main caches): the
+    S new tokens' K and V may be given as separate tensors k_aux, v_aux
+    [B, S, Hkv, D] in the query's floating type. A selected key t of
+    sequence b with t >= T_b - S (a new token, R1) then reads
+    k_aux[b, t - (T_b - S)] and v_aux[...] at their own values -- never
+    converted to the cache's type -- and every other selected key reads the
+    cache. The indexer and the selection are unchanged.
 
 Parity pins for every function live in tests/test_oracle_pins.py.
 """
@@ -191,6 +201,37 @@ def sparse_attention(q, k, v, idx, num_kv_heads: int, k_scale=None,
         sel = sel[sel >= 0]
         Kb = dequantize(k[b, sel], None if k_scale is None else k_scale[b, sel])
         Vb = dequantize(v[b, sel], None if v_scale is None else v_scale[b, sel])
+        for h in range(Hq):
+            g = h // G
+            out[b, s, h] = attend_row(q[b, s, h], Kb[:, g], Vb[:, g], scale)
+    return out
+
+
+def sparse_attention_aux(q, k, v, idx, num_kv_heads: int, k_aux, v_aux, total_len,
+                         k_scale=None, v_scale=None, softmax_scale: float = 0.0,
+                         rows=None) -> np.ndarray:
+    """Sparse attention with floating auxiliary K/V for the new tokens (R14).
+
+    As sparse_attention, except that a selected key t of sequence b with
+    t >= T_b - S takes its K and V from k_aux / v_aux [B,S,Hkv,D] at row
+    t - (T_b - S), as the values given (no conversion to the cache type).
+    Returns float64 [B,S,Hq,D] (rows not in ``rows`` stay NaN).
+    """
+    B, S, Hq, D = q.shape
+    G = Hq // num_kv_heads
+    scale = softmax_scale if softmax_scale else 1.0 / np.sqrt(D)
+    out = np.full(q.shape, np.nan)
+    todo = rows if rows is not None else [(b, s) for b in range(B) for s in range(S)]
+    for b, s in todo:
+        past = int(total_len[b]) - S          # the first new token's position
+        sel = idx[b, s]
+        sel = sel[sel >= 0]
+        Kb = dequantize(k[b, sel], None if k_scale is None else k_scale[b, sel])
+        Vb = dequantize(v[b, sel], None if v_scale is None else v_scale[b, sel])
+        for j, t in enumerate(sel):
+            if t >= past:
+                Kb[j] = k_aux[b, t - past]
+                Vb[j] = v_aux[b, t - past]
         for h in range(Hq):
             g = h // G
             out[b, s, h] = attend_row(q[b, s, h], Kb[:, g], Vb[:, g], scale)

@@ -509,6 +509,79 @@ def test_rope_scale_invariance():
 
 
 # ---------------------------------------------------------------------------
+# floating auxiliary K/V (R14)
+# ---------------------------------------------------------------------------
+def _aux_case(case):
+    f = lambda rows: np.array([[_num(x) for x in r] for r in rows], dtype=np.float64)
+    T, S = case["total_len"], case["q_len"]
+    q = f(case["q"]).reshape(1, S, 1, -1)
+    k = f(case["k_cache"]).reshape(1, T, 1, -1)
+    v = f(case["v_cache"]).reshape(1, T, 1, -1)
+    ka = f(case["k_aux"]).reshape(1, S, 1, -1)
+    va = f(case["v_aux"]).reshape(1, S, 1, -1)
+    if "idx_rows" in case:
+        idx = np.array(case["idx_rows"], dtype=np.int64).reshape(1, S, -1)
+    else:
+        idx = np.array(case["idx"], dtype=np.int64).reshape(1, S, -1)
+    return q, k, v, ka, va, idx, np.array([T])
+
+
+def check_aux_fixture(mod):
+    cases = _load("aux_kv_tiny.json")["cases"]
+    for case in cases:
+        q, k, v, ka, va, idx, T = _aux_case(case)
+        with np.errstate(invalid="ignore", over="ignore"):
+            got = mod.sparse_attention_aux(q, k, v, idx, 1, ka, va, T,
+                                           softmax_scale=case["softmax_scale"])
+        if "expected" in case:
+            assert np.allclose(got[0, 0, 0], case["expected"], rtol=0, atol=1e-9), (case["what"], got)
+        elif "expected_rows" in case:
+            for s, exp in enumerate(case["expected_rows"]):
+                assert np.allclose(got[0, s, 0], exp, rtol=1e-15, atol=0), (case["what"], got)
+        else:
+            e = math.e
+            assert np.allclose(got[0, 0, 0], [2 / (1 + e), 2 * e / (1 + e)], rtol=1e-15), (case["what"], got)
+
+
+def check_aux_reduces_to_cache(mod):
+    """With k_aux / v_aux equal to the cache's new rows the result is the plain
+    sparse attention (ties the aux row of key t to cache row t, R1)."""
+    wl = small_workload(batch=2, q_len=3, total_len=300, num_q_heads=8, num_kv_heads=2,
+                        top_k=64, kv_dtype="bf16", seed=44)
+    cpu = make_inputs(wl)
+    f = {k: to_f64(v) for k, v in cpu.items() if v is not None and k != "total_len"}
+    T = cpu["total_len"].numpy()
+    idx = mod.topk(mod.index_scores(f["qI"], f["w"], f["kI"], T), T, 64)
+    # make sure the new tokens are selected (the oracle picks by score)
+    for b in range(2):
+        for s in range(3):
+            row = idx[b, s]
+            row[:s + 1] = np.arange(T[b] - 3, T[b] - 3 + s + 1)
+            idx[b, s] = np.sort(row)
+    ka = np.stack([f["k"][b, T[b] - 3:T[b]] for b in range(2)])
+    va = np.stack([f["v"][b, T[b] - 3:T[b]] for b in range(2)])
+    plain = mod.sparse_attention(f["q"], f["k"], f["v"], idx, 2)
+    got = mod.sparse_attention_aux(f["q"], f["k"], f["v"], idx, 2, ka, va, T)
+    assert np.allclose(got, plain, rtol=1e-13, atol=0)
+    # and a perturbed aux row changes exactly the rows that selected it
+    ka2 = ka.copy()
+    ka2[1, 0] += 1.0
+    got2 = mod.sparse_attention_aux(f["q"], f["k"], f["v"], idx, 2, ka2, va, T)
+    changed = ~np.isclose(got2, got, rtol=1e-13, atol=0).all(axis=(2, 3))
+    expect = np.zeros((2, 3), dtype=bool)
+    expect[1, :] = True   # every query of sequence 1 selected key T-3 (aux row 0)
+    assert (changed == expect).all(), changed
+
+
+def test_aux_golden_fixture():
+    check_aux_fixture(O)
+
+
+def test_aux_reduces_to_plain_attention():
+    check_aux_reduces_to_cache(O)
+
+
+# ---------------------------------------------------------------------------
 # mutation tests: plant a mistake in a copy of the oracle, a pin must fail
 # ---------------------------------------------------------------------------
 class _Mutant:
@@ -696,3 +769,24 @@ def test_mutant_round_toward_zero_is_caught():
         m, e = np.frexp(t.numpy().astype(np.float64))
         return np.ldexp(np.trunc(m * 2.0 ** (bits + 1)) / 2.0 ** (bits + 1), e)
     assert _fails(check_round_to, _Mutant(round_to=bad))
+
+
+def test_mutant_aux_row_off_by_one_is_caught():
+    def bad(q, k, v, idx, num_kv_heads, k_aux, v_aux, total_len, k_scale=None, v_scale=None,
+            softmax_scale=0.0, rows=None):
+        # reads aux row t - (T - S) - 1 (wrapping), a plausible indexing slip
+        S = q.shape[1]
+        ka = np.roll(k_aux, 1, axis=1)
+        va = np.roll(v_aux, 1, axis=1)
+        return O.sparse_attention_aux(q, k, v, idx, num_kv_heads, ka, va, total_len, k_scale,
+                                      v_scale, softmax_scale, rows)
+    m = _Mutant(sparse_attention_aux=bad)
+    assert _fails(check_aux_fixture, m) or _fails(check_aux_reduces_to_cache, m)
+    assert _fails(check_aux_reduces_to_cache, m)
+
+
+def test_mutant_aux_ignored_is_caught():
+    def bad(q, k, v, idx, num_kv_heads, k_aux, v_aux, total_len, k_scale=None, v_scale=None,
+            softmax_scale=0.0, rows=None):
+        return O.sparse_attention(q, k, v, idx, num_kv_heads, k_scale, v_scale, softmax_scale, rows)
+    assert _fails(check_aux_fixture, _Mutant(sparse_attention_aux=bad))

@@ -60,10 +60,13 @@ def peaks():
 # ------------------------------------------------------------------ measured traffic
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one indexer
 # launch per workload, from an ncu capture of that launch at full size (see
-# profiles/). They hold for the indexer source they were taken on: when any of
-# these files changes, the figure is dropped (null) until it is measured again.
-TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh", "dsa_internal.h"]
-TRAFFIC_SOURCE_SHA = "50175b152edd17f4"
+# profiles/). They hold for the indexer source they were taken on: the
+# indexer's own file, the device headers it includes, and the part of the
+# shared internal header it compiles against (its parameters and the cache
+# addressing). When any of that changes, the figure is dropped (null) until it
+# is measured again.
+TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh"]
+TRAFFIC_SOURCE_SHA = "213d0e4930919e27"
 INDEXER_TRAFFIC = {
     "decode_4k": 573184,
     "grouped_decode_32k": 16906240,
@@ -72,14 +75,24 @@ INDEXER_TRAFFIC = {
 }
 
 
-def indexer_traffic(name):
+def indexer_source_hash():
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "top_sparse_attention_chunked_gb300", "csrc")
     for f in TRAFFIC_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
-    if h.hexdigest()[:16] != TRAFFIC_SOURCE_SHA:
+    with open(os.path.join(csrc, "dsa_internal.h"), "rb") as fh:
+        text = fh.read()
+    # from the indexer's constants through its parameter block
+    a = text.index(b"constexpr int kChunk")
+    b = text.index(b"};", text.index(b"struct IndexerParams")) + 2
+    h.update(text[a:b])
+    return h.hexdigest()[:16]
+
+
+def indexer_traffic(name):
+    if indexer_source_hash() != TRAFFIC_SOURCE_SHA:
         return None
     return INDEXER_TRAFFIC.get(name)
 

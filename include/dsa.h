@@ -192,6 +192,34 @@ int dsa_sparse_attn_decode(const dsa_problem* p, const void* q, const void* qI,
                            void* stream);
 
 /*
+ * dsa_sparse_attn_decode_aux -- dsa_sparse_attn_decode with floating
+ * auxiliary K/V: the step's new tokens' own key and value rows, given beside
+ * the caches in the query's floating type. PR #33997 "[CUDA] Support FP16 KV
+ * cache and FP16 query/key in DynamicSparseAttention<BFloat16> ...": its
+ * review summary notes that grouped attention can overflow BF16 auxiliary
+ * values when converting them to FP16, and its second commit keeps floating
+ * auxiliary K/V with FP16 main caches. Reading taken here: a selected key t
+ * of sequence b with t >= total_len[b] - q_len (one of the new tokens, whose
+ * rows are the last q_len cache rows) takes K and V from
+ * k_aux[b][t - (total_len[b] - q_len)] and v_aux[...] at their own values
+ * (attended in fp32, never converted to the cache's type; a BF16 value above
+ * FP16's 65504 stays finite); every other selected key reads the cache. The
+ * indexer and the selection are those of dsa_sparse_attn_decode (the new
+ * tokens' index keys are in kI as always).
+ *
+ *   k_aux, v_aux  [B, S, Hkv, 128] q_dtype, 16-byte aligned, required
+ *   all other arguments, the workspace and the errors as for
+ *   dsa_sparse_attn_decode (same workspace size).
+ */
+int dsa_sparse_attn_decode_aux(const dsa_problem* p, const void* q, const void* qI,
+                               const float* w, const void* kI, const void* k,
+                               const void* v, const float* k_scale,
+                               const float* v_scale, const void* k_aux,
+                               const void* v_aux, int32_t* idx_out, void* out,
+                               void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
  * dsa_sparse_attn_prefill -- the whole step for a chunk of many new tokens
  * (any S >= 1): the indexer as a dense causal contraction on tcgen05 tensor
  * cores, a per-row top-k held in shared memory, then sparse attention.

@@ -53,7 +53,8 @@ constexpr int kMaxCombine = kAttnMaxSplits;
 // padded to 136 floats so the fragment stores of a half-warp hit distinct banks)
 constexpr int kORow = DSA_HEAD_DIM + 8;
 constexpr int kWarpState = 2 * kAttnRows + kAttnRows * kORow;
-constexpr int kMergeFloats = kAttnWarps * kWarpState + 2 * kMaxCombine * kAttnRows + 2 * kAttnRows;
+// (one more state than warps: the auxiliary keys' own, when there are any)
+constexpr int kMergeFloats = (kAttnWarps + 1) * kWarpState + 2 * kMaxCombine * kAttnRows + 2 * kAttnRows;
 constexpr int kStageBytes = (kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnWarps * kWarpSmem
                                                                        : kMergeFloats * 4;
 // Cluster combine: every CTA receives from each peer q its M, L (32 floats at
@@ -119,6 +120,20 @@ __device__ __forceinline__ uint32_t load_q2(const void* q, size_t elem) {
     float2 f = __bfloat1622float2(h);
     return pack_f16(f.x, f.y);
   }
+}
+
+// Query-dtype (BF16 or FP16) values as fp32: two consecutive, or one.
+template <bool F16>
+__device__ __forceinline__ float2 load_f2(const void* base, size_t elem) {
+  const uint32_t raw = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + elem);
+  if constexpr (F16) return __half22float2(*reinterpret_cast<const __half2*>(&raw));
+  else return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw));
+}
+template <bool F16>
+__device__ __forceinline__ float load_f1(const void* base, size_t elem) {
+  const uint16_t raw = static_cast<const uint16_t*>(base)[elem];
+  if constexpr (F16) return __half2float(*reinterpret_cast<const __half*>(&raw));
+  else return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(&raw));
 }
 
 // Exact float value of the signed byte `i` of `x`: the byte plus 128 lands in
@@ -201,6 +216,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   __shared__ int s_abort;
   __shared__ float s_sc[kAttnWarps][64];        // INT8: [stage][k 16 | v 16] scales per warp
   __shared__ uint64_t s_merge_bar;              // cluster combine: every peer's slice landed
+  __shared__ float s_auxp[kAttnRows][kAttnRows];  // auxiliary keys: logits, then weights
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DSA_TS_DECL;
@@ -218,8 +234,12 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   // in a cluster every split takes part in the combine, empty or not
   if (split_begin >= keff && !p.cluster) return;
   const int split_len = max(0, min(p.split_keys, keff - split_begin));
+  // keys of this split read from the cache; with auxiliary K/V the split's
+  // keys at or after the first new token (its tail: the indices ascend) are
+  // attended separately from the auxiliary rows, after the tile loop
+  int split_main = split_len;
   const int nreal = (keff + p.split_keys - 1) / p.split_keys;
-  const int ntiles = (split_len + kTileKeys - 1) / kTileKeys;
+  int ntiles = (split_len + kTileKeys - 1) / kTileKeys;
 
   uint8_t* wsm = smem + warp * kWarpSmem;
   uint8_t* sK[2] = {wsm, wsm + kTile16};
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     const int tile = warp + it * kAttnWarps;
     const int o = tile * kTileKeys;
     int key = -1;
-    if (lane < kTileKeys && o + lane < split_len) {
+    if (lane < kTileKeys && o + lane < split_main) {
       key = s_idx[o + lane];
       if (key < 0 || key >= T) key = -1;
     }
@@ -324,7 +344,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   float m_run[2] = {-INFINITY, -INFINITY};   // rows gq, gq+8 (log2 units)
   float l_run[2] = {0.0f, 0.0f};             // thread-partial sums
 
-  const int my_tiles = ntiles > warp ? (ntiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
+  int my_tiles = ntiles > warp ? (ntiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
   // ---- query fragments (A operand of QK^T), resident for the whole CTA
   uint32_t qa[kD / 16][4];
   {
@@ -350,6 +370,20 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   // the split's selected indices, loaded once (all loads in flight together)
   for (int i = threadIdx.x; i < split_len; i += kAttnThreads) s_idx[i] = __ldcg(idx_row + i);
   __syncthreads();
+  const int past = T - p.S;                   // the sequence's first new token
+  if (p.k_aux != nullptr) {
+    // the split's keys below `past` (s_idx ascends): a binary search
+    int lo = 0, hi = split_len;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_idx[mid] < past) lo = mid + 1;
+      else hi = mid;
+    }
+    split_main = lo;
+    ntiles = (split_main + kTileKeys - 1) / kTileKeys;
+    my_tiles = ntiles > warp ? (ntiles - warp + kAttnWarps - 1) / kAttnWarps : 0;
+  }
+  const int naux = split_len - split_main;    // the same in every thread
   if (threadIdx.x == 0) DSA_TS(2);
   if (my_tiles > 0) issue_tile(0, 0);
   cp_async_commit();
@@ -372,7 +406,7 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     if (it == 0 && lane == 0) DSA_TS(3);
     __syncwarp();
     const int tile = warp + it * kAttnWarps;
-    const int nvalid = min(kTileKeys, split_len - tile * kTileKeys);
+    const int nvalid = min(kTileKeys, split_main - tile * kTileKeys);
 
     const uint8_t* tK = sK[st];
     const uint8_t* tV = sV[st];
@@ -529,8 +563,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
   __syncthreads();   // stage buffers become the merge area
   if (threadIdx.x == 0 && s_abort && p.status) atomicOr(p.status, kDevTimeout);
   if (__any_sync(0xffffffffu, bad_page) && lane == 0 && p.status) atomicOr(p.status, kDevBadPage);
-  float* ws = reinterpret_cast<float*>(smem);      // [warps][kWarpState]
-  float* fac1 = ws + kAttnWarps * kWarpState;      // [max(warps, splits)][16]
+  float* ws = reinterpret_cast<float*>(smem);      // [warps + 1][kWarpState]
+  float* fac1 = ws + (kAttnWarps + 1) * kWarpState;  // [max(warps + 1, splits)][16]
   float* fac2 = fac1 + kMaxCombine * kAttnRows;
   float* sML = fac2 + kMaxCombine * kAttnRows;     // M[16], L[16]
   float* mine = ws + warp * kWarpState;
@@ -549,8 +583,59 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
           make_float2(o_acc[nd][2 * h], o_acc[nd][2 * h + 1]);
     }
   __syncthreads();
+  const int nparts = kAttnWarps + (naux > 0 ? 1 : 0);
+  if (naux > 0) {
+    // ---- the split's auxiliary keys (the new tokens' own K / V, read at
+    // their values in fp32): one more online-softmax state, merged like a warp's
+    float* st = ws + kAttnWarps * kWarpState;   // m[16], l[16], o[16][kORow]
+    for (int pr = threadIdx.x; pr < naux * kAttnRows; pr += kAttnThreads) {
+      const int a = pr / kAttnRows, row = pr % kAttnRows;
+      float dot = 0.0f;
+      if (row < nh) {
+        const int j = s_idx[split_main + a] - past;   // auxiliary row of this key
+        const size_t qo = (static_cast<size_t>(r) * p.Hq + h0 + row) * kD;
+        const size_t ko = ((static_cast<size_t>(b) * p.S + j) * p.Hkv + g) * kD;
+#pragma unroll 8
+        for (int c = 0; c < kD; c += 2) {
+          const float2 qv = load_f2<Q_F16>(p.q, qo + c);
+          const float2 kv = load_f2<Q_F16>(p.k_aux, ko + c);
+          dot = fmaf(qv.x, kv.x, dot);
+          dot = fmaf(qv.y, kv.y, dot);
+        }
+      }
+      s_auxp[a][row] = dot * p.scale_log2;
+    }
+    __syncthreads();
+    if (threadIdx.x < kAttnRows) {
+      const int row = threadIdx.x;
+      float m = -INFINITY;
+      for (int a = 0; a < naux; ++a) m = fmaxf(m, s_auxp[a][row]);
+      float l = 0.0f;
+      for (int a = 0; a < naux; ++a) {
+        const float pa = exp2f(s_auxp[a][row] - m);
+        s_auxp[a][row] = pa;
+        l += pa;
+      }
+      st[row] = m;
+      st[kAttnRows + row] = l;
+    }
+    __syncthreads();
+    float o[kAttnRows];
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row) o[row] = 0.0f;
+    for (int a = 0; a < naux; ++a) {
+      const int j = s_idx[split_main + a] - past;
+      const size_t vo = ((static_cast<size_t>(b) * p.S + j) * p.Hkv + g) * kD + threadIdx.x;
+      const float vv = load_f1<Q_F16>(p.v_aux, vo);
+#pragma unroll
+      for (int row = 0; row < kAttnRows; ++row) o[row] = fmaf(s_auxp[a][row], vv, o[row]);
+    }
+#pragma unroll
+    for (int row = 0; row < kAttnRows; ++row) st[2 * kAttnRows + row * kORow + threadIdx.x] = o[row];
+    __syncthreads();
+  }
   if (threadIdx.x < kAttnRows)
-    combine_factors(ws, kWarpState, kAttnWarps, fac1, fac2, sML);
+    combine_factors(ws, kWarpState, nparts, fac1, fac2, sML);
   __syncthreads();
   if (threadIdx.x == 0) DSA_TS(5);
 
@@ -561,11 +646,13 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
 #pragma unroll
   for (int row = 0; row < kAttnRows; ++row) acc[row] = 0.0f;
 #pragma unroll
-  for (int w = 0; w < kAttnWarps; ++w)
+  for (int w = 0; w < kAttnWarps + 1; ++w)
+    if (w < nparts) {
 #pragma unroll
-    for (int row = 0; row < kAttnRows; ++row)
-      acc[row] += ws[w * kWarpState + 2 * kAttnRows + row * kORow + d] *
-                  fac1[w * kAttnRows + row] * fac2[w * kAttnRows + row];
+      for (int row = 0; row < kAttnRows; ++row)
+        acc[row] += ws[w * kWarpState + 2 * kAttnRows + row * kORow + d] *
+                    fac1[w * kAttnRows + row] * fac2[w * kAttnRows + row];
+    }
   if (single) {
 #pragma unroll
     for (int row = 0; row < kAttnRows; ++row)

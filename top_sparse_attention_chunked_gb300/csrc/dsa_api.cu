@@ -502,8 +502,10 @@ int run_topk(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const
 int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Layout& L,
                   const Paging& pg, const void* q, const void* k, const void* v, const float* ks,
                   const float* vs, const int32_t* idx, void* out, void* ws, bool prefill,
-                  cudaStream_t st) {
-  AttnParams ap;
+                  cudaStream_t st, const void* k_aux = nullptr, const void* v_aux = nullptr) {
+  AttnParams ap{};
+  ap.k_aux = k_aux;
+  ap.v_aux = v_aux;
   ap.pg = pg;
   ap.q = q;
   ap.k = k;
@@ -604,7 +606,8 @@ int check_attn_ptrs(const dsa_problem* p, const void* q, const void* qI, const f
 
 int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, const void* qI, const float* w,
               const void* kI, const void* k, const void* v, const float* ks, const float* vs,
-              int32_t* idx_out, void* out, void* ws, size_t ws_bytes, void* stream) {
+              int32_t* idx_out, void* out, void* ws, size_t ws_bytes, void* stream,
+              const void* k_aux = nullptr, const void* v_aux = nullptr) {
   reset_launches();
   Derived d;
   int rc = check_problem(p, op, &d);
@@ -647,7 +650,7 @@ int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, con
   rc = run_topk(p, d, di, L, scores, idx, ws, hist_in_indexer, topk_rows, true, st,
                 decode ? &pf : nullptr);
   if (rc) return rc;
-  return run_attention(p, d, di, L, pg, q, k, v, ks, vs, idx, out, ws, !decode, st);
+  return run_attention(p, d, di, L, pg, q, k, v, ks, vs, idx, out, ws, !decode, st, k_aux, v_aux);
 }
 
 int index_call(const dsa_problem* p, const dsa_kv_pages* pages, const void* qI, const float* w,
@@ -791,6 +794,19 @@ int dsa_topk(const dsa_problem* p, const float* scores, int32_t* idx, void* ws, 
   // few rows: spread each row over its chunks; many short rows: one CTA per row
   const bool prefer_rows = d.rows >= 2 * di.sms;
   return run_topk(p, d, di, L, scores, idx, ws, false, prefer_rows, false, st);
+}
+
+int dsa_sparse_attn_decode_aux(const dsa_problem* p, const void* q, const void* qI, const float* w,
+                               const void* kI, const void* k, const void* v, const float* k_scale,
+                               const float* v_scale, const void* k_aux, const void* v_aux,
+                               int32_t* idx_out, void* out, void* ws, size_t ws_bytes,
+                               void* stream) {
+  reset_launches();
+  if (!k_aux || !v_aux) return fail(DSA_ERR_INVALID_ARG, "k_aux and v_aux are required");
+  if (!aligned(k_aux, 16) || !aligned(v_aux, 16))
+    return fail(DSA_ERR_MISALIGNED, "k_aux and v_aux must be 16-byte aligned");
+  return attn_call(p, DSA_OP_DECODE, kDense, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, ws,
+                   ws_bytes, stream, k_aux, v_aux);
 }
 
 int dsa_sparse_attn_decode(const dsa_problem* p, const void* q, const void* qI, const float* w,

@@ -156,6 +156,11 @@ struct AttnParams {
   const float* k_scale;    // [B, cap, Hkv] (INT8 only)
   const float* v_scale;
   const int32_t* idx;      // [B*S, topk]
+  // The new tokens' own K / V [B, S, Hkv, 128] in the query dtype, or nullptr.
+  // A selected key at or after a sequence's first new token reads these rows
+  // (fp32 arithmetic at their own values) instead of the cache.
+  const void* k_aux;
+  const void* v_aux;
   void* out;               // [B, S, Hq, 128]
   float* partial;          // split-K partial states
   uint32_t* ticket;        // [B*S*Hkv*HG] zeroed when nsplit > 1

@@ -34,7 +34,8 @@ EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_version", "dsa_timing_select", "dsa_timing_read", "dsa_topk_noalloc",
             "dsa_last_launches", "dsa_cache_append", "dsa_index_scores_paged",
             "dsa_sparse_attn_decode_paged", "dsa_sparse_attn_prefill_paged",
-            "dsa_cache_append_paged", "dsa_rmsnorm_rotary", "dsa_rope_append"]
+            "dsa_cache_append_paged", "dsa_rmsnorm_rotary", "dsa_rope_append",
+            "dsa_sparse_attn_decode_aux"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -133,6 +134,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_topk": (i32, [P, vp, vp, vp, sz, vp]),
         "dsa_sparse_attn_decode": (i32, [P] + [vp] * 11 + [sz, vp]),
         "dsa_sparse_attn_prefill": (i32, [P] + [vp] * 11 + [sz, vp]),
+        "dsa_sparse_attn_decode_aux": (i32, [P] + [vp] * 13 + [sz, vp]),
         "dsa_read_device_status": (i32, [vp, sz, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "dsa_last_error_string": (ctypes.c_char_p, []),
         "dsa_status_string": (ctypes.c_char_p, [i32]),
@@ -392,6 +394,34 @@ def dsa_sparse_attn_decode(p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out
                            stream=None, pages=None):
     _attn("dsa_sparse_attn_decode", p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out,
           workspace, stream, pages)
+
+
+def dsa_sparse_attn_decode_aux(p, q, qI, w, kI, k, v, k_scale, v_scale, k_aux, v_aux, idx_out,
+                               out, workspace, stream=None):
+    """dsa_sparse_attn_decode with the new tokens' own K / V rows k_aux, v_aux
+    [B, S, Hkv, 128] in the query dtype (read at their values for selected
+    keys at or after each sequence's first new token)."""
+    B, S, Hq, Hkv = p.batch, p.q_len, p.num_q_heads, p.num_kv_heads
+    lib = load_library()
+    wp, wn = _ws(workspace)
+    kvdt = _TORCH_DT[p.kv_dtype]
+    qdt = _TORCH_DT[p.q_dtype]
+    lead = _cache_shapes(p, None)
+    _check(lib.dsa_sparse_attn_decode_aux(
+        ctypes.byref(p),
+        _ptr(q, "q", qdt, (B, S, Hq, 128)),
+        _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
+        _ptr(w, "w", torch.float32, (B, S, 16)),
+        _ptr(kI, "kI", torch.bfloat16, lead + (64,)),
+        _ptr(k, "k", kvdt, lead + (Hkv, 128)),
+        _ptr(v, "v", kvdt, lead + (Hkv, 128)),
+        _ptr(k_scale, "k_scale", torch.float32, lead + (Hkv,)),
+        _ptr(v_scale, "v_scale", torch.float32, lead + (Hkv,)),
+        _ptr(k_aux, "k_aux", qdt, (B, S, Hkv, 128)),
+        _ptr(v_aux, "v_aux", qdt, (B, S, Hkv, 128)),
+        _ptr(idx_out, "idx_out", torch.int32, (B, S, p.top_k)),
+        _ptr(out, "out", _TORCH_DT[p.out_dtype], (B, S, Hq, 128)),
+        wp, wn, _stream(stream)))
 
 
 def dsa_sparse_attn_prefill(p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, workspace,

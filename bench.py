@@ -66,12 +66,12 @@ def peaks():
 # addressing). When any of that changes, the figure is dropped (null) until it
 # is measured again.
 TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh"]
-TRAFFIC_SOURCE_SHA = "213d0e4930919e27"
+TRAFFIC_SOURCE_SHA = "775a5be3f9d86128"
 INDEXER_TRAFFIC = {
-    "decode_4k": 573184,
-    "grouped_decode_32k": 16906240,
-    "decode_128k": 16826112,
-    "decode_256k_int8": 33627392,
+    "decode_4k": 574464,
+    "grouped_decode_32k": 16907776,
+    "decode_128k": 16827904,
+    "decode_256k_int8": 33630464,
 }
 
 

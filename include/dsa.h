@@ -466,6 +466,21 @@ int dsa_cache_append_paged(const dsa_problem* p, const dsa_kv_pages* pages, cons
 int dsa_read_device_status(const void* workspace, size_t workspace_bytes,
                            void* stream, uint32_t* status_out);
 
+/*
+ * dsa_set_wait_budget -- how long the indexer's pipeline waits (TMA loads,
+ * tensor-core results, accumulator hand-offs) may run before the kernel gives
+ * up, for the calls that this host thread makes afterwards: `cycles` SM clock
+ * cycles (0: a wait gives up unless it is complete at its first try), or any
+ * negative value for the default of about a second. A kernel whose wait gives
+ * up lets every copy and tensor-core operation it issued finish (those drains
+ * keep the default budget), frees its tensor memory, sets the timeout bit of
+ * the workspace status word (dsa_read_device_status then returns
+ * DSA_ERR_TIMEOUT) and leaves the call's outputs undefined; the CUDA context
+ * stays usable and the next call with the default budget is correct. A test
+ * aid for the failure path: the pages have no counterpart. Returns DSA_OK.
+ */
+int dsa_set_wait_budget(long long cycles);
+
 /* Message for the last failed call on this host thread ("" if none). */
 const char* dsa_last_error_string(void);
 

@@ -13,6 +13,7 @@ namespace dsa {
 namespace {
 
 thread_local std::string g_err;
+thread_local long long g_wait_budget = -1;  // < 0: the default budget
 thread_local int g_timing_kind = -1;
 thread_local cudaEvent_t g_ev[2] = {nullptr, nullptr};
 thread_local bool g_ev_recorded = false;
@@ -358,7 +359,7 @@ int pow2_at_least(int x) {
 int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, const Paging& pg,
                 const void* qI, const float* w, const void* kI, float* scores, uint32_t* hist,
                 uint32_t* status, cudaStream_t st) {
-  IndexerParams ip;
+  IndexerParams ip{};
   ip.pg = pg;
   ip.w = w;
   ip.scores = scores;
@@ -383,6 +384,7 @@ int run_indexer(const dsa_problem* p, const Derived& d, const DeviceInfo& di, co
     if (nb > per_seq_max) per_seq_max = nb;
   }
   ip.total_units = total;
+  ip.wait_budget = g_wait_budget >= 0 ? g_wait_budget : kDefaultWaitBudget;
   CUtensorMap tm_kI, tm_qI;
   int rc = make_map_rows64(&tm_kI, kI, pool_tokens(p, pg), kKeyTile);
   if (rc) return rc;
@@ -950,6 +952,11 @@ int dsa_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32
 }
 
 const char* dsa_last_error_string(void) { return g_err.c_str(); }
+
+int dsa_set_wait_budget(long long cycles) {
+  g_wait_budget = cycles;
+  return DSA_OK;
+}
 
 const char* dsa_status_string(int s) {
   switch (s) {

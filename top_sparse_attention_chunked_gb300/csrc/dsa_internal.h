@@ -42,6 +42,7 @@ constexpr int kHistBits = 11;              // first radix digit: top 11 key bits
 constexpr int kHistBins = 1 << kHistBits;  // 2,048 bins per query row
 constexpr int kKeyTile = 128;              // keys per tcgen05 indexer tile (M)
 constexpr uint32_t kDevTimeout = 1u;       // status bit: a bounded wait ran out
+constexpr long long kDefaultWaitBudget = 2000000000ll;   // SM cycles before a wait gives up
 
 struct SeqLens {
   int32_t T[DSA_MAX_BATCH];
@@ -81,6 +82,7 @@ struct IndexerParams {
   int QB;                // query tokens per block (N = 16 * QB)
   int nqb;               // query blocks per sequence, ceil(S / QB)
   long long total_units; // (sequence, query block, key tile) triples
+  long long wait_budget; // SM cycles before one of its pipeline waits gives up
   Paging pg;               // cache addressing (dense or paged)
   SeqLens lens;
 };

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (c.b != ps.pb || c.qb != ps.pqb) {
         const int bi = ps.nblk & 1;
         if (ps.nblk >= 2 &&
-            !mbar_wait_bounded(&bars->bempty[bi], ((ps.nblk >> 1) - 1) & 1, abort_flag))
+            !mbar_wait_bounded(&bars->bempty[bi], ((ps.nblk >> 1) - 1) & 1, abort_flag, p.wait_budget))
           return;
         mbar_arrive_expect_tx(&bars->bfull[bi], C::kBBytes);
         tma_load_2d(sB + bi * C::kBBytes, &tm_qI, &bars->bfull[bi], 0,
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         ps.pqb = c.qb;
       }
       const int s = ps.s;
-      if (ps.r > 0 && !mbar_wait_bounded(&bars->empty[s], (ps.r - 1) & 1u, abort_flag)) return;
+      if (ps.r > 0 && !mbar_wait_bounded(&bars->empty[s], (ps.r - 1) & 1u, abort_flag, p.wait_budget)) return;
       mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
       // a 128-key tile never straddles a cache block (block sizes are
       // multiples of 128); an entry outside the pool reads block 0 (the
@@ -267,17 +267,17 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (c.b != pb || c.qb != pqb) {
           if (nblk > 0) tc_commit(&bars->bempty[bi]);
           bi = nblk & 1;
-          if (!mbar_wait_bounded(&bars->bfull[bi], (nblk >> 1) & 1, abort_flag)) break;
+          if (!mbar_wait_bounded(&bars->bfull[bi], (nblk >> 1) & 1, abort_flag, p.wait_budget)) break;
           ++nblk;
           pb = c.b;
           pqb = c.qb;
         }
-        if (!mbar_wait_bounded(&bars->full[s], round & 1u, abort_flag)) break;
+        if (!mbar_wait_bounded(&bars->full[s], round & 1u, abort_flag, p.wait_budget)) break;
         if (i == 0) DSA_TS(1);
         if (i == count - 1) DSA_TS(2);
         const int a = static_cast<int>(i % C::NACC);
         if (i >= C::NACC &&
-            !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag))
+            !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag, p.wait_budget))
           break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * N;
@@ -333,7 +333,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         continue;
       }
       const int a = static_cast<int>(i % C::NACC);
-      if (!mbar_wait_bounded(&bars->accfull[a], static_cast<uint32_t>((i / C::NACC) & 1), abort_flag)) break;
+      // every lane of the warp leaves together (tcgen05.ld below is warp-wide)
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars->accfull[a], static_cast<uint32_t>((i / C::NACC) & 1),
+                                                     abort_flag, p.wait_budget)))
+        break;
       tc_fence_after();
       const int t = c.kt * kKeyTile + quarter * 32 + lane;
       const int T = p.lens.T[c.b];

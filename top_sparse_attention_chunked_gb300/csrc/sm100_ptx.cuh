@@ -13,8 +13,9 @@
 
 namespace dsa {
 
-// A bounded wait gives up after about a second of SM clock cycles.
-constexpr long long kWaitBudgetCycles = 2000000000ll;
+// A bounded wait gives up after about a second of SM clock cycles (the
+// default; a call may lower it for the indexer's waits, see IndexerParams).
+constexpr long long kWaitBudgetCycles = kDefaultWaitBudget;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,19 +58,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of `bar` to complete. Returns false (and sets
-// *abort) if the budget runs out or another role already aborted.
+// *abort) once `budget` SM cycles have passed since the first try without the
+// phase completing, or if another role already aborted. A budget of 0 gives
+// up on any wait that is not already complete at its first try.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort_flag) {
+                                                  volatile int* abort_flag,
+                                                  long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
+  const long long t0 = clock64();
   while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       *abort_flag = 1;
       return false;
     }
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
   }
 }
 

@@ -35,7 +35,7 @@ EXPORTED = ["dsa_workspace_size", "dsa_index_scores", "dsa_topk",
             "dsa_last_launches", "dsa_cache_append", "dsa_index_scores_paged",
             "dsa_sparse_attn_decode_paged", "dsa_sparse_attn_prefill_paged",
             "dsa_cache_append_paged", "dsa_rmsnorm_rotary", "dsa_rope_append",
-            "dsa_sparse_attn_decode_aux"]
+            "dsa_sparse_attn_decode_aux", "dsa_set_wait_budget"]
 
 _DT = {"bf16": DSA_BF16, "fp16": DSA_FP16, "int8": DSA_INT8, "fp32": DSA_FP32}
 _TORCH_DT = {DSA_BF16: torch.bfloat16, DSA_FP16: torch.float16, DSA_INT8: torch.int8,
@@ -135,6 +135,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         "dsa_sparse_attn_decode": (i32, [P] + [vp] * 11 + [sz, vp]),
         "dsa_sparse_attn_prefill": (i32, [P] + [vp] * 11 + [sz, vp]),
         "dsa_sparse_attn_decode_aux": (i32, [P] + [vp] * 13 + [sz, vp]),
+        "dsa_set_wait_budget": (i32, [ctypes.c_longlong]),
         "dsa_read_device_status": (i32, [vp, sz, vp, ctypes.POINTER(ctypes.c_uint32)]),
         "dsa_last_error_string": (ctypes.c_char_p, []),
         "dsa_status_string": (ctypes.c_char_p, [i32]),
@@ -436,6 +437,12 @@ def dsa_read_device_status(workspace, stream=None) -> int:
     st = ctypes.c_uint32(0)
     _check(lib.dsa_read_device_status(wp, wn, _stream(stream), ctypes.byref(st)))
     return st.value
+
+
+def dsa_set_wait_budget(cycles: int):
+    """Budget of the indexer's pipeline waits for this thread's later calls
+    (SM cycles; negative: the default)."""
+    _check(load_library().dsa_set_wait_budget(int(cycles)))
 
 
 def dsa_timing_select(kind: int):

@@ -47,6 +47,27 @@ def test_noalloc_topk_matches_workspace_topk_twice(D):
         assert torch.equal(got.cpu(), ref.cpu()), f"call {i}: differs from dsa_topk"
 
 
+def test_noalloc_topk_capacity_above_its_scratch_length(D):
+    """A cache capacity beyond the scratch's row length is fine while the
+    visible length stays within it (the kernels index only visible keys);
+    one row also against the oracle's selection directly."""
+    import oracle.dsa_oracle as O
+    B, S, cap, T, k = 1, 2, 200000, 131072, 2048
+    p = D.make_problem(batch=B, q_len=S, total_len=[T], top_k=k, cache_capacity=cap)
+    sc = _scores((B, S, cap), "cont", 501).cuda()
+    sc[:, :, T:] = float("nan")   # never read
+    ref = torch.full((B, S, k), -7, dtype=torch.int32, device="cuda")
+    ws = D.alloc_workspace(p, D.DSA_OP_TOPK)
+    D.dsa_topk(p, sc, ref, ws)
+    for _ in range(2):
+        got = torch.full((B, S, k), -9, dtype=torch.int32, device="cuda")
+        D.dsa_topk_noalloc(p, sc, got)
+        torch.cuda.synchronize()
+        assert torch.equal(got.cpu(), ref.cpu())
+    row = sc[0, 1, :T].double().cpu().numpy()
+    assert (got[0, 1].cpu().numpy() == O.topk_select_row(row, k)).all()
+
+
 def test_noalloc_topk_rejects_sizes_beyond_its_scratch(D):
     sc = torch.zeros(1, 9, 64, device="cuda")
     idx = torch.zeros(1, 9, 8, dtype=torch.int32, device="cuda")

@@ -32,7 +32,26 @@ constexpr size_t kNaBytes = kNaCands + static_cast<size_t>(kNaRows) * kNaLen * 8
 static __device__ __align__(256) uint8_t g_topk_scratch[kNaBytes];
 
 std::mutex g_na_mu;
-uint8_t* g_na_ptr[64] = {};   // device address of g_topk_scratch per device ordinal
+// Device address of g_topk_scratch per device ordinal, with the CUDA context
+// it was looked up in: a new context on that device (after a device reset the
+// module is loaded again and the array may move) looks it up again.
+uint8_t* g_na_ptr[64] = {};
+void* g_na_ctx[64] = {};
+
+using CtxGetCurrentFn = int (*)(void**);   // cuCtxGetCurrent(CUcontext*)
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
 
 }  // namespace
 
@@ -60,14 +79,19 @@ extern "C" int dsa_topk_noalloc(const dsa_problem* p, const float* scores, int32
   if ((reinterpret_cast<uintptr_t>(scores) & 3) || (reinterpret_cast<uintptr_t>(idx) & 3))
     return noalloc_fail(DSA_ERR_MISALIGNED, "scores and idx must be 4-byte aligned");
 
-  // once per device, with that device current: the array's device address
+  // once per device and context, with that device current: the array's
+  // device address (the first call on a device does this set-up, so make it
+  // before capturing calls in a CUDA graph)
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
     return noalloc_fail(DSA_ERR_NO_DEVICE, "no CUDA device is current");
+  CtxGetCurrentFn ctx_fn = ctx_get_current();
+  void* ctx = nullptr;
+  if (ctx_fn) ctx_fn(&ctx);
   uint8_t* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_na_mu);
-    if (!g_na_ptr[dev]) {
+    if (!g_na_ptr[dev] || ctx == nullptr || g_na_ctx[dev] != ctx) {
       void* ptr = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&ptr, g_topk_scratch);
       if (e != cudaSuccess || !ptr) {
@@ -77,6 +101,9 @@ extern "C" int dsa_topk_noalloc(const dsa_problem* p, const float* scores, int32
         return noalloc_fail(DSA_ERR_CUDA, buf);
       }
       g_na_ptr[dev] = static_cast<uint8_t*>(ptr);
+      // the lookup made the device's context current if none was
+      if (ctx_fn) ctx_fn(&ctx);
+      g_na_ctx[dev] = ctx;
     }
     base = g_na_ptr[dev];
   }

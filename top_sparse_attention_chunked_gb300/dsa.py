@@ -281,7 +281,9 @@ def dsa_topk(p: DsaProblem, scores, idx, workspace, stream=None):
 def dsa_topk_noalloc(p: DsaProblem, scores, idx, stream=None):
     """dsa_topk without a workspace, for callers that cannot allocate device
     memory (the library keeps the scratch in a static device array; at most
-    8 query rows of at most 131,072 visible keys)."""
+    8 query rows of at most 131,072 visible keys). Every call shares that one
+    array: calls that could overlap on the GPU (other streams or threads)
+    must be serialised by the caller."""
     B, S, cap = p.batch, p.q_len, p.cache_capacity
     lib = load_library()
     _check(lib.dsa_topk_noalloc(ctypes.byref(p),

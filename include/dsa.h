@@ -131,6 +131,18 @@ typedef struct dsa_problem {
   int32_t kv_dtype;
   int32_t out_dtype;
   int32_t attn_split_keys;
+  /* K / V cache layout, in elements: the strides of the batch, token and KV
+   * head dimensions (in this order). All zero: the default token-major
+   * layout [B, cap, Hkv, 128] (strides cap*Hkv*128, Hkv*128, 128). Otherwise
+   * each (batch, token, head) vector of 128 values must be contiguous, so
+   * every stride is a multiple of 128 (the token stride at least 128, the
+   * head stride at least 128 when Hkv > 1); a BNSH cache [B, Hkv, cap, 128]
+   * is (Hkv*cap*128, 128, cap*128). The same layout holds for K and V (INT8
+   * codes included); INT8 scales stay [B, cap, Hkv]. Used by the decode and
+   * prefill calls on dense caches; the paged calls, dsa_cache_append and
+   * dsa_rope_append take only the default (all zero), else
+   * DSA_ERR_UNSUPPORTED. */
+  int64_t kv_strides[3];
 } dsa_problem;
 
 /*

@@ -38,8 +38,9 @@ def test_binding_names_match_header():
 
 def test_problem_struct_matches_header():
     from top_sparse_attention_chunked_gb300.dsa import DsaProblem
-    # 9 ints, 64 lengths, 1 float, 4 ints
-    assert ctypes.sizeof(DsaProblem) == 4 * (9 + 64 + 1 + 4)
+    # 9 ints, 64 lengths, 1 float, 4 ints, then 3 int64 strides (8-aligned: no padding)
+    assert DsaProblem.kv_strides.offset == 4 * (9 + 64 + 1 + 4)
+    assert ctypes.sizeof(DsaProblem) == 4 * (9 + 64 + 1 + 4) + 8 * 3
 
 
 def _prob(**kw):

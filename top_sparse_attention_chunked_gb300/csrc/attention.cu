@@ -284,6 +284,10 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     }
     // the key's cache row (key 0's for invalid keys, whose logits are masked)
     const long long crow = cache_row(p.pg, b, p.cap, key < 0 ? 0 : key, &bad_page);
+    // the K / V row (128 values) of this key and KV head
+    const long long kvr = p.pg.table ? crow * p.Hkv + g
+                                     : b * p.kv_sb + static_cast<long long>(key < 0 ? 0 : key) * p.kv_st +
+                                           g * p.kv_sh;
     if constexpr (KV == KV_INT8) {
       // INT8 rows (128 B): 16-byte cp.async measured faster here than row
       // gathers; codes and scales land zero-filled for invalid keys
@@ -294,8 +298,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
         const int j = lane + 32 * i;            // 0..127: row j/8, chunk j%8
         const int row = j >> 3, c = j & 7;
         const int kr = __shfl_sync(0xffffffffu, key, row);
-        const long long cr = __shfl_sync(0xffffffffu, crow, row);
-        const size_t off = (static_cast<size_t>(cr) * p.Hkv + g) * kD + c * 16;
+        const long long kr2 = __shfl_sync(0xffffffffu, kvr, row);
+        const size_t off = static_cast<size_t>(kr2) * kD + c * 16;
         cp_async16(sKc[st] + row * kD + c * 16, kb + off, kr >= 0);
         cp_async16(sVc[st] + row * kD + c * 16, vb + off, kr >= 0);
       }
@@ -315,15 +319,15 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       for (int i = 0; i < kTileKeys / 2; ++i) {
         const int row = 2 * i + (lane >> 4);
         const int kr = __shfl_sync(0xffffffffu, key, row);
-        const long long cr = __shfl_sync(0xffffffffu, crow, row);
-        const size_t off = ((static_cast<size_t>(cr) * p.Hkv + g) * kD) * 2 + c * 16;
+        const long long kr2 = __shfl_sync(0xffffffffu, kvr, row);
+        const size_t off = (static_cast<size_t>(kr2) * kD) * 2 + c * 16;
         cp_async16(sK[st] + swz(row, c), kb + off, kr >= 0);
         cp_async16(sV[st] + swz(row, c), vb + off, kr >= 0);
       }
     } else {
       // 16-bit rows (256 B): TMA row gathers, lane l of the first 16 issuing
       // one for 4 rows (grp) of one column block (blk) of K or V (tsr)
-      const int yrow = static_cast<int>(crow * p.Hkv + g);
+      const int yrow = static_cast<int>(kvr);
       const int grp = lane & 3, blk = (lane >> 2) & 1, tsr = lane >> 3;
       const int y0 = __shfl_sync(0xffffffffu, yrow, 4 * grp);
       const int y1 = __shfl_sync(0xffffffffu, yrow, 4 * grp + 1);

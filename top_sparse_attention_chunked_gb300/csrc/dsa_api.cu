@@ -146,6 +146,8 @@ struct Derived {
   int kmax = 0;        // largest k_eff
   int G = 0, HG = 0;   // group size, head groups per KV head
   int bm_words = 0;    // bitmap words per row
+  long long kv_sb = 0, kv_st = 0, kv_sh = 0;   // K / V row strides (rows of 128 values)
+  bool kv_default = true;                      // the token-major layout
 };
 
 int check_problem(const dsa_problem* p, int op, Derived* d) {
@@ -197,6 +199,28 @@ int check_problem(const dsa_problem* p, int op, Derived* d) {
       return fail(DSA_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
     d->G = p->num_q_heads / p->num_kv_heads;
     d->HG = ceil_div(d->G, kAttnRows);
+  }
+  if (op == DSA_OP_DECODE || op == DSA_OP_PREFILL) {
+    const int64_t* ks = p->kv_strides;
+    d->kv_default = (ks[0] == 0 && ks[1] == 0 && ks[2] == 0);
+    if (d->kv_default) {
+      d->kv_sb = static_cast<long long>(p->cache_capacity) * p->num_kv_heads;
+      d->kv_st = p->num_kv_heads;
+      d->kv_sh = 1;
+    } else {
+      for (int i = 0; i < 3; ++i)
+        if (ks[i] < 0 || ks[i] % DSA_HEAD_DIM != 0)
+          return fail(DSA_ERR_INVALID_ARG, "kv_strides[%d] = %lld must be a non-negative multiple of %d",
+                      i, static_cast<long long>(ks[i]), DSA_HEAD_DIM);
+      if (ks[1] < DSA_HEAD_DIM || (p->num_kv_heads > 1 && ks[2] < DSA_HEAD_DIM))
+        return fail(DSA_ERR_INVALID_ARG, "kv_strides: the token stride (and, with several KV heads, "
+                    "the head stride) must be at least %d", DSA_HEAD_DIM);
+      d->kv_sb = ks[0] / DSA_HEAD_DIM;
+      d->kv_st = ks[1] / DSA_HEAD_DIM;
+      d->kv_sh = ks[2] / DSA_HEAD_DIM;
+    }
+  } else if (p->kv_strides[0] || p->kv_strides[1] || p->kv_strides[2]) {
+    return fail(DSA_ERR_UNSUPPORTED, "kv_strides apply to the decode and prefill calls only");
   }
   if (op == DSA_OP_DECODE && p->q_len > DSA_MAX_DECODE_Q_LEN)
     return fail(DSA_ERR_UNSUPPORTED, "decode takes at most %d query tokens per sequence (got %d)",
@@ -327,9 +351,17 @@ long long pool_tokens(const dsa_problem* p, const Paging& pg) {
 
 const Paging kDense = {nullptr, 0, 0, 0};
 
+// Calls that take only the token-major K / V layout.
+int check_default_layout(const dsa_problem* p) {
+  if (p->kv_strides[0] || p->kv_strides[1] || p->kv_strides[2])
+    return fail(DSA_ERR_UNSUPPORTED, "paged caches and cache writes take only the default kv_strides");
+  return DSA_OK;
+}
+
 // Validates a paged-cache descriptor against the problem and fills *pg.
 int check_pages(const dsa_problem* p, const dsa_kv_pages* pages, Paging* pg) {
   if (!pages) return fail(DSA_ERR_INVALID_ARG, "pages is NULL");
+  if (int rc = check_default_layout(p)) return rc;
   const int bs = pages->block_size;
   if (bs < 128 || bs > (1 << 20) || (bs & (bs - 1)) != 0)
     return fail(DSA_ERR_UNSUPPORTED, "block_size %d must be a power of two from 128 to 2^20", bs);
@@ -526,6 +558,9 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.HG = d.HG;
   ap.cap = p->cache_capacity;
   ap.topk = p->top_k;
+  ap.kv_sb = d.kv_sb;
+  ap.kv_st = d.kv_st;
+  ap.kv_sh = d.kv_sh;
   choose_split(p, d, di.sms, &ap.split_keys, &ap.nsplit);
   if (ap.nsplit > kAttnMaxSplits)
     return fail(DSA_ERR_UNSUPPORTED, "attn_split_keys %d gives %d splits (max %d)",
@@ -542,9 +577,19 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.status = at<uint32_t>(ws, 0);
   cudaError_t e;
   timing_before(DSA_KERNEL_ATTENTION, st);
+  // K / V rows the caches span (the row maps' extent): the pool's, or the
+  // last (batch, token, head) row of the strided layout plus one
+  const long long kv_rows =
+      pg.table ? pool_tokens(p, pg) * p->num_kv_heads
+               : (p->batch - 1) * d.kv_sb + (p->cache_capacity - 1LL) * d.kv_st +
+                     (p->num_kv_heads - 1LL) * d.kv_sh + 1;
   if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin)) {
     CUtensorMap tm_k, tm_v;
-    const long long rows = pool_tokens(p, pg) * p->num_kv_heads;
+    const long long rows = kv_rows;
+    if (rows >= (1LL << 31)) {
+      timing_after(DSA_KERNEL_ATTENTION, st);
+      return fail(DSA_ERR_UNSUPPORTED, "the K / V caches must span fewer than 2^31 rows");
+    }
     int rc = make_map_kv_rows(&tm_k, k, rows);
     if (rc == DSA_OK) rc = make_map_kv_rows(&tm_v, v, rows);
     if (rc != DSA_OK) {
@@ -554,7 +599,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
     e = launch_prefill_tc(ap, p->kv_dtype, di.sms, tm_k, tm_v, at<uint32_t>(ws, 0), st);
   } else {
     // row gathers (16-bit caches) address rows with signed 32-bit coordinates
-    const long long rows = pool_tokens(p, pg) * p->num_kv_heads;
+    const long long rows = kv_rows;
     if (p->kv_dtype != DSA_INT8 && rows >= (1LL << 31)) {
       timing_after(DSA_KERNEL_ATTENTION, st);
       return fail(DSA_ERR_UNSUPPORTED, "cache rows * num_kv_heads must be below 2^31");
@@ -649,8 +694,9 @@ int attn_call(const dsa_problem* p, int op, const Paging& pg, const void* q, con
                    status, st);
   if (rc) return rc;
   const KvPrefetch pf{k, v, ks, vs, pg};
+  // the prefetch takes a token's rows of all KV heads as one span
   rc = run_topk(p, d, di, L, scores, idx, ws, hist_in_indexer, topk_rows, true, st,
-                decode ? &pf : nullptr);
+                decode && d.kv_default ? &pf : nullptr);
   if (rc) return rc;
   return run_attention(p, d, di, L, pg, q, k, v, ks, vs, idx, out, ws, !decode, st, k_aux, v_aux);
 }
@@ -704,7 +750,8 @@ int report_error(int status, const char* msg) { return fail(status, "%s", msg); 
 // Problem validation for calls that write caches (any q_len, as for prefill).
 int problem_check_for_append(const dsa_problem* p) {
   Derived d;
-  return check_problem(p, DSA_OP_PREFILL, &d);
+  if (int rc = check_problem(p, DSA_OP_PREFILL, &d)) return rc;
+  return check_default_layout(p);
 }
 
 int noalloc_check_topk(const dsa_problem* p, int* rows, int* max_n) {
@@ -834,6 +881,7 @@ static int append_call(const dsa_problem* p, const dsa_kv_pages* pages, const vo
   Derived d;
   int rc = check_problem(p, DSA_OP_PREFILL, &d);
   if (rc) return rc;
+  if ((rc = check_default_layout(p))) return rc;
   Paging pg = kDense;
   if (pages && (rc = check_pages(p, pages, &pg))) return rc;
   if (!kI_new || !k_new || !v_new || !kI || !k || !v)

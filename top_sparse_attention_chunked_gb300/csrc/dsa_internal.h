@@ -167,6 +167,10 @@ struct AttnParams {
   float* partial;          // split-K partial states
   uint32_t* ticket;        // [B*S*Hkv*HG] zeroed when nsplit > 1
   int B, S, Hq, Hkv, G, HG, cap, topk;
+  // K / V row (128 values) of (sequence b, token t, KV head g) on a dense
+  // cache: b * kv_sb + t * kv_st + g * kv_sh (the paged pool keeps its
+  // token-major rows)
+  long long kv_sb, kv_st, kv_sh;
   int split_keys, nsplit;
   int cluster;             // nsplit in {2,4,8,16}: splits merged inside a thread-block cluster
   int q_dtype, out_dtype;

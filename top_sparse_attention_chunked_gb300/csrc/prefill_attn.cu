@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           if constexpr (PAGED)
             y[e] = static_cast<int>(cache_row(p.pg, b, p.cap, key, &bad_page) * p.Hkv + w.g);
           else
-            y[e] = (b * p.cap + key) * p.Hkv + w.g;
+            y[e] = b * static_cast<int>(p.kv_sb) + key * static_cast<int>(p.kv_st) +
+                   w.g * static_cast<int>(p.kv_sh);   // the host keeps every row below 2^31
         }
       };
       for (int pass = 0; pass < 2 && ok; ++pass) {            // K tiles, then V tiles

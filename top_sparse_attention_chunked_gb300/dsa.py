@@ -103,6 +103,7 @@ class DsaProblem(ctypes.Structure):
         ("kv_dtype", ctypes.c_int32),
         ("out_dtype", ctypes.c_int32),
         ("attn_split_keys", ctypes.c_int32),
+        ("kv_strides", ctypes.c_int64 * 3),
     ]
 
 
@@ -171,8 +172,10 @@ def make_problem(batch: int, q_len: int, total_len: Sequence[int] | int, top_k: 
                  num_q_heads: int = 24, num_kv_heads: int = 2, cache_capacity: Optional[int] = None,
                  q_dtype="bf16", kv_dtype="bf16", out_dtype=None, softmax_scale: float = 0.0,
                  head_dim: int = 128, idx_heads: int = 16, idx_dim: int = 64,
-                 attn_split_keys: int = 0) -> DsaProblem:
-    """Fill a DsaProblem; dtypes by name ('bf16', 'fp16', 'int8', 'fp32')."""
+                 attn_split_keys: int = 0, kv_strides: Optional[Sequence[int]] = None) -> DsaProblem:
+    """Fill a DsaProblem; dtypes by name ('bf16', 'fp16', 'int8', 'fp32');
+    kv_strides: the K / V caches' (batch, token, head) strides in elements
+    (None: the default token-major layout)."""
     if isinstance(total_len, int):
         total_len = [total_len] * max(1, min(batch, DSA_MAX_BATCH))
     p = DsaProblem()
@@ -188,6 +191,9 @@ def make_problem(batch: int, q_len: int, total_len: Sequence[int] | int, top_k: 
     p.kv_dtype = _DT[kv_dtype]
     p.out_dtype = _DT[out_dtype if out_dtype is not None else q_dtype]
     p.attn_split_keys = attn_split_keys
+    if kv_strides is not None:
+        for i, v in enumerate(kv_strides):
+            p.kv_strides[i] = int(v)
     return p
 
 
@@ -247,6 +253,19 @@ def make_pages(block_table: torch.Tensor, block_size: int, num_blocks: int) -> D
     pg = DsaKvPages(block_size, num_blocks, block_table.shape[1], block_table.data_ptr())
     pg._table = block_table
     return pg
+
+
+def _kv_ptr(p: DsaProblem, t, name, dtype, shape):
+    """A K / V cache pointer: the default layout is checked by shape; with
+    kv_strides the tensor only has to be contiguous and hold the last row."""
+    st = list(p.kv_strides)
+    if not any(st):
+        return _ptr(t, name, dtype, shape)
+    ptr = _ptr(t, name, dtype)
+    last = (p.batch - 1) * st[0] + (p.cache_capacity - 1) * st[1] + (p.num_kv_heads - 1) * st[2] + 128
+    if t.numel() < last:
+        raise ValueError(f"{name} holds {t.numel()} elements, the strides reach {last}")
+    return ptr
 
 
 def _cache_shapes(p: DsaProblem, pages: Optional[DsaKvPages]):
@@ -379,8 +398,8 @@ def _attn(fn_name, p, q, qI, w, kI, k, v, k_scale, v_scale, idx_out, out, worksp
         _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
         _ptr(w, "w", torch.float32, (B, S, 16)),
         _ptr(kI, "kI", torch.bfloat16, lead + (64,)),
-        _ptr(k, "k", kvdt, lead + (Hkv, 128)),
-        _ptr(v, "v", kvdt, lead + (Hkv, 128)),
+        _kv_ptr(p, k, "k", kvdt, lead + (Hkv, 128)),
+        _kv_ptr(p, v, "v", kvdt, lead + (Hkv, 128)),
         _ptr(k_scale, "k_scale", torch.float32, lead + (Hkv,)),
         _ptr(v_scale, "v_scale", torch.float32, lead + (Hkv,)),
         _ptr(idx_out, "idx_out", torch.int32, (B, S, p.top_k)),
@@ -416,8 +435,8 @@ def dsa_sparse_attn_decode_aux(p, q, qI, w, kI, k, v, k_scale, v_scale, k_aux, v
         _ptr(qI, "qI", torch.bfloat16, (B, S, 16, 64)),
         _ptr(w, "w", torch.float32, (B, S, 16)),
         _ptr(kI, "kI", torch.bfloat16, lead + (64,)),
-        _ptr(k, "k", kvdt, lead + (Hkv, 128)),
-        _ptr(v, "v", kvdt, lead + (Hkv, 128)),
+        _kv_ptr(p, k, "k", kvdt, lead + (Hkv, 128)),
+        _kv_ptr(p, v, "v", kvdt, lead + (Hkv, 128)),
         _ptr(k_scale, "k_scale", torch.float32, lead + (Hkv,)),
         _ptr(v_scale, "v_scale", torch.float32, lead + (Hkv,)),
         _ptr(k_aux, "k_aux", qdt, (B, S, Hkv, 128)),

@@ -285,9 +285,13 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
     // the key's cache row (key 0's for invalid keys, whose logits are masked)
     const long long crow = cache_row(p.pg, b, p.cap, key < 0 ? 0 : key, &bad_page);
     // the K / V row (128 values) of this key and KV head
-    const long long kvr = p.pg.table ? crow * p.Hkv + g
-                                     : b * p.kv_sb + static_cast<long long>(key < 0 ? 0 : key) * p.kv_st +
-                                           g * p.kv_sh;
+    long long kvr = p.pg.table ? crow * p.Hkv + g
+                               : b * p.kv_sb + static_cast<long long>(key < 0 ? 0 : key) * p.kv_st +
+                                     g * p.kv_sh;
+    if (!bounds_ok(kvr >= 0 && kvr < p.kv_rows && crow * p.Hkv + g < p.scale_rows, p.status)) {
+      kvr = 0;     // read row 0 and mask the key
+      key = -1;
+    }
     if constexpr (KV == KV_INT8) {
       // INT8 rows (128 B): 16-byte cp.async measured faster here than row
       // gathers; codes and scales land zero-filled for invalid keys
@@ -596,7 +600,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
       const int a = pr / kAttnRows, row = pr % kAttnRows;
       float dot = 0.0f;
       if (row < nh) {
-        const int j = s_idx[split_main + a] - past;   // auxiliary row of this key
+        int j = s_idx[split_main + a] - past;         // auxiliary row of this key
+        if (!bounds_ok(j >= 0 && j < p.S, p.status)) j = 0;
         const size_t qo = (static_cast<size_t>(r) * p.Hq + h0 + row) * kD;
         const size_t ko = ((static_cast<size_t>(b) * p.S + j) * p.Hkv + g) * kD;
 #pragma unroll 8
@@ -628,7 +633,8 @@ __global__ void __launch_bounds__(kAttnThreads) sparse_attn_kernel(const __grid_
 #pragma unroll
     for (int row = 0; row < kAttnRows; ++row) o[row] = 0.0f;
     for (int a = 0; a < naux; ++a) {
-      const int j = s_idx[split_main + a] - past;
+      int j = s_idx[split_main + a] - past;
+      if (!bounds_ok(j >= 0 && j < p.S, p.status)) j = 0;
       const size_t vo = ((static_cast<size_t>(b) * p.S + j) * p.Hkv + g) * kD + threadIdx.x;
       const float vv = load_f1<Q_F16>(p.v_aux, vo);
 #pragma unroll

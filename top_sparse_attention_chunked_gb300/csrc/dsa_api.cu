@@ -561,6 +561,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
   ap.kv_sb = d.kv_sb;
   ap.kv_st = d.kv_st;
   ap.kv_sh = d.kv_sh;
+  ap.scale_rows = pool_tokens(p, pg) * p->num_kv_heads;
   choose_split(p, d, di.sms, &ap.split_keys, &ap.nsplit);
   if (ap.nsplit > kAttnMaxSplits)
     return fail(DSA_ERR_UNSUPPORTED, "attn_split_keys %d gives %d splits (max %d)",
@@ -583,6 +584,7 @@ int run_attention(const dsa_problem* p, const Derived& d, const DeviceInfo& di, 
       pg.table ? pool_tokens(p, pg) * p->num_kv_heads
                : (p->batch - 1) * d.kv_sb + (p->cache_capacity - 1LL) * d.kv_st +
                      (p->num_kv_heads - 1LL) * d.kv_sh + 1;
+  ap.kv_rows = kv_rows;
   if (prefill && p->attn_split_keys == 0 && prefill_tc_supported(ap, p->kv_dtype, di.smem_optin)) {
     CUtensorMap tm_k, tm_v;
     const long long rows = kv_rows;
@@ -996,6 +998,8 @@ int dsa_read_device_status(const void* ws, size_t ws_bytes, void* stream, uint32
   if (v & kDevTimeout) return fail(DSA_ERR_TIMEOUT, "a kernel's bounded wait ran out");
   if (v & kDevBadPage)
     return fail(DSA_ERR_INVALID_ARG, "a gathered key's block-table entry lies outside the pool");
+  if (v & kDevBounds)
+    return fail(DSA_ERR_INVALID_ARG, "a debug bounds check failed (a row outside its array)");
   return DSA_OK;
 }
 

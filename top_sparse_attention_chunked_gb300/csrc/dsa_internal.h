@@ -87,6 +87,21 @@ struct IndexerParams {
   SeqLens lens;
 };
 
+constexpr uint32_t kDevBounds = 4u;    // status bit: a debug bounds check failed
+
+// Debug builds (-DDSA_DEBUG_BOUNDS) check the rows that index-driven gathers
+// compute against the extent of the array they read: a row outside it sets
+// kDevBounds in the status word and the access is skipped (never a trap).
+// Release builds compile the check to `true`.
+#ifdef DSA_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool cond, uint32_t* status) {
+  if (!cond && status) atomicOr(status, kDevBounds);
+  return cond;
+}
+#else
+__device__ __forceinline__ constexpr bool bounds_ok(bool, uint32_t*) { return true; }
+#endif
+
 // Kernel kinds for the timing hook (mirror DSA_KERNEL_*).
 void timing_before(int kind, cudaStream_t stream);
 void timing_after(int kind, cudaStream_t stream);
@@ -171,6 +186,8 @@ struct AttnParams {
   // cache: b * kv_sb + t * kv_st + g * kv_sh (the paged pool keeps its
   // token-major rows)
   long long kv_sb, kv_st, kv_sh;
+  long long kv_rows;       // K / V rows (128 values) the caches span
+  long long scale_rows;    // INT8 scale entries the scale arrays hold
   int split_keys, nsplit;
   int cluster;             // nsplit in {2,4,8,16}: splits merged inside a thread-block cluster
   int q_dtype, out_dtype;

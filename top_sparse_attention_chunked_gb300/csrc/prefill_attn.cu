@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           else
             y[e] = b * static_cast<int>(p.kv_sb) + key * static_cast<int>(p.kv_st) +
                    w.g * static_cast<int>(p.kv_sh);   // the host keeps every row below 2^31
+          if (!bounds_ok(y[e] >= 0 && y[e] < p.kv_rows, status)) y[e] = 0;
         }
       };
       for (int pass = 0; pass < 2 && ok; ++pass) {            // K tiles, then V tiles

@@ -121,7 +121,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     global _lib
     if _lib is not None and path is None:
         return _lib
-    p = path or LIB_PATH
+    # DSA_LIBRARY names another build of the library (e.g. libdsa_debug.so)
+    p = path or os.environ.get("DSA_LIBRARY") or LIB_PATH
     if not os.path.exists(p):
         raise RuntimeError(f"libdsa.so not found at {p}: build it with "
                            "top_sparse_attention_chunked_gb300.build_lib.build()")

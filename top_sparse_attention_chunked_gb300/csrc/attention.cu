@@ -26,6 +26,7 @@
 // P keeps 16 significant bits. INT8 codes are exact in BF16/FP16; k_scale
 // multiplies the logit after the dot product and v_scale is folded into P.
 #include <cooperative_groups.h>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -63,7 +64,11 @@ constexpr int kStageBytes = (kAttnWarps * kWarpSmem > kMergeFloats * 4) ? kAttnW
 // 16 * 32 + 2,048 floats, written by the peers with st.async while this CTA
 // may still be gathering, so it has its own region.
 constexpr int kRecvFloats = 16 * 2 * kAttnRows + kAttnRows * DSA_HEAD_DIM;
-constexpr int kAttnSmem = kStageBytes + kRecvFloats * 4 + 1024;   // + slack to align the base
+// dynamic shared memory (+ slack to align the base): the stage buffers, and
+// in a cluster the receive area after them (outside a cluster three CTAs fit
+// on an SM, in one two)
+constexpr int kAttnSmem = kStageBytes + 1024;
+constexpr int kAttnSmemCluster = kStageBytes + kRecvFloats * 4 + 1024;
 
 enum { KV_BF16 = 0, KV_FP16 = 1, KV_INT8 = 2 };
 
@@ -786,11 +791,12 @@ template <int KV, bool Q_F16, int OUT>
 static cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             cudaStream_t stream) {
   auto kern = sparse_attn_kernel<KV, Q_F16, OUT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  const int smem = p.cluster ? kAttnSmemCluster : kAttnSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
   if (!p.cluster)
-    return launch_kernel("sparse_attn_kernel", kern, grid, dim3(kAttnThreads), kAttnSmem, stream, true,
+    return launch_kernel("sparse_attn_kernel", kern, grid, dim3(kAttnThreads), smem, stream, true,
                          tm_k, tm_v, p);
   if (p.nsplit > 8) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -799,7 +805,7 @@ static cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tm_k, const 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kAttnThreads);
-  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -826,35 +832,41 @@ static cudaError_t launch_out(const AttnParams& p, int out_dtype, const CUtensor
   }
 }
 
-int attn_max_cluster() {
-  static int cached[64] = {};
+int attn_cluster_capacity(int size) {
+  // per device and cluster size (2, 4, 8, 16): clusters resident at once
+  static std::mutex mu;
+  static int cached[64][5] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
-  if (cached[dev]) return cached[dev];
-  int result = 8;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int si = size == 2 ? 0 : size == 4 ? 1 : size == 8 ? 2 : size == 16 ? 3 : 4;
+  if (si == 4) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev][si]) return cached[dev][si] - 1;
+  int n = 0;
   auto kern = sparse_attn_kernel<KV_FP16, false, DSA_BF16>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem) ==
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemCluster) ==
           cudaSuccess &&
-      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-          cudaSuccess) {
+      (size <= 8 || cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                        cudaSuccess)) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1, 1);
+    cfg.gridDim = dim3(size, 1, 1);
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.dynamicSmemBytes = kAttnSmemCluster;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.x = size;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) result = 16;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
-  cached[dev] = result;
-  return result;
+  cached[dev][si] = n + 1;
+  return n;
 }
+
+int attn_max_cluster() { return attn_cluster_capacity(16) >= 1 ? 16 : 8; }
 
 cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int out_dtype,
                              const CUtensorMap& tm_k, const CUtensorMap& tm_v, cudaStream_t stream) {

@@ -261,6 +261,10 @@ void choose_split(const dsa_problem* p, const Derived& d, int sms, int* split_ke
     const int s_min = ceil_div(d.kmax, kAttnMaxSplitKeys);
     int s2 = 1;
     while (s2 * 2 <= s) s2 *= 2;
+    // clusters that do not all fit at once would run in a second wave:
+    // halve the split count while the units need more clusters than fit
+    while (s2 > 2 && s2 / 2 >= s_min && attn_uses_cluster(s2) && units > attn_cluster_capacity(s2))
+      s2 /= 2;
     while (s2 < s_min) s2 *= 2;
     s = s2;
     sk = ceil_div(ceil_div(d.kmax, s), 16) * 16;

@@ -211,6 +211,9 @@ cudaError_t launch_attention(const AttnParams& p, int q_dtype, int kv_dtype, int
 // (16 if a 16-CTA cluster can be placed, else 8), and whether a split count
 // is merged inside a cluster.
 int attn_max_cluster();
+// Clusters of `size` attention CTAs (2, 4, 8 or 16) resident at once on this
+// device (0 if none fits or the size is not one of those).
+int attn_cluster_capacity(int size);
 inline bool attn_uses_cluster(int nsplit) {
   return (nsplit == 2 || nsplit == 4 || nsplit == 8 || nsplit == 16) && nsplit <= attn_max_cluster();
 }

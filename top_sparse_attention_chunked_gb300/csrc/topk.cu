@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
   for (int i = ri.keff + threadIdx.x; i < p.k; i += kRowThreads) out[i] = -1;
 }
 
-constexpr int kClThreads = 512;
+constexpr int kClThreads = 512;   // cluster select CTA size with 16 or 32 keys a thread (1,024 with 8)
 // Candidates gathered into every CTA of the cluster: 8,192, or 4,096 for the
 // shortest slices, whose CTAs then fit two to an SM (many short rows, as in
 // grouped decode, run in one wave).
@@ -979,25 +979,27 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
 }
 
 // ---------------------------------------------------------------------------
-// 2b. cluster select: one thread-block cluster of up to 8 CTAs per row. Each
-// CTA holds a contiguous slice of the row's keys in shared memory. From the
+// 2b. cluster select: one thread-block cluster of up to 16 CTAs per row. Each
+// CTA holds a contiguous slice of the row's keys in registers. From the
 // row histogram every CTA finds the threshold bin and compacts its keys in
-// that bin (the candidates, usually a few hundred). The exact threshold
-// composite (key << 32 | ~index) is then refined 8 bits at a time over the
-// candidates only, summing the CTAs' digit histograms through distributed
-// shared memory. Finally each CTA emits its own slice in ascending order (one
-// block scan) at the offset given by the peers' selected counts. No global
-// scratch beyond the histogram and no serial tail.
+// that bin (the candidates, usually a few hundred to a few thousand). Every
+// CTA gathers all candidates through distributed shared memory and resolves
+// the exact threshold composite (key << 32 | ~index) locally in 11-bit digit
+// rounds; with more candidates than the gather holds (heavy ties) the digits
+// are refined 8 bits at a time with the CTAs' digit histograms summed through
+// distributed shared memory. Finally each CTA emits its own slice in ascending
+// order (one block scan) at the offset given by the peers' selected counts. No
+// global scratch beyond the histogram and no serial tail.
 // ---------------------------------------------------------------------------
-// Each thread owns PER consecutive keys of the slice, held in registers
-// (PER = 8, 16 or 32), so the emit needs a single block scan and no
-// shared-memory bank conflicts arise; the threshold-bin candidates go to
-// shared memory.
-template <int PER>
-__global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_select_kernel(const TopkParams p) {
+// Each of the NT threads owns PER consecutive keys of the slice, held in
+// registers (PER = 8 with 1,024 threads, 16 or 32 with 512), so the emit needs
+// a single block scan and no shared-memory bank conflicts arise; the
+// threshold-bin candidates go to shared memory.
+template <int PER, int NT>
+__global__ void __launch_bounds__(NT, (PER <= 8 && NT <= 512) ? 2 : 1) topk_cluster_select_kernel(const TopkParams p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  constexpr int kSlice = PER * kClThreads;
+  constexpr int kSlice = PER * NT;
   extern __shared__ unsigned long long scand[];  // candidate composites of this CTA
   __shared__ __align__(16) uint32_t h[kHistBins];   // row histogram, then digit counts
   __shared__ uint32_t hloc[kHistBins];           // this CTA's slice histogram
@@ -1046,14 +1048,14 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
     // ---- the row histogram came with the scores (indexer epilogue)
     const uint32_t* gh = p.hist + static_cast<size_t>(rl) * kHistBins;
 #pragma unroll
-    for (int u = 0; u < kHistBins / kClThreads; ++u)
-      h[u * kClThreads + threadIdx.x] = __ldcg(gh + u * kClThreads + threadIdx.x);
+    for (int u = 0; u < kHistBins / NT; ++u)
+      h[u * NT + threadIdx.x] = __ldcg(gh + u * NT + threadIdx.x);
     __syncthreads();
   } else {
     // ---- the row histogram of the top 11 key bits, built by the cluster:
     // each CTA counts its slice, each CTA then sums one range of bins over all
     // peers, and every CTA reads the summed ranges back
-    for (int i = threadIdx.x; i < kHistBins; i += kClThreads) hloc[i] = 0u;
+    for (int i = threadIdx.x; i < kHistBins; i += NT) hloc[i] = 0u;
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < PER; ++j)
@@ -1061,7 +1063,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
     cluster.sync();                              // every CTA's slice histogram is complete
     {
       const int b0 = rank * kHistBins / ncta, b1 = (rank + 1) * kHistBins / ncta;
-      for (int b = b0 + static_cast<int>(threadIdx.x); b < b1; b += kClThreads) {
+      for (int b = b0 + static_cast<int>(threadIdx.x); b < b1; b += NT) {
         uint32_t tot = 0;
         for (int q = 0; q < ncta; ++q) tot += cluster.map_shared_rank(hloc, q)[b];
         hred[b] = tot;
@@ -1069,8 +1071,8 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
     }
     cluster.sync();                              // every range is summed
 #pragma unroll
-    for (int u = 0; u < kHistBins / kClThreads; ++u) {
-      const int b = u * kClThreads + threadIdx.x;
+    for (int u = 0; u < kHistBins / NT; ++u) {
+      const int b = u * NT + threadIdx.x;
       const int owner = ((b + 1) * ncta - 1) / kHistBins;
       h[b] = cluster.map_shared_rank(hred, owner)[b];
     }
@@ -1078,7 +1080,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
   }
   if (threadIdx.x == 0) DSA_TS(2);
   // ---- threshold bin: a block-wide scan of the histogram
-  find_threshold_digit<kClThreads>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
+  find_threshold_digit<NT>(h, kHistBins, static_cast<uint32_t>(ri.keff), warp_tot, &s_d,
                                    &s_above, &s_cnt);
   if (threadIdx.x == 0) DSA_TS(3);
   const uint32_t bin = static_cast<uint32_t>(s_d);
@@ -1134,7 +1136,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
   int off_mine = 0;                              // gathered candidates of lower ranks
   if (gather) {
     // ---- every CTA gathers all candidates and counts, then resolves locally
-    unsigned long long* sg = scand + PER * kClThreads;   // gathered candidates
+    unsigned long long* sg = scand + PER * NT;   // gathered candidates
     if (threadIdx.x < ncta) {
       s_pc[threadIdx.x] = ld_cluster_u32(cluster_map(&s_ncand, threadIdx.x));
       s_ps[threadIdx.x] = ld_cluster_u32(cluster_map(&s_nsure, threadIdx.x));
@@ -1174,7 +1176,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (threadIdx.x == 0) DSA_TS(5);
     if (!all0)
-      resolve_composites<kClThreads>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
+      resolve_composites<NT>(sg, off, &prefix, &mask, need, h, warp_tot, &s_d, &s_above,
                                      &s_cnt, 52);
   } else {
     // ---- many candidates (heavy ties): refine the threshold 8 bits at a time,
@@ -1188,7 +1190,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
       if (threadIdx.x < 256) hd[threadIdx.x] = 0u;
       __syncthreads();
       const int cround = ((static_cast<int>(ncand) + 31) / 32) * 32;   // whole warps take part
-      for (int c = threadIdx.x; c < cround; c += kClThreads) {
+      for (int c = threadIdx.x; c < cround; c += NT) {
         uint32_t dg = 0xFFFFFFFFu;
         if (c < static_cast<int>(ncand)) {
           const unsigned long long cc = scand[c];
@@ -1204,7 +1206,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
       }
       if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
       __syncthreads();
-      find_threshold_digit<kClThreads>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
+      find_threshold_digit<NT>(h, 1 << w, need, warp_tot, &s_d, &s_above, &s_cnt);
       need -= s_above;
       prefix |= static_cast<unsigned long long>(s_d) << sh;
       mask |= static_cast<unsigned long long>(dm) << sh;
@@ -1238,11 +1240,11 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
   }
   uint32_t lower = 0;
   if (gather && !all0) {
-    const unsigned long long* sg = scand + PER * kClThreads;
-    for (int c = threadIdx.x; c < off_mine; c += kClThreads) lower += (sg[c] & mask) >= prefix ? 1u : 0u;
+    const unsigned long long* sg = scand + PER * NT;
+    for (int c = threadIdx.x; c < off_mine; c += NT) lower += (sg[c] & mask) >= prefix ? 1u : 0u;
   }
   uint32_t total;
-  const uint32_t packed = block_exclusive_scan<kClThreads>(mine | (lower << 16), warp_tot, &total);
+  const uint32_t packed = block_exclusive_scan<NT>(mine | (lower << 16), warp_tot, &total);
   if (threadIdx.x == 0) DSA_TS(7);
   pos += (packed & 0xFFFFu) + (total >> 16);
   if (!gather) {
@@ -1276,7 +1278,7 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
     }
   }
   if (rank == 0)
-    for (int i = ri.keff + threadIdx.x; i < p.k; i += kClThreads) out[i] = -1;
+    for (int i = ri.keff + threadIdx.x; i < p.k; i += NT) out[i] = -1;
   if (gather) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   else cluster.sync();                           // peers may still read this CTA's s_count
   if (threadIdx.x == 0) DSA_TS(8);
@@ -1285,11 +1287,15 @@ __global__ void __launch_bounds__(kClThreads, PER <= 8 ? 2 : 1) topk_cluster_sel
 
 // Cluster shape for rows of up to max_n keys: keys per thread and CTAs per
 // row (0 CTAs: the row is too long for the cluster select).
+// Threads of a cluster-select CTA holding `per` keys a thread: 1,024 with 8
+// (64 registers), else 512 (the keys need more registers than 1,024 threads
+// leave).
+static int cl_threads(int per) { return per == 8 ? 1024 : kClThreads; }
 static void cluster_shape(int max_n, int* per, int* ctas) {
   // as few keys per thread as up to 16 CTAs allow: the slice load from L2 and
   // the per-thread work shrink with the slice
-  *per = max_n <= 16 * 8 * kClThreads ? 8 : max_n <= 16 * 16 * kClThreads ? 16 : 32;
-  *ctas = (max_n + *per * kClThreads - 1) / (*per * kClThreads);
+  *per = max_n <= 16 * 8 * 1024 ? 8 : max_n <= 16 * 16 * kClThreads ? 16 : 32;
+  *ctas = (max_n + *per * cl_threads(*per) - 1) / (*per * cl_threads(*per));
   if (*ctas > kTopkClusterMax) *ctas = 0;
 }
 
@@ -1302,9 +1308,9 @@ bool topk_cluster_feasible(int max_n) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   const int pi = per == 8 ? 0 : per == 16 ? 1 : 2;
   if (cached[dev][pi]) return cached[dev][pi] == 1;
-  const size_t smem = (static_cast<size_t>(per) * kClThreads + cl_gather_max(per)) * sizeof(unsigned long long);
-  auto kern = per == 8 ? topk_cluster_select_kernel<8>
-            : per == 16 ? topk_cluster_select_kernel<16> : topk_cluster_select_kernel<32>;
+  const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
+  auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
+            : per == 16 ? topk_cluster_select_kernel<16, 512> : topk_cluster_select_kernel<32, 512>;
   bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) == cudaSuccess &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
@@ -1312,7 +1318,7 @@ bool topk_cluster_feasible(int max_n) {
   if (ok) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16, 1);
-    cfg.blockDim = dim3(kClThreads);
+    cfg.blockDim = dim3(cl_threads(per));
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1341,9 +1347,9 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   cluster_shape(max_n, &per, &ctas);
   if (ctas == 0) return cudaErrorInvalidValue;
   // worst case every key of the slice is a candidate; then the gathered list
-  const size_t smem = (static_cast<size_t>(per) * kClThreads + cl_gather_max(per)) * sizeof(unsigned long long);
-  auto kern = per == 8 ? topk_cluster_select_kernel<8>
-            : per == 16 ? topk_cluster_select_kernel<16> : topk_cluster_select_kernel<32>;
+  const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
+  auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
+            : per == 16 ? topk_cluster_select_kernel<16, 512> : topk_cluster_select_kernel<32, 512>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1353,7 +1359,7 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, p.nrows);
-  cfg.blockDim = dim3(kClThreads);
+  cfg.blockDim = dim3(cl_threads(per));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
   for (int i = ri.keff + threadIdx.x; i < p.k; i += kRowThreads) out[i] = -1;
 }
 
-constexpr int kClThreads = 512;   // cluster select CTA size with 16 or 32 keys a thread (1,024 with 8)
+constexpr int kClThreads = 512;   // cluster select CTA size with 32 keys a thread (1,024 with 8 or 16)
 // Candidates gathered into every CTA of the cluster: 8,192, or 4,096 for the
 // shortest slices, whose CTAs then fit two to an SM (many short rows, as in
 // grouped decode, run in one wave).
@@ -992,7 +992,7 @@ cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
 // global scratch beyond the histogram and no serial tail.
 // ---------------------------------------------------------------------------
 // Each of the NT threads owns PER consecutive keys of the slice, held in
-// registers (PER = 8 with 1,024 threads, 16 or 32 with 512), so the emit needs
+// registers (PER = 8 or 16 with 1,024 threads, 32 with 512), so the emit needs
 // a single block scan and no shared-memory bank conflicts arise; the
 // threshold-bin candidates go to shared memory.
 template <int PER, int NT>
@@ -1287,14 +1287,14 @@ __global__ void __launch_bounds__(NT, (PER <= 8 && NT <= 512) ? 2 : 1) topk_clus
 
 // Cluster shape for rows of up to max_n keys: keys per thread and CTAs per
 // row (0 CTAs: the row is too long for the cluster select).
-// Threads of a cluster-select CTA holding `per` keys a thread: 1,024 with 8
-// (64 registers), else 512 (the keys need more registers than 1,024 threads
-// leave).
-static int cl_threads(int per) { return per == 8 ? 1024 : kClThreads; }
+// Threads of a cluster-select CTA holding `per` keys a thread: 1,024 with 8 or
+// 16 (64 registers, no spills), 512 with 32 (the keys need more registers
+// than 1,024 threads leave).
+static int cl_threads(int per) { return per <= 16 ? 1024 : kClThreads; }
 static void cluster_shape(int max_n, int* per, int* ctas) {
   // as few keys per thread as up to 16 CTAs allow: the slice load from L2 and
   // the per-thread work shrink with the slice
-  *per = max_n <= 16 * 8 * 1024 ? 8 : max_n <= 16 * 16 * kClThreads ? 16 : 32;
+  *per = max_n <= 16 * 8 * 1024 ? 8 : max_n <= 16 * 16 * 1024 ? 16 : 32;
   *ctas = (max_n + *per * cl_threads(*per) - 1) / (*per * cl_threads(*per));
   if (*ctas > kTopkClusterMax) *ctas = 0;
 }
@@ -1310,7 +1310,7 @@ bool topk_cluster_feasible(int max_n) {
   if (cached[dev][pi]) return cached[dev][pi] == 1;
   const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
   auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
-            : per == 16 ? topk_cluster_select_kernel<16, 512> : topk_cluster_select_kernel<32, 512>;
+            : per == 16 ? topk_cluster_select_kernel<16, 1024> : topk_cluster_select_kernel<32, 512>;
   bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) == cudaSuccess &&
             cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
@@ -1349,7 +1349,7 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   // worst case every key of the slice is a candidate; then the gathered list
   const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
   auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
-            : per == 16 ? topk_cluster_select_kernel<16, 512> : topk_cluster_select_kernel<32, 512>;
+            : per == 16 ? topk_cluster_select_kernel<16, 1024> : topk_cluster_select_kernel<32, 512>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

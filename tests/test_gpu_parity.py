@@ -232,6 +232,29 @@ def test_prefill_fp16_query_fp16_cache(dsa):
     check_step(wl, cpu, idx, out)
 
 
+@pytest.mark.parametrize("qd", ["bf16", "fp16"])
+def test_prefill_int8_ragged(dsa, qd):
+    """INT8 prefill with a BF16 or FP16 query, ragged lengths and more
+    selected keys than one 128-key tile."""
+    wl = small_workload(batch=2, q_len=70, total_len=3000, capacity=3100, num_q_heads=24,
+                        num_kv_heads=2, top_k=600, q_dtype=qd, kv_dtype="int8", seed=47)
+    cpu = make_inputs(wl)
+    cpu["total_len"] = torch.tensor([3000, 2200], dtype=torch.int32)
+    cpu, idx, out = run_step(dsa, wl, cpu=cpu, prefill=True, total_len=[3000, 2200])
+    check_step(wl, cpu, idx, out)
+
+
+def test_prefill_int8_8k_on_32k_sampled(dsa):
+    """The prefill workload's shape with an INT8 cache, on 8 sampled rows."""
+    base = WORKLOADS["prefill_8k_on_32k"]
+    wl = Workload("prefill_int8", base.batch, base.q_len, base.total_len, base.num_q_heads,
+                  base.num_kv_heads, base.top_k, base.q_dtype, "int8", seed=base.seed)
+    cpu, idx, out = run_step(dsa, wl, prefill=True)
+    rng = np.random.default_rng(1)
+    rows = sorted({0, wl.q_len - 1, *rng.integers(0, wl.q_len, 6).tolist()})
+    check_step(wl, cpu, idx, out, rows=[(0, s) for s in rows])
+
+
 def test_prefill_and_decode_agree(dsa):
     """The same 8 query tokens through the decode path and the prefill path."""
     wl = small_workload(batch=2, q_len=8, total_len=6000, num_q_heads=24, num_kv_heads=2,
@@ -324,6 +347,29 @@ def test_int8_large_value_scale_worked_example(dsa, spacing, split):
     cpu.update(k=k, v=v, k_scale=ks, v_scale=torch.full((1, m, 1), 2.0 ** 120))
     _, idx, out = run_step(dsa, wl, cpu=cpu, softmax_scale=1.0, out_dtype="fp32",
                            attn_split_keys=split)
+    expect = 2.0 ** 120 * math.exp(-88) / (1 + math.exp(-88))
+    np.testing.assert_allclose(out[0, 0, 0], expect, rtol=2e-5)
+
+
+@pytest.mark.parametrize("spacing", [0, 126, 127, 300])
+def test_int8_large_value_scale_worked_example_prefill(dsa, spacing):
+    """PR #33847's case through the prefill call: the two candidates in one
+    128-key stretch or far apart."""
+    m = 2 + spacing
+    wl = Workload("worked_pf", 1, 1, m, 1, 1, m, "bf16", "int8", seed=1)
+    cpu = make_inputs(wl)
+    q = torch.zeros(1, 1, 1, 128)
+    q[0, 0, 0, 0] = 88.0
+    cpu["q"] = q.to(torch.bfloat16)
+    k = torch.zeros(1, m, 1, 128, dtype=torch.int8)
+    k[0, m - 1, 0, 0] = 1
+    k[0, 1:m - 1, 0, 0] = -1
+    ks = torch.ones(1, m, 1)
+    ks[0, 1:m - 1, 0] = 1000.0 / 88.0
+    v = torch.zeros(1, m, 1, 128, dtype=torch.int8)
+    v[0, 0, 0, :] = 1
+    cpu.update(k=k, v=v, k_scale=ks, v_scale=torch.full((1, m, 1), 2.0 ** 120))
+    _, idx, out = run_step(dsa, wl, cpu=cpu, prefill=True, softmax_scale=1.0, out_dtype="fp32")
     expect = 2.0 ** 120 * math.exp(-88) / (1 + math.exp(-88))
     np.testing.assert_allclose(out[0, 0, 0], expect, rtol=2e-5)
 

@@ -792,14 +792,14 @@ static cudaError_t launch_t(const AttnParams& p, const CUtensorMap& tm_k, const 
                             cudaStream_t stream) {
   auto kern = sparse_attn_kernel<KV, Q_F16, OUT>;
   const int smem = p.cluster ? kAttnSmemCluster : kAttnSmem;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.nsplit, p.Hkv * p.HG, p.B * p.S);
   if (!p.cluster)
     return launch_kernel("sparse_attn_kernel", kern, grid, dim3(kAttnThreads), smem, stream, true,
                          tm_k, tm_v, p);
   if (p.nsplit > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = set_nonportable_cluster(reinterpret_cast<const void*>(kern));
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -844,10 +844,8 @@ int attn_cluster_capacity(int size) {
   if (cached[dev][si]) return cached[dev][si] - 1;
   int n = 0;
   auto kern = sparse_attn_kernel<KV_FP16, false, DSA_BF16>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemCluster) ==
-          cudaSuccess &&
-      (size <= 8 || cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                        cudaSuccess)) {
+  if (set_max_smem(reinterpret_cast<const void*>(kern), kAttnSmemCluster) == cudaSuccess &&
+      (size <= 8 || set_nonportable_cluster(reinterpret_cast<const void*>(kern)) == cudaSuccess)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size, 1, 1);
     cfg.blockDim = dim3(kAttnThreads);

@@ -108,8 +108,40 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Encoded maps of this thread's recent calls: an encoding is a pure function
+// of (kind, base, rows, box rows), and the same caches and query buffers come
+// back call after call, so a hit skips the driver call.
+struct MapCacheEntry {
+  int kind;
+  const void* base;
+  long long rows;
+  int box_rows;
+  CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+thread_local MapCacheEntry g_map_cache[kMapCache];
+thread_local int g_map_cache_n = 0, g_map_cache_next = 0;
+
+bool map_cached(int kind, const void* base, long long rows, int box_rows, CUtensorMap* m) {
+  for (int i = 0; i < g_map_cache_n; ++i) {
+    const MapCacheEntry& e = g_map_cache[i];
+    if (e.kind == kind && e.base == base && e.rows == rows && e.box_rows == box_rows) {
+      *m = e.map;
+      return true;
+    }
+  }
+  return false;
+}
+void map_remember(int kind, const void* base, long long rows, int box_rows, const CUtensorMap& m) {
+  MapCacheEntry& e = g_map_cache[g_map_cache_next];
+  e = MapCacheEntry{kind, base, rows, box_rows, m};
+  g_map_cache_next = (g_map_cache_next + 1) % kMapCache;
+  if (g_map_cache_n < kMapCache) ++g_map_cache_n;
+}
+
 // rows x 64 bf16 matrix, box of box_rows x 64, 128-byte swizzle
 int make_map_rows64(CUtensorMap* m, const void* base, long long rows, int box_rows) {
+  if (map_cached(0, base, rows, box_rows, m)) return DSA_OK;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(DSA_IDX_DIM), static_cast<cuuint64_t>(rows)};
@@ -120,12 +152,14 @@ int make_map_rows64(CUtensorMap* m, const void* base, long long rows, int box_ro
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  map_remember(0, base, rows, box_rows, *m);
   return DSA_OK;
 }
 
 // rows x 128 16-bit matrix (one KV head of one token per row), box 64 x 1,
 // 128-byte swizzle: the source of TMA row gathers
 int make_map_kv_rows(CUtensorMap* m, const void* base, long long rows) {
+  if (map_cached(1, base, rows, 1, m)) return DSA_OK;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(DSA_HEAD_DIM), static_cast<cuuint64_t>(rows)};
@@ -136,6 +170,7 @@ int make_map_kv_rows(CUtensorMap* m, const void* base, long long rows) {
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DSA_ERR_CUDA, "cuTensorMapEncodeTiled (KV rows) failed (%d)", (int)r);
+  map_remember(1, base, rows, 1, *m);
   return DSA_OK;
 }
 
@@ -746,6 +781,58 @@ int attn_entry(const dsa_problem* p, int op, const dsa_kv_pages* pages, const vo
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------ kernel attributes
+namespace {
+using CtxGetCurrentFn2 = int (*)(void**);   // cuCtxGetCurrent(CUcontext*)
+CtxGetCurrentFn2 ctx_current_fn() {
+  static CtxGetCurrentFn2 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn2>(f);
+  });
+  return fn;
+}
+struct AttrEntry {
+  const void* kern;
+  void* ctx;
+  int attr, value;
+};
+std::mutex g_attr_mu;
+AttrEntry g_attr[256];
+int g_attr_n = 0;
+
+cudaError_t set_attr_once(const void* kern, cudaFuncAttribute attr, int value) {
+  void* ctx = nullptr;
+  CtxGetCurrentFn2 fn = ctx_current_fn();
+  if (!fn || fn(&ctx) != 0 || !ctx) return cudaFuncSetAttribute(kern, attr, value);
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  for (int i = 0; i < g_attr_n; ++i) {
+    AttrEntry& e = g_attr[i];
+    if (e.kern == kern && e.ctx == ctx && e.attr == static_cast<int>(attr)) {
+      if (e.value == value) return cudaSuccess;
+      const cudaError_t r = cudaFuncSetAttribute(kern, attr, value);
+      if (r == cudaSuccess) e.value = value;
+      return r;
+    }
+  }
+  const cudaError_t r = cudaFuncSetAttribute(kern, attr, value);
+  if (r == cudaSuccess && g_attr_n < 256) g_attr[g_attr_n++] = AttrEntry{kern, ctx, static_cast<int>(attr), value};
+  return r;
+}
+}  // namespace
+
+cudaError_t set_max_smem(const void* kern, int bytes) {
+  return set_attr_once(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+cudaError_t set_nonportable_cluster(const void* kern) {
+  return set_attr_once(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
 
 // ------------------------------------------------------------------ no-alloc top-k helpers
 int noalloc_fail(int status, const char* msg) { return fail(status, "%s", msg); }

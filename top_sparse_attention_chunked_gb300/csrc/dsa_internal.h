@@ -16,6 +16,12 @@ namespace dsa {
 void note_launch(const char* name);
 void reset_launches();
 
+// cudaFuncSetAttribute(kern, MaxDynamicSharedMemorySize, bytes) and
+// (NonPortableClusterSizeAllowed, 1), each issued once per kernel, CUDA
+// context and value: a driver call per launch costs host time on every call.
+cudaError_t set_max_smem(const void* kern, int bytes);
+cudaError_t set_nonportable_cluster(const void* kern);
+
 // Launch `kern` (recorded as `name`) on `stream`; with `pdl` the launch may overlap the tail of the
 // previous kernel in the stream (the kernel calls pdl_wait() before reading
 // what that kernel wrote).

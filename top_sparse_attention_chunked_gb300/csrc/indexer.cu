@@ -461,8 +461,7 @@ static cudaError_t launch_n(const IndexerParams& p, const CUtensorMap& tm_kI,
                             const CUtensorMap& tm_qI, dim3 grid, size_t smem, int stages,
                             cudaStream_t stream) {
   auto kern = indexer_tc_kernel<N, HIST>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // with histograms the kernel follows the scratch-clearing kernel and waits
   // for it only before its final flush

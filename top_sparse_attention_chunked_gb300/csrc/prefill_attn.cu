@@ -469,8 +469,7 @@ static cudaError_t launch_prefill_variant(const AttnParams& p, int grid, const C
                                           const CUtensorMap& tm_v, long long n_items,
                                           uint32_t* status, cudaStream_t stream) {
   auto k = sparse_attn_prefill_tc_kernel<F16, PAGED>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(pf::kSmemBytes));
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(k), static_cast<int>(pf::kSmemBytes));
   if (e != cudaSuccess) return e;
   return launch_kernel("sparse_attn_prefill_tc_kernel", k, dim3(grid), dim3(pf::kThreads),
                        pf::kSmemBytes, stream, true, tm_k, tm_v, p, n_items, status);

@@ -933,9 +933,7 @@ int topk_row_stream_max_len() { return kRsMaxLen; }
 cudaError_t launch_topk_row_stream(const TopkParams& p, int max_n, bool pdl, cudaStream_t stream) {
   if (max_n > kRsMaxLen) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>((max_n + 31) / 32) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_row_stream_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(topk_row_stream_kernel), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_kernel("topk_row_stream_kernel", topk_row_stream_kernel, dim3(p.nrows),
                        dim3(kRsThreads), smem, stream, pdl, p);
@@ -970,9 +968,7 @@ cudaError_t launch_topk_hist(const TopkParams& p, cudaStream_t stream) {
 
 cudaError_t launch_topk_chunk_select(const TopkParams& p, cudaStream_t stream) {
   const size_t smem = kCandSmem * sizeof(unsigned long long);
-  cudaError_t e = cudaFuncSetAttribute(topk_chunk_select_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(topk_chunk_select_kernel), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_kernel("topk_chunk_select_kernel", topk_chunk_select_kernel, dim3(p.nchunks, p.nrows), dim3(kSelThreads), smem,
                        stream, true, p);
@@ -1311,10 +1307,8 @@ bool topk_cluster_feasible(int max_n) {
   const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
   auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
             : per == 16 ? topk_cluster_select_kernel<16, 1024> : topk_cluster_select_kernel<32, 512>;
-  bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) == cudaSuccess &&
-            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                cudaSuccess;
+  bool ok = set_max_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) == cudaSuccess &&
+            set_nonportable_cluster(reinterpret_cast<const void*>(kern)) == cudaSuccess;
   if (ok) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16, 1);
@@ -1350,11 +1344,10 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
   auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
             : per == 16 ? topk_cluster_select_kernel<16, 1024> : topk_cluster_select_kernel<32, 512>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (ctas > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = set_nonportable_cluster(reinterpret_cast<const void*>(kern));
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1381,9 +1374,7 @@ cudaError_t launch_topk_row(const TopkParams& p, int max_n, size_t smem_limit, b
                             cudaStream_t stream) {
   const size_t smem = (static_cast<size_t>((max_n + 3) & ~3) + kHistBins) * sizeof(uint32_t);
   if (smem + 1024 > smem_limit) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(topk_row_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(topk_row_kernel), static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_kernel("topk_row_kernel", topk_row_kernel, dim3(p.B * p.S), dim3(kRowThreads), smem, stream, pdl, p);
 }

@@ -209,23 +209,33 @@ def problem_for(wl, **overrides) -> DsaProblem:
 
 
 def _ptr(t: Optional[torch.Tensor], name: str, dtype=None, shape=None):
+    """The device address of a checked tensor (an int; ctypes passes it as a
+    void pointer). The checks are ordered and written for a low per-call cost:
+    the step calls run once per layer and token."""
     if t is None:
         return None
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and t.shape != shape:
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
-        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream) -> int:
+    """The CUDA stream to enqueue on: the given one, else the current stream
+    of the current device (read without building a stream object)."""
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device())
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def dsa_workspace_size(p: DsaProblem, op: int) -> int:
@@ -259,8 +269,8 @@ def make_pages(block_table: torch.Tensor, block_size: int, num_blocks: int) -> D
 def _kv_ptr(p: DsaProblem, t, name, dtype, shape):
     """A K / V cache pointer: the default layout is checked by shape; with
     kv_strides the tensor only has to be contiguous and hold the last row."""
-    st = list(p.kv_strides)
-    if not any(st):
+    st = p.kv_strides
+    if not (st[0] or st[1] or st[2]):
         return _ptr(t, name, dtype, shape)
     ptr = _ptr(t, name, dtype)
     last = (p.batch - 1) * st[0] + (p.cache_capacity - 1) * st[1] + (p.num_kv_heads - 1) * st[2] + 128
@@ -372,10 +382,10 @@ def dsa_rope_append(p: DsaProblem, q, qI, k_new, kI_new, v_new, kI, k, v, k_scal
                        None if cos is None else cos.data_ptr(), None if sin is None else sin.data_ptr(),
                        None if cos_index is None else cos_index.data_ptr(),
                        None if sin_index is None else sin_index.data_ptr(),
-                       _ptr(gamma_q, "gamma_q", torch.float32, (128,)).value,
-                       _ptr(gamma_k, "gamma_k", torch.float32, (128,)).value,
-                       _ptr(gamma_qI, "gamma_qI", torch.float32, (64,)).value,
-                       _ptr(gamma_kI, "gamma_kI", torch.float32, (64,)).value)
+                       _ptr(gamma_q, "gamma_q", torch.float32, (128,)),
+                       _ptr(gamma_k, "gamma_k", torch.float32, (128,)),
+                       _ptr(gamma_qI, "gamma_qI", torch.float32, (64,)),
+                       _ptr(gamma_kI, "gamma_kI", torch.float32, (64,)))
     for t, n in ((cos, "cos"), (sin, "sin"), (cos_index, "cos_index"), (sin_index, "sin_index")):
         _ptr(t, n)
     _check(lib.dsa_rope_append(

@@ -91,6 +91,32 @@ def test_index_scores_parity(dsa, B, S, T, cap):
             assert (got[b, s, n:] == -7.25).all(), "wrote past the visible length"
 
 
+def test_index_scores_split_query_bit_exact(dsa):
+    """Blocks of 16 queries split their queries between the two epilogue
+    groups, hold the head weights in registers and take half of the heads'
+    ReLU as x + |x| against halved weights; a block of one query reads the
+    weights from shared memory and uses max(x, 0). For finite dot products
+    the two give the same real products, summed in the same order, so every
+    visible score must match bit for bit: each of 16 queries is scored alone,
+    on a cache cut to the keys it sees inside the block."""
+    S, T, cap = 16, 3001, 3001
+    wl = small_workload(batch=1, q_len=S, total_len=T, capacity=cap, top_k=8, seed=77)
+    cpu = make_inputs(wl)
+    dev = to_device(cpu)
+    p = dsa.problem_for(wl, total_len=[T])
+    blk = torch.full((1, S, cap), -7.25, dtype=torch.float32, device="cuda")
+    dsa.dsa_index_scores(p, dev["qI"], dev["w"], dev["kI"], blk, dsa.alloc_workspace(p, dsa.DSA_OP_INDEX_SCORES))
+    wl1 = small_workload(batch=1, q_len=1, total_len=T, capacity=cap, top_k=8, seed=77)
+    for s in range(S):
+        n = O.visible_len(T, S, s)
+        p1 = dsa.problem_for(wl1, total_len=[n])
+        one = torch.full((1, 1, cap), -7.25, dtype=torch.float32, device="cuda")
+        dsa.dsa_index_scores(p1, dev["qI"][:, s:s + 1].contiguous(), dev["w"][:, s:s + 1].contiguous(),
+                             dev["kI"], one, dsa.alloc_workspace(p1, dsa.DSA_OP_INDEX_SCORES))
+        a, b = blk[0, s, :n].cpu(), one[0, 0, :n].cpu()
+        assert torch.equal(a, b), f"query {s}: {int((a != b).sum())} of {n} scores differ"
+
+
 def test_index_scores_full_128k(dsa):
     wl = WORKLOADS["decode_128k"]
     cpu = make_inputs(wl)

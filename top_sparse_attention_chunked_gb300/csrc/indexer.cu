@@ -19,12 +19,25 @@
 // and prefill (QB = 16, N = 256, causal: tile ranges stop at each block's
 // last visible key).
 //
-// Warp roles (192 threads): warp 0 issues TMA loads into a ring of shared
-// stages, warp 1 owns tensor memory and issues the MMAs, warps 2-5 are the
-// epilogue (warp w reads TMEM lanes 32*(w%4) .. +31). Accumulators are
-// double-buffered in TMEM so the MMA of tile i+1 overlaps the epilogue of
-// tile i. Work is a flat list of (sequence, query block, key tile) units split
-// evenly over a persistent grid of one CTA per SM.
+// Warp roles (320 threads): warp 0 issues TMA loads into a ring of shared
+// stages, warp 1 owns tensor memory and issues the MMAs, warps 2-9 are two
+// epilogue groups of 4 warps (warp w reads TMEM lanes 32*(w%4) .. +31).
+// Accumulators are double-buffered in TMEM so the MMA of tile i+1 overlaps
+// the epilogue of tile i. Two epilogue organisations:
+//   * alternate tiles (decode, histograms, blocks under 8 queries): group g
+//     takes the tiles of parity g with all of the block's queries, head
+//     weights read from shared memory;
+//   * split queries (blocks of 8 or 16 queries without histograms, i.e.
+//     prefill): both groups read every tile, group g taking half of the
+//     block's queries, with those queries' head weights held in registers
+//     across the block's tiles. At K = 64 the epilogue has about as many
+//     instructions per tile as the MMA has cycles, so it sets the pace: a
+//     warp-wide broadcast read of the weights from shared memory costs
+//     several shared-pipe wavefronts per 16 bytes, enough to saturate that
+//     pipe, and half of the heads take their ReLU on the FMA pipe (see
+//     relu_weighted_sum_r) to relieve the half-rate ALU pipe.
+// Work is a flat list of (sequence, query block, key tile) units split evenly
+// over a persistent grid of one CTA per SM.
 #include <cstdio>
 
 #include "dsa_common.cuh"
@@ -33,8 +46,6 @@
 
 namespace dsa {
 
-constexpr int kIdxThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 two epilogue groups
-constexpr int kIdxEpiThreads = 256;
 constexpr int kMaxAcc = 4;
 constexpr int kIdxMaxStages = 8;
 constexpr uint32_t kATileBytes = kKeyTile * DSA_IDX_DIM * 2;   // 16 KB
@@ -73,6 +84,39 @@ __device__ __forceinline__ void advance_unit(const IndexerParams& p, UnitCursor&
   } while (c.ntiles == 0);
 }
 
+// sum over heads of w_h * ReLU(dot_h), two heads per paired FMA, with the
+// weights in registers. For the first kAbsHeads heads the weight is held
+// halved (hw = w / 2) and ReLU(x) is taken as x + |x|: for finite x that is
+// exactly 2 * ReLU(x), and (w / 2) * (2 * ReLU(x)) is the same real product
+// as w * ReLU(x), so the sum rounds exactly as with max(x, 0) throughout. The
+// addition (|x| is a free source modifier) runs on the FMA pipe, where a max
+// takes a slot of the half-rate ALU pipe.
+// heads whose ReLU is taken as x + |x| (FMA pipe) with a halved weight; the
+// rest use max(x, 0) (ALU pipe), which balances the two pipes
+constexpr int kAbsHeads = 8;
+__device__ __forceinline__ float relu2(float x, int h) { return h < kAbsHeads ? x + fabsf(x) : fmaxf(x, 0.0f); }
+__device__ __forceinline__ float relu_weighted_sum_r(const float (&d)[16], const float (&hw)[16]) {
+  float2 acc2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int h2 = 0; h2 < DSA_IDX_HEADS / 2; ++h2)
+    acc2 = fma_f32x2(make_float2(hw[2 * h2], hw[2 * h2 + 1]),
+                     make_float2(relu2(d[2 * h2], 2 * h2), relu2(d[2 * h2 + 1], 2 * h2 + 1)), acc2);
+  return acc2.x + acc2.y;
+}
+
+// the same with the weights read from shared memory
+__device__ __forceinline__ float relu_weighted_sum(const float (&d)[16], const float* w) {
+  const float4* w4p = reinterpret_cast<const float4*>(w);
+  float2 acc2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int h4 = 0; h4 < DSA_IDX_HEADS / 4; ++h4) {
+    const float4 w4 = w4p[h4];
+    acc2 = fma_f32x2(make_float2(w4.x, w4.y), make_float2(fmaxf(d[4 * h4], 0.0f), fmaxf(d[4 * h4 + 1], 0.0f)), acc2);
+    acc2 = fma_f32x2(make_float2(w4.z, w4.w), make_float2(fmaxf(d[4 * h4 + 2], 0.0f), fmaxf(d[4 * h4 + 3], 0.0f)), acc2);
+  }
+  return acc2.x + acc2.y;
+}
+
 // Bounded wait used on the unwinding path: ignores the abort flag.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   long long t0 = clock64();
@@ -81,17 +125,28 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int N>
+// Blocks of 8 or more queries without histograms split their queries between
+// the two epilogue groups; other blocks alternate tiles between them.
+constexpr int kIdxGroups = 2;
+__host__ __device__ constexpr bool idx_qsplit(int QB, bool hist) { return !hist && QB >= 8; }
+
+template <int N, bool HIST>
 struct IdxCfg {
   static constexpr int QB = N / 16;
+  static constexpr int NG = kIdxGroups;
+  static constexpr bool QSPLIT = idx_qsplit(QB, HIST);
+  static constexpr int QPG = QSPLIT ? QB / NG : QB;   // queries a group sums per tile
+  static constexpr int kEpiThreads = 128 * NG;
+  static constexpr int kThreads = 64 + kEpiThreads;   // warp 0 TMA, warp 1 MMA, epilogue
   static constexpr uint32_t kBBytes = N * DSA_IDX_DIM * 2;
   // accumulator buffers in tensor memory: 4 for narrow tiles, 2 for wide ones
   static constexpr int NACC = N <= 64 ? 4 : 2;
   static constexpr uint32_t kTmemCols = (NACC * N <= 32) ? 32 : (NACC * N <= 64) ? 64
                                       : (NACC * N <= 128) ? 128 : (NACC * N <= 256) ? 256 : 512;
   // queries whose accumulator columns are read per tcgen05.ld batch (two
-  // batches in flight: the next is loaded while the current is summed)
-  static constexpr int QG = QB < 2 ? QB : 2;
+  // batches in flight: the next is loaded while the current is summed); one
+  // when the group's head weights live in registers
+  static constexpr int QG = QSPLIT ? 1 : (QPG < 2 ? QPG : 2);
 };
 
 struct IdxBarriers {
@@ -113,8 +168,11 @@ __host__ __device__ inline size_t indexer_smem_layout(int N, bool with_hist, int
   // two query-block buffers when a CTA may move to a new block (prefill);
   // with histograms a CTA owns one sequence's single block
   o += (with_hist ? 1ull : 2ull) * N * DSA_IDX_DIM * 2;
-  *off_w = o;   // one copy of the block's head weights per epilogue warp
-  o += 8ull * QB * 16 * sizeof(float);
+  // one copy per epilogue warp of the head weights of the queries it sums
+  *off_w = o;
+  const int ng = kIdxGroups;
+  const int qpg = idx_qsplit(QB, with_hist) ? QB / ng : QB;
+  o += static_cast<size_t>(4 * ng) * qpg * 16 * sizeof(float);
   o = (o + 15) & ~size_t(15);
   *off_hist = o;
   if (with_hist) o += static_cast<size_t>(QB) * kHistBins * sizeof(uint32_t);
@@ -125,11 +183,11 @@ __host__ __device__ inline size_t indexer_smem_layout(int N, bool with_hist, int
 }
 
 template <int N, bool HIST>
-__global__ void __launch_bounds__(kIdxThreads, 1)
+__global__ void __launch_bounds__(IdxCfg<N, HIST>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_kI,
                       const __grid_constant__ CUtensorMap tm_qI, const IndexerParams p,
                       int stages) {
-  using C = IdxCfg<N>;
+  using C = IdxCfg<N, HIST>;
   constexpr int QB = C::QB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -177,7 +235,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
     for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&bars->accfull[i], 1);
-      mbar_init(&bars->accempty[i], 4);   // the 4 warps of one epilogue group
+      // the 4 warps of the group that owns the tile, or every epilogue warp
+      mbar_init(&bars->accempty[i], C::QSPLIT ? 4 * C::NG : 4);
     }
     mbar_init(&bars->done, 1);
     bars->abort_flag = 0;
@@ -227,7 +286,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   };
   if (warp == 1) tmem_alloc(&bars->tmem_base, C::kTmemCols);
   if constexpr (HIST) {
-    for (int i = threadIdx.x; i < QB * kHistBins; i += kIdxThreads) sHist[i] = 0u;
+    for (int i = threadIdx.x; i < QB * kHistBins; i += C::kThreads) sHist[i] = 0u;
   }
   tc_fence_before();
   __syncthreads();
@@ -301,16 +360,24 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Two groups of 4 warps take alternate tiles (group = tile index parity);
-    // each group covers all 4 TMEM lane quarters.
-    const int et = threadIdx.x - 64;            // 0 .. 255
+    // Groups of 4 warps, each covering all 4 TMEM lane quarters: they take
+    // alternate tiles (group = tile index parity) or, with QSPLIT, queries
+    // q0 .. q0 + QPG - 1 of every tile.
+    constexpr int QPG = C::QPG;
+    const int et = threadIdx.x - 64;            // 0 .. kEpiThreads - 1
     const int group = (warp - 2) >> 2;
+    const int q0 = C::QSPLIT ? group * QPG : 0;
     const int quarter = warp & 3;               // TMEM lanes 32*quarter ..
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
-    float* wv_warp = sW + (warp - 2) * QB * DSA_IDX_HEADS;
+    float* wv_warp = sW + (warp - 2) * QPG * DSA_IDX_HEADS;
     UnitCursor c = count > 0 ? locate_unit(p, u0) : UnitCursor{p.B, 0, 0, 0};
     const int hist_b = c.b;
     int pb = -1, pqb = -1;
+    // Split-query groups keep their queries' head weights in registers,
+    // reloaded when the block changes: a warp-wide broadcast of 16 bytes from
+    // shared memory takes several shared-pipe wavefronts, and per tile those
+    // reads would outrun the MMA.
+    float wreg[C::QSPLIT ? QPG : 1][16];
 
     // No CTA-wide barrier inside this loop: a bounded wait that gives up
     // leaves the loop early, and every epilogue thread still reaches the
@@ -318,17 +385,23 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     for (long long i = 0; i < count; ++i) {
       if (c.b != pb || c.qb != pqb) {
         __syncwarp();
-        for (int j = lane; j < QB * DSA_IDX_HEADS; j += 32) {
-          const int s = c.qb * QB + j / DSA_IDX_HEADS;
+        for (int j = lane; j < QPG * DSA_IDX_HEADS; j += 32) {
+          const int s = c.qb * QB + q0 + j / DSA_IDX_HEADS;
           wv_warp[j] = s < p.S
               ? p.w[(static_cast<size_t>(c.b) * p.S + s) * DSA_IDX_HEADS + (j % DSA_IDX_HEADS)]
               : 0.0f;
         }
         __syncwarp();
+        if constexpr (C::QSPLIT) {
+#pragma unroll
+          for (int g = 0; g < QPG; ++g)
+#pragma unroll
+            for (int h = 0; h < DSA_IDX_HEADS; ++h) wreg[g][h] = (h < kAbsHeads ? 0.5f : 1.0f) * wv_warp[g * DSA_IDX_HEADS + h];
+        }
         pb = c.b;
         pqb = c.qb;
       }
-      if ((i & 1) != group) {
+      if (!C::QSPLIT && (i & 1) != group) {
         advance_unit(p, c);
         continue;
       }
@@ -340,27 +413,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       tc_fence_after();
       const int t = c.kt * kKeyTile + quarter * 32 + lane;
       const int T = p.lens.T[c.b];
-      float* srow = p.scores + (static_cast<size_t>(c.b) * p.S + c.qb * QB) * p.cap + t;
-      const uint32_t acc_addr = tmem_base + lane_addr + a * N;
+      float* srow = p.scores + (static_cast<size_t>(c.b) * p.S + c.qb * QB + q0) * p.cap + t;
+      const uint32_t acc_addr = tmem_base + lane_addr + a * N + q0 * 16;
+      // this key is kept for the warp's queries j in [jlo, jhi): query
+      // s0 + j exists (s < S) and sees key t (t < T - S + s + 1)
+      const int s0 = c.qb * QB + q0;
+      const int jlo = t - (T - p.S) - s0;
+      const int jhi = p.S - s0;
       // weighted head sum of query column group jq (buffer vb), then store
       auto finish = [&](const float (&vb)[C::QG][16], int jq) {
 #pragma unroll
         for (int g = 0; g < C::QG; ++g) {
-          const int s = c.qb * QB + jq + g;
-          // sum over heads of w_h * ReLU(dot_h), two heads per paired FMA
-          const float4* wv4 = reinterpret_cast<const float4*>(wv_warp + (jq + g) * DSA_IDX_HEADS);
-          float2 acc2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-          for (int h4 = 0; h4 < DSA_IDX_HEADS / 4; ++h4) {
-            const float4 w4 = wv4[h4];
-            acc2 = fma_f32x2(make_float2(w4.x, w4.y),
-                             make_float2(fmaxf(vb[g][4 * h4], 0.0f), fmaxf(vb[g][4 * h4 + 1], 0.0f)), acc2);
-            acc2 = fma_f32x2(make_float2(w4.z, w4.w),
-                             make_float2(fmaxf(vb[g][4 * h4 + 2], 0.0f), fmaxf(vb[g][4 * h4 + 3], 0.0f)), acc2);
-          }
-          const float acc = acc2.x + acc2.y;
+          float acc;
+          if constexpr (C::QSPLIT) acc = relu_weighted_sum_r(vb[g], wreg[jq + g]);
+          else acc = relu_weighted_sum(vb[g], wv_warp + (jq + g) * DSA_IDX_HEADS);
           // queries past S (padding of the last block) are computed, not kept
-          const bool valid = s < p.S && t < visible_len(T, p.S, s);
+          const bool valid = jq + g >= jlo && jq + g < jhi;
           if (valid) srow[static_cast<size_t>(jq + g) * p.cap] = acc;
           if constexpr (HIST) {
             // plain shared atomics: cheaper than warp-aggregating each update
@@ -373,16 +441,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       for (int g = 0; g < C::QG; ++g) tmem_ld16(acc_addr + g * 16, v0[g]);
       tmem_ld_wait();
 #pragma unroll
-      for (int jq = 0; jq < QB; jq += 2 * C::QG) {
+      for (int jq = 0; jq < QPG; jq += 2 * C::QG) {
         // buffer v0 holds group jq; load jq + QG into v1 while v0 is summed
-        if (jq + C::QG < QB) {
+        if (jq + C::QG < QPG) {
 #pragma unroll
           for (int g = 0; g < C::QG; ++g) tmem_ld16(acc_addr + (jq + C::QG + g) * 16, v1[g]);
         }
         finish(v0, jq);
         tmem_ld_wait();
-        if (jq + C::QG < QB) {
-          if (jq + 2 * C::QG < QB) {
+        if (jq + C::QG < QPG) {
+          if (jq + 2 * C::QG < QPG) {
 #pragma unroll
             for (int g = 0; g < C::QG; ++g) tmem_ld16(acc_addr + (jq + 2 * C::QG + g) * 16, v0[g]);
           }
@@ -401,13 +469,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       // histograms were cleared by the previous kernel of the call
       pdl_wait();
       if (et == 0) DSA_TS(4);
-      named_bar_sync(1, kIdxEpiThreads);
+      named_bar_sync(1, C::kEpiThreads);
       if (count > 0) {
         for (int j = 0; j < QB; ++j) {
           const int s = j;
           if (s >= p.S) break;
           uint32_t* g = p.hist + static_cast<size_t>(hist_b * p.S + s) * kHistBins;
-          for (int bin = et; bin < kHistBins; bin += kIdxEpiThreads) {
+          for (int bin = et; bin < kHistBins; bin += C::kEpiThreads) {
             const uint32_t v = sHist[j * kHistBins + bin];
             if (v) atomicAdd(g + bin, v);
           }
@@ -465,7 +533,7 @@ static cudaError_t launch_n(const IndexerParams& p, const CUtensorMap& tm_kI,
   if (e != cudaSuccess) return e;
   // with histograms the kernel follows the scratch-clearing kernel and waits
   // for it only before its final flush
-  return launch_kernel("indexer_tc_kernel", kern, grid, dim3(kIdxThreads), smem, stream, HIST, tm_kI,
+  return launch_kernel("indexer_tc_kernel", kern, grid, dim3(IdxCfg<N, HIST>::kThreads), smem, stream, HIST, tm_kI,
                        tm_qI, p, stages);
 }
 

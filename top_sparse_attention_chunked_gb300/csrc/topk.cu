@@ -354,11 +354,14 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkParams 
   for (int i = ri.keff + threadIdx.x; i < p.k; i += kRowThreads) out[i] = -1;
 }
 
-constexpr int kClThreads = 512;   // cluster select CTA size with 32 keys a thread (1,024 with 8 or 16)
+constexpr int kClThreads = 512;   // cluster select CTA size with 32 keys a thread (1,024 with 8 to 24)
 // Candidates gathered into every CTA of the cluster: 8,192, or 4,096 for the
 // shortest slices, whose CTAs then fit two to an SM (many short rows, as in
-// grouped decode, run in one wave).
-__host__ __device__ constexpr int cl_gather_max(int per) { return per <= 8 ? 4096 : 8192; }
+// grouped decode, run in one wave), or 3,072 with 24 keys a thread, whose
+// 24,576-key slice leaves no more room. The first 16 KB of the gathered list
+// also hold the cluster's histogram exchange, which is over before any
+// candidate is gathered.
+__host__ __device__ constexpr int cl_gather_max(int per) { return per <= 8 ? 4096 : per == 24 ? 3072 : 8192; }
 
 // Exact threshold over a list of candidate composites held by this CTA:
 // refines (prefix, mask) until `need` candidates are at or above it.
@@ -996,10 +999,16 @@ __global__ void __launch_bounds__(NT, (PER <= 8 && NT <= 512) ? 2 : 1) topk_clus
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   constexpr int kSlice = PER * NT;
-  extern __shared__ unsigned long long scand[];  // candidate composites of this CTA
+  // candidate composites of this CTA (PER * NT), then the gathered list
+  // (cl_gather_max(PER)), whose start first holds this CTA's slice histogram
+  // and the range of bins it sums for the cluster (read by peers only before
+  // the cluster barrier that precedes any gather)
+  extern __shared__ unsigned long long scand[];
+  static_assert(cl_gather_max(PER) * sizeof(unsigned long long) >= 2 * kHistBins * sizeof(uint32_t),
+                "the histogram exchange must fit in the gather area");
+  uint32_t* hloc = reinterpret_cast<uint32_t*>(scand + PER * NT);   // this CTA's slice histogram
+  uint32_t* hred = hloc + kHistBins;             // the range of bins this CTA sums
   __shared__ __align__(16) uint32_t h[kHistBins];   // row histogram, then digit counts
-  __shared__ uint32_t hloc[kHistBins];           // this CTA's slice histogram
-  __shared__ uint32_t hred[kHistBins];           // the range of bins this CTA sums
   __shared__ uint32_t hd[256];                   // this CTA's digit histogram
   __shared__ uint32_t warp_tot[32];
   __shared__ int s_d;
@@ -1248,8 +1257,8 @@ __global__ void __launch_bounds__(NT, (PER <= 8 && NT <= 512) ? 2 : 1) topk_clus
     cluster.sync();                              // every CTA's count is published
     for (int q = 0; q < rank; ++q) pos += *cluster.map_shared_rank(&s_count, q);
   }
-#pragma unroll
   const int seq = r / p.S;
+#pragma unroll
   for (int wd = 0; wd < (PER + 31) / 32; ++wd) {
     uint32_t bits = selm[wd];
     while (bits) {
@@ -1281,73 +1290,103 @@ __global__ void __launch_bounds__(NT, (PER <= 8 && NT <= 512) ? 2 : 1) topk_clus
   DSA_TS_FLUSH(p.status, 1);
 }
 
-// Cluster shape for rows of up to max_n keys: keys per thread and CTAs per
-// row (0 CTAs: the row is too long for the cluster select).
-// Threads of a cluster-select CTA holding `per` keys a thread: 1,024 with 8 or
-// 16 (64 registers, no spills), 512 with 32 (the keys need more registers
-// than 1,024 threads leave).
-static int cl_threads(int per) { return per <= 16 ? 1024 : kClThreads; }
-static void cluster_shape(int max_n, int* per, int* ctas) {
-  // as few keys per thread as up to 16 CTAs allow: the slice load from L2 and
-  // the per-thread work shrink with the slice
-  *per = max_n <= 16 * 8 * 1024 ? 8 : max_n <= 16 * 16 * 1024 ? 16 : 32;
-  *ctas = (max_n + *per * cl_threads(*per) - 1) / (*per * cl_threads(*per));
-  if (*ctas > kTopkClusterMax) *ctas = 0;
+// Threads of a cluster-select CTA holding `per` keys a thread: 1,024 with 8,
+// 16 or 24 (64 registers, no spills), 512 with 32 (the keys need more
+// registers than 1,024 threads leave).
+static int cl_threads(int per) { return per <= 24 ? 1024 : kClThreads; }
+static size_t cl_smem(int per) {
+  return (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
 }
-
-bool topk_cluster_feasible(int max_n) {
-  int per, ctas;
-  cluster_shape(max_n, &per, &ctas);
-  if (ctas <= 8) return ctas > 0;
-  static int cached[64][3] = {};   // per device: PER 8 / 16 / 32 -> 1 ok, 2 not
+static const void* cl_kernel(int per) {
+  return per == 8    ? reinterpret_cast<const void*>(topk_cluster_select_kernel<8, 1024>)
+         : per == 16 ? reinterpret_cast<const void*>(topk_cluster_select_kernel<16, 1024>)
+         : per == 24 ? reinterpret_cast<const void*>(topk_cluster_select_kernel<24, 1024>)
+                     : reinterpret_cast<const void*>(topk_cluster_select_kernel<32, 512>);
+}
+// CTAs per row with `per` keys a thread (0: more than a cluster can hold).
+static int cl_ctas(int max_n, int per) {
+  const int slice = per * cl_threads(per);
+  const int ctas = (max_n + slice - 1) / slice;
+  return ctas > kTopkClusterMax ? 0 : ctas;
+}
+// Clusters of `ctas` CTAs of the `per` kernel that are resident at once on
+// the current device, cached (0 if it cannot launch). A cluster must fit in
+// one GPC, so on this GPU 15 clusters of 8 or 9 fit, 8 of 11 or 12 and 7 of
+// 13 to 16.
+static int cl_capacity(int per, int ctas) {
+  static int cached[64][4][kTopkClusterMax + 1] = {};   // capacity + 1; 0: not queried
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  const int pi = per == 8 ? 0 : per == 16 ? 1 : 2;
-  if (cached[dev][pi]) return cached[dev][pi] == 1;
-  const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
-  auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
-            : per == 16 ? topk_cluster_select_kernel<16, 1024> : topk_cluster_select_kernel<32, 512>;
-  bool ok = set_max_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)) == cudaSuccess &&
-            set_nonportable_cluster(reinterpret_cast<const void*>(kern)) == cudaSuccess;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int pi = per == 8 ? 0 : per == 16 ? 1 : per == 24 ? 2 : 3;
+  int& slot = cached[dev][pi][ctas];
+  if (slot) return slot - 1;
+  const void* kern = cl_kernel(per);
+  int n = 0;
+  bool ok = set_max_smem(kern, static_cast<int>(cl_smem(per))) == cudaSuccess &&
+            (ctas <= 8 || set_nonportable_cluster(kern) == cudaSuccess);
   if (ok) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1);
+    cfg.gridDim = dim3(ctas, 1);
     cfg.blockDim = dim3(cl_threads(per));
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = cl_smem(per);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.x = ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    ok = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
-  cached[dev][pi] = ok ? 1 : 2;
-  return ok;
+  slot = n + 1;
+  return n;
+}
+// Cluster shape for `nrows` rows of up to max_n keys: the fewest keys a
+// thread (the slice load from L2 and the per-thread work shrink with them)
+// whose clusters, one per row, are all resident at once; if none is, the
+// fewest keys a thread that launch at all. ctas = 0: no shape fits.
+static void cluster_shape(int max_n, int nrows, int* per, int* ctas) {
+  static const int kPers[4] = {8, 16, 24, 32};
+  *per = 0;
+  *ctas = 0;
+  for (int pass = 0; pass < 2 && *ctas == 0; ++pass)
+    for (int i = 0; i < 4; ++i) {
+      const int c = cl_ctas(max_n, kPers[i]);
+      if (c == 0) continue;
+      const int cap = cl_capacity(kPers[i], c);
+      if (cap >= (pass == 0 ? nrows : 1)) {
+        *per = kPers[i];
+        *ctas = c;
+        break;
+      }
+    }
+}
+
+bool topk_cluster_feasible(int max_n) {
+  int per, ctas;
+  cluster_shape(max_n, 1, &per, &ctas);
+  return ctas > 0;
 }
 
 int topk_cluster_ctas(int max_n) {
   int per, ctas;
-  cluster_shape(max_n, &per, &ctas);
+  cluster_shape(max_n, 1, &per, &ctas);
   return ctas;
 }
 
 cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
                                        cudaStream_t stream) {
   int per, ctas;
-  cluster_shape(max_n, &per, &ctas);
-  if (ctas == 0) return cudaErrorInvalidValue;
+  cluster_shape(max_n, p.nrows, &per, &ctas);
+  if (ctas == 0) return cudaErrorNotSupported;
   // worst case every key of the slice is a candidate; then the gathered list
-  const size_t smem = (static_cast<size_t>(per) * cl_threads(per) + cl_gather_max(per)) * sizeof(unsigned long long);
-  auto kern = per == 8 ? topk_cluster_select_kernel<8, 1024>
-            : per == 16 ? topk_cluster_select_kernel<16, 1024> : topk_cluster_select_kernel<32, 512>;
-  cudaError_t e = set_max_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem));
+  const size_t smem = cl_smem(per);
+  const void* kern = cl_kernel(per);
+  cudaError_t e = set_max_smem(kern, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if (ctas > 8) {
-    e = set_nonportable_cluster(reinterpret_cast<const void*>(kern));
+    e = set_nonportable_cluster(kern);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1364,8 +1403,8 @@ cudaError_t launch_topk_cluster_select(const TopkParams& p, int max_n, bool pdl,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  if (ctas > 8 && !topk_cluster_feasible(max_n)) return cudaErrorNotSupported;
-  const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, p);
+  void* args[] = {const_cast<TopkParams*>(&p)};
+  const cudaError_t le = cudaLaunchKernelExC(&cfg, kern, args);
   if (le == cudaSuccess) note_launch("topk_cluster_select_kernel");
   return le;
 }

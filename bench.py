@@ -66,9 +66,9 @@ def peaks():
 # addressing). When any of that changes, the figure is dropped (null) until it
 # is measured again.
 TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh"]
-TRAFFIC_SOURCE_SHA = "7002c4c5b7516fc0"
-INDEXER_TRAFFIC = {"decode_4k": 574464, "grouped_decode_32k": 16907776, "decode_128k": 16827648,
-                   "decode_256k_int8": 33629440}
+TRAFFIC_SOURCE_SHA = "63ca7840c1becf8e"
+INDEXER_TRAFFIC = {"decode_4k": 573952, "grouped_decode_32k": 16908800, "decode_128k": 16827904,
+                   "decode_256k_int8": 33626624}
 
 
 def indexer_source_hash():

@@ -24,13 +24,13 @@
 // epilogue groups of 4 warps (warp w reads TMEM lanes 32*(w%4) .. +31).
 // Accumulators are double-buffered in TMEM so the MMA of tile i+1 overlaps
 // the epilogue of tile i. Two epilogue organisations:
-//   * alternate tiles (decode, histograms, blocks under 8 queries): group g
+//   * alternate tiles (blocks under 8 queries: single-token decode): group g
 //     takes the tiles of parity g with all of the block's queries, head
 //     weights read from shared memory;
-//   * split queries (blocks of 8 or 16 queries without histograms, i.e.
-//     prefill): both groups read every tile, group g taking half of the
-//     block's queries, with those queries' head weights held in registers
-//     across the block's tiles. At K = 64 the epilogue has about as many
+//   * split queries (blocks of 8 or 16 queries: prefill, multi-token decode):
+//     both groups read every tile, group g taking half of the block's
+//     queries, with those queries' head weights held in registers across the
+//     block's tiles. At K = 64 the epilogue has about as many
 //     instructions per tile as the MMA has cycles, so it sets the pace: a
 //     warp-wide broadcast read of the weights from shared memory costs
 //     several shared-pipe wavefronts per 16 bytes, enough to saturate that
@@ -125,10 +125,10 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Blocks of 8 or more queries without histograms split their queries between
-// the two epilogue groups; other blocks alternate tiles between them.
+// Blocks of 8 or more queries split their queries between the two epilogue
+// groups; smaller blocks alternate tiles between them.
 constexpr int kIdxGroups = 2;
-__host__ __device__ constexpr bool idx_qsplit(int QB, bool hist) { return !hist && QB >= 8; }
+__host__ __device__ constexpr bool idx_qsplit(int QB, bool) { return QB >= 8; }
 
 template <int N, bool HIST>
 struct IdxCfg {
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(IdxCfg<N, HIST>::kThreads, 1)
           if (valid) srow[static_cast<size_t>(jq + g) * p.cap] = acc;
           if constexpr (HIST) {
             // plain shared atomics: cheaper than warp-aggregating each update
-            if (valid) atomicAdd(&sHist[(jq + g) * kHistBins + (float_key(acc) >> (32 - kHistBits))], 1u);
+            if (valid) atomicAdd(&sHist[(q0 + jq + g) * kHistBins + (float_key(acc) >> (32 - kHistBits))], 1u);
           }
         }
       };

@@ -66,9 +66,9 @@ def peaks():
 # addressing). When any of that changes, the figure is dropped (null) until it
 # is measured again.
 TRAFFIC_SOURCES = ["indexer.cu", "sm100_ptx.cuh", "dsa_common.cuh"]
-TRAFFIC_SOURCE_SHA = "63ca7840c1becf8e"
-INDEXER_TRAFFIC = {"decode_4k": 573952, "grouped_decode_32k": 16908800, "decode_128k": 16827904,
-                   "decode_256k_int8": 33626624}
+TRAFFIC_SOURCE_SHA = "58e783604f49e682"
+INDEXER_TRAFFIC = {"decode_4k": 580608, "grouped_decode_32k": 16910848, "decode_128k": 16834304,
+                   "decode_256k_int8": 33632512}
 
 
 def indexer_source_hash():

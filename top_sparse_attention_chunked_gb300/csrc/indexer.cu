@@ -47,6 +47,11 @@
 namespace dsa {
 
 constexpr int kMaxAcc = 4;
+// Backoff (ns) of the roles' mbarrier retries: the epilogue sets the pace, and
+// the producer and MMA warps, which wait most of each tile, share schedulers
+// with epilogue warps (prefill indexer 775 -> 761 us; 128 ns and a try_wait
+// suspend hint were slower).
+constexpr int kIdxNap = 32;
 constexpr int kIdxMaxStages = 8;
 constexpr uint32_t kATileBytes = kKeyTile * DSA_IDX_DIM * 2;   // 16 KB
 
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(IdxCfg<N, HIST>::kThreads, 1)
       if (c.b != ps.pb || c.qb != ps.pqb) {
         const int bi = ps.nblk & 1;
         if (ps.nblk >= 2 &&
-            !mbar_wait_bounded(&bars->bempty[bi], ((ps.nblk >> 1) - 1) & 1, abort_flag, p.wait_budget))
+            !mbar_wait_bounded<kIdxNap>(&bars->bempty[bi], ((ps.nblk >> 1) - 1) & 1, abort_flag, p.wait_budget))
           return;
         mbar_arrive_expect_tx(&bars->bfull[bi], C::kBBytes);
         tma_load_2d(sB + bi * C::kBBytes, &tm_qI, &bars->bfull[bi], 0,
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(IdxCfg<N, HIST>::kThreads, 1)
         ps.pqb = c.qb;
       }
       const int s = ps.s;
-      if (ps.r > 0 && !mbar_wait_bounded(&bars->empty[s], (ps.r - 1) & 1u, abort_flag, p.wait_budget)) return;
+      if (ps.r > 0 && !mbar_wait_bounded<kIdxNap>(&bars->empty[s], (ps.r - 1) & 1u, abort_flag, p.wait_budget)) return;
       mbar_arrive_expect_tx(&bars->full[s], kATileBytes);
       // a 128-key tile never straddles a cache block (block sizes are
       // multiples of 128); an entry outside the pool reads block 0 (the
@@ -326,17 +331,17 @@ __global__ void __launch_bounds__(IdxCfg<N, HIST>::kThreads, 1)
         if (c.b != pb || c.qb != pqb) {
           if (nblk > 0) tc_commit(&bars->bempty[bi]);
           bi = nblk & 1;
-          if (!mbar_wait_bounded(&bars->bfull[bi], (nblk >> 1) & 1, abort_flag, p.wait_budget)) break;
+          if (!mbar_wait_bounded<kIdxNap>(&bars->bfull[bi], (nblk >> 1) & 1, abort_flag, p.wait_budget)) break;
           ++nblk;
           pb = c.b;
           pqb = c.qb;
         }
-        if (!mbar_wait_bounded(&bars->full[s], round & 1u, abort_flag, p.wait_budget)) break;
+        if (!mbar_wait_bounded<kIdxNap>(&bars->full[s], round & 1u, abort_flag, p.wait_budget)) break;
         if (i == 0) DSA_TS(1);
         if (i == count - 1) DSA_TS(2);
         const int a = static_cast<int>(i % C::NACC);
         if (i >= C::NACC &&
-            !mbar_wait_bounded(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag, p.wait_budget))
+            !mbar_wait_bounded<kIdxNap>(&bars->accempty[a], static_cast<uint32_t>(((i / C::NACC) - 1) & 1), abort_flag, p.wait_budget))
           break;
         tc_fence_after();
         const uint32_t d = tmem_base + a * N;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(IdxCfg<N, HIST>::kThreads, 1)
       }
       const int a = static_cast<int>(i % C::NACC);
       // every lane of the warp leaves together (tcgen05.ld below is warp-wide)
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars->accfull[a], static_cast<uint32_t>((i / C::NACC) & 1),
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded<kIdxNap>(&bars->accfull[a], static_cast<uint32_t>((i / C::NACC) & 1),
                                                      abort_flag, p.wait_budget)))
         break;
       tc_fence_after();

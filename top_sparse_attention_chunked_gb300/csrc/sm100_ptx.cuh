@@ -60,7 +60,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for phase `parity` of `bar` to complete. Returns false (and sets
 // *abort) once `budget` SM cycles have passed since the first try without the
 // phase completing, or if another role already aborted. A budget of 0 gives
-// up on any wait that is not already complete at its first try.
+// up on any wait that is not already complete at its first try. NAP > 0
+// sleeps NAP ns between retries, which leaves the issue slots of the waiting
+// warp's scheduler to the warps that share it.
+template <int NAP = 0>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort_flag,
                                                   long long budget = kWaitBudgetCycles) {
@@ -72,8 +75,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       *abort_flag = 1;
       return false;
     }
-    for (int i = 0; i < 64; ++i)
+    for (int i = 0; i < 64; ++i) {
       if (mbar_try_wait(bar, parity)) return true;
+      if constexpr (NAP > 0) __nanosleep(NAP);
+    }
   }
 }
 

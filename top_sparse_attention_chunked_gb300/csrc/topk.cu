@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(kRrThreads, 1) topk_row_reg_kernel(const TopkP
 }
 
 // ---------------------------------------------------------------------------
-// 3c. streaming whole-row select (many rows: prefill). One CTA of 512 threads
+// 3c. streaming whole-row select (many rows: prefill). One CTA of 256 threads
 // per row keeps no keys in registers:
 //   1. a sample of the row (every 16th 128-byte line, so no extra DRAM
 //      sectors) gives a provisional threshold theta a little below the k-th
@@ -606,11 +606,14 @@ __global__ void __launch_bounds__(kRrThreads, 1) topk_row_reg_kernel(const TopkP
 // than kRsCandMax), an exact path takes over: a histogram of the row's top 11
 // key bits, a pass that marks the keys above the threshold bin and lists the
 // bin's keys, and the same resolve (for a bin of more than kRsCandMax keys,
-// rounds that re-read the row). With ~40 KB of shared memory and few
-// registers several rows are in flight per SM, so one row's reads overlap
-// another's resolve.
+// rounds that re-read the row). Each row's phases are chains of dependent
+// loads and block barriers, so throughput comes from rows in flight: with
+// ~46 KB of shared memory and at most 64 registers, four 256-thread rows run
+// per SM (against two 512-thread rows at 56 registers: 8K-on-32K 563 -> 524
+// us; four 512-thread rows at 32 registers 541 us, five 256-thread rows with
+// a smaller list 660 us, six 128-thread rows 966 us).
 // ---------------------------------------------------------------------------
-constexpr int kRsThreads = 512;
+constexpr int kRsThreads = 256;
 constexpr int kRsCandMax = 4096;
 constexpr int kRsMaxLen = 262144;
 #ifndef RS_UNROLL
@@ -647,7 +650,7 @@ __device__ unsigned long long rs_resolve(const unsigned long long* list, uint32_
   return prefix;
 }
 
-__global__ void __launch_bounds__(kRsThreads) topk_row_stream_kernel(const TopkParams p) {
+__global__ void __launch_bounds__(kRsThreads, 4) topk_row_stream_kernel(const TopkParams p) {
   extern __shared__ uint32_t rs_bm[];                  // [ceil(n / 32)] selection bits
   __shared__ unsigned long long rs_c[kRsCandMax];      // listed composites
   __shared__ __align__(16) uint32_t h[kHistBins];

@@ -162,6 +162,7 @@ def _topk_case(dsa, B, S, T, cap, k, kind, seed):
     (2, 3, [5000, 3000], 5000, 100), (1, 1, 4096, 4096, 512), (2, 2, [2049, 2], 4100, 2048),
     (1, 4, 70, 80, 64), (1, 1, 1, 1, 1), (1, 2, 9000, 9000, 8999),
     (1, 1, 600000, 600000, 2048),   # longer than the cluster select: global merge path
+    (2, 1, [300000, 262145], 300000, 2048),   # 24 keys a thread, clusters of 13 CTAs (one row ragged)
     (1, 2, 40000, 40000, 3000),     # tie-heavy rows with > 8,192 threshold-bin candidates
 ])
 def test_topk_bitexact_chunked(dsa, kind, B, S, T, cap, k):

@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
   Bars* bars = reinterpret_cast<Bars*>(sP + 2 * kPBytes);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // trace build: phase stamps of each CTA's third item (steady state)
+  DSA_TS_DECL;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -181,7 +183,8 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
     long long seq = 0;                   // position in the ring (tiles issued)
     bool ok = true;
     bool bad_page = false;               // a block-table entry outside the pool was read
-    for (long long it = my_first; it < n_items && ok; it += stride) {
+    long long nit = 0;                   // items of this CTA so far (trace stamps)
+    for (long long it = my_first; it < n_items && ok; it += stride, ++nit) {
       const PfItem w = pf_item(p, it);
       const int b = w.r / p.S;
       const int T = p.lens.T[b];
@@ -220,6 +223,8 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             break;
           }
           if (lane == 0) mbar_arrive_expect_tx(&bars->full[st], kTileBytes / kLoadWarps);
+          if (nit == 2 && lane == 0 && t == 0) DSA_TS(pass == 0 ? 0 : 1);
+          if (nit == 2 && lane == 0 && pass == 1 && t == w.ntiles - 1) DSA_TS(2);
           __syncwarp();
           if (issuer)
             tma_gather4(sKV + st * kTileBytes + cb * kBlockBytes + grp * 512, tm, &bars->full[st],
@@ -254,6 +259,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           break;
         if (!mbar_wait_bounded(&bars->q_ready, static_cast<uint32_t>(n & 1), abort_flag)) break;
         tc_fence_after();
+        if (n == 2) DSA_TS(3);
         bool ok = true;
         for (int t = 0; t < w.ntiles; ++t, ++seq) {
           const int st = static_cast<int>(seq % kStages);
@@ -262,6 +268,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
             break;
           }
           tc_fence_after();
+          if (n == 2 && t == 0) DSA_TS(4);
           const uint32_t a0 = smem_u32(sKV + st * kTileBytes);
           const uint32_t b0 = smem_u32(sQ);
 #pragma unroll
@@ -274,6 +281,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           tc_commit(&bars->empty[st]);
         }
         if (!ok) break;
+        if (n == 2) DSA_TS(5);
         tc_commit(&bars->logits_ready);
         for (int t = 0; t < w.ntiles; ++t, ++seq, ++ptile) {
           const int st = static_cast<int>(seq % kStages);
@@ -303,6 +311,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
           tc_commit(&bars->p_free);
         }
         if (!ok) break;
+        if (n == 2) DSA_TS(9);
         tc_commit(&bars->o_ready);
       }
       tc_commit(&bars->done);
@@ -351,6 +360,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       const PfItem w = pf_item(p, it);
       if (!mbar_wait_bounded(&bars->logits_ready, static_cast<uint32_t>(n & 1), abort_flag)) break;
       tc_fence_after();
+      if (n == 2 && et == 0) DSA_TS(6);
       // the query buffer is free once the logits are in: stage the next item's
       if (it + stride < n_items) load_q(pf_item(p, it + stride));
 
@@ -376,6 +386,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         for (int h = 0; h < 16; ++h) bars->red[0][warp - 1][h] = mx[h];
       }
       if (!group_sync(&bars->grp, &gphase, abort_flag)) break;
+      if (n == 2 && et == 0) DSA_TS(7);
       float M[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h)
@@ -412,6 +423,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         fence_proxy_async_smem();
         mbar_arrive(&bars->p_ready);
       }
+      if (n == 2 && et == 0) DSA_TS(8);
       // ---- row sums
 #pragma unroll
       for (int h = 0; h < 16; ++h)
@@ -425,6 +437,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
       // ---- O^T: TMEM lane = head dim, columns = heads
       if (!mbar_wait_bounded(&bars->o_ready, static_cast<uint32_t>(n & 1), abort_flag)) break;
       tc_fence_after();
+      if (n == 2 && et == 0) DSA_TS(10);
       float o[16];
       tmem_ld16(tmem + lane_addr + kOCol, o);
       tmem_ld_wait();
@@ -441,6 +454,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
         else if (p.out_dtype == DSA_FP16) static_cast<__half*>(p.out)[oi] = __float2half_rn(val);
         else static_cast<float*>(p.out)[oi] = val;
       }
+      if (n == 2 && et == 0) DSA_TS(11);
       tc_fence_before();
       mbar_arrive(&bars->tmem_free);
       // red[] reads done before the next item reuses it
@@ -453,6 +467,7 @@ __global__ void __launch_bounds__(pf::kThreads, 2)
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && bars->abort_flag) atomicOr(status, kDevTimeout);
+  DSA_TS_FLUSH(status, 2);
 }
 
 bool prefill_tc_supported(const AttnParams& p, int kv_dtype, size_t smem_optin) {

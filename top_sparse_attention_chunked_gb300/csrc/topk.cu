@@ -494,8 +494,9 @@ __global__ void __launch_bounds__(kRrThreads, 1) topk_row_reg_kernel(const TopkP
     const uint32_t b1 = static_cast<uint32_t>(s_d);
     const uint32_t need2 = rs - s_above;
     for (int i = threadIdx.x; i < kHistBins; i += kRrThreads) h[i] = 0u;
-    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+    // every thread has read the search's outputs before they are reset
     __syncthreads();
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
 #pragma unroll
     for (int i = 0; i < PER; ++i)
       if (((i + lane) & 15) == 0 && valid(i) && (key[i] >> 21) == b1)
@@ -633,8 +634,11 @@ __device__ unsigned long long rs_resolve(const unsigned long long* list, uint32_
     const int sh = hi - w + 1;
     const uint32_t dm = (1u << w) - 1u;
     for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
-    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
+    // every thread has read the previous round's outputs before they are
+    // reset (the barrier after the counting orders the reset before the
+    // next search)
     __syncthreads();
+    if (threadIdx.x == 0) { *sd = 0; *sabove = 0; *scnt = 0; }
     for (uint32_t i = threadIdx.x; i < n; i += kRsThreads) {
       const unsigned long long cc = list[i];
       if ((cc & mask) == prefix) atomicAdd(&h[static_cast<uint32_t>(cc >> sh) & dm], 1u);
@@ -726,8 +730,9 @@ __global__ void __launch_bounds__(kRsThreads, 4) topk_row_stream_kernel(const To
     const uint32_t sb = static_cast<uint32_t>(s_d);
     const uint32_t need2 = rs - s_above;
     for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
-    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+    // every thread has read the search's outputs before they are reset
     __syncthreads();
+    if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
 #pragma unroll
     for (int j = 0; j < kRsSmpReg; ++j) {
       const int t = 32 * 16 * (warp + kWarps * j) + lane;
@@ -872,8 +877,11 @@ __global__ void __launch_bounds__(kRsThreads, 4) topk_row_stream_kernel(const To
           const int sh = hi - w + 1;
           const uint32_t dm = (1u << w) - 1u;
           for (int i = threadIdx.x; i < kHistBins; i += kRsThreads) h[i] = 0u;
-          if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
+          // every thread has read the previous round's outputs before they
+          // are reset (the barrier after the counting orders the reset
+          // before the next search)
           __syncthreads();
+          if (threadIdx.x == 0) { s_d = 0; s_above = 0; s_cnt = 0; }
           for (int base = 0; base < n; base += kRsThreads) {
             const int t = base + threadIdx.x;
             uint32_t dg = 0xFFFFFFFFu;

@@ -1,0 +1,80 @@
+"""Run-to-run determinism: every kernel sums in a fixed order and every
+selection is exact, so repeated calls on the same inputs must return the same
+indices and outputs bit for bit. A race between threads of a block (a shared
+result reset before every thread has read it, say) shows here as a rare
+difference between two runs, which the parity tests could miss."""
+import pytest
+import torch
+
+from dsa_inputs import WORKLOADS, make_inputs, small_workload
+from tests._helpers import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from top_sparse_attention_chunked_gb300 import build_lib, dsa as D
+    build_lib.build()
+    D.load_library()
+    return D
+
+
+def _repeat_step(D, wl, prefill, reps):
+    cpu = make_inputs(wl)
+    dev = to_device(cpu)
+    p = D.problem_for(wl)
+    ws = D.alloc_workspace(p, D.DSA_OP_PREFILL if prefill else D.DSA_OP_DECODE)
+    fn = D.dsa_sparse_attn_prefill if prefill else D.dsa_sparse_attn_decode
+    first = None
+    for rep in range(reps):
+        ws.fill_(0xA5 if rep % 2 else 0x5A)   # stale scratch must not matter either
+        out = torch.empty(wl.batch, wl.q_len, wl.num_q_heads, 128, dtype=D._TORCH_DT[p.out_dtype],
+                          device="cuda")
+        idx = torch.empty(wl.batch, wl.q_len, wl.top_k, dtype=torch.int32, device="cuda")
+        fn(p, dev["q"], dev["qI"], dev["w"], dev["kI"], dev["k"], dev["v"], dev["k_scale"],
+           dev["v_scale"], idx, out, ws)
+        torch.cuda.synchronize()
+        assert D.dsa_read_device_status(ws) == 0
+        if first is None:
+            first = (idx.clone(), out.clone())
+        else:
+            assert torch.equal(idx, first[0]), f"indices differ on run {rep}"
+            assert torch.equal(out.view(torch.int16), first[1].view(torch.int16)), f"outputs differ on run {rep}"
+
+
+@pytest.mark.parametrize("name", ["grouped_decode_32k", "decode_256k_int8", "decode_128k"])
+def test_decode_deterministic(dsa, name):
+    _repeat_step(dsa, WORKLOADS[name], False, 12)
+
+
+def test_prefill_deterministic_small(dsa):
+    wl = small_workload(batch=2, q_len=200, total_len=1400, num_q_heads=8, num_kv_heads=2,
+                        top_k=256, kv_dtype="bf16", capacity=1536, seed=64)
+    _repeat_step(dsa, wl, True, 20)
+
+
+def test_prefill_deterministic_full_size(dsa):
+    _repeat_step(dsa, WORKLOADS["prefill_8k_on_32k"], True, 4)
+
+
+@pytest.mark.parametrize("kind", ["ties", "cont"])
+def test_topk_rows_deterministic(dsa, kind):
+    """Many rows (the streaming row select), tie-heavy or continuous scores."""
+    g = torch.Generator().manual_seed(9)
+    S, T, k = 512, 5000, 700
+    sc = (torch.randint(-3, 4, (1, S, T), generator=g).float() if kind == "ties"
+          else torch.randn(1, S, T, generator=g)).cuda()
+    p = dsa.make_problem(batch=1, q_len=S, total_len=[T], top_k=k, cache_capacity=T)
+    ws = dsa.alloc_workspace(p, dsa.DSA_OP_TOPK)
+    first = None
+    for rep in range(20):
+        idx = torch.full((1, S, k), -99, dtype=torch.int32, device="cuda")
+        dsa.dsa_topk(p, sc, idx, ws)
+        torch.cuda.synchronize()
+        if first is None:
+            first = idx.clone()
+        else:
+            assert torch.equal(idx, first), f"indices differ on run {rep}"

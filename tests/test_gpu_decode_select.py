@@ -113,16 +113,19 @@ def test_decode_select_full_size(dsa, name):
     decode_vs_oracle(dsa, wl, make_inputs(wl))
 
 
-@pytest.mark.parametrize("zero", [False, True])
-def test_decode_select_wide_slices(dsa, zero):
-    """Eight rows of up to 200,000 keys: clusters of 16 CTAs would not all be
-    resident at once, so the select takes 24 keys a thread in clusters of 9.
-    With every score equal the threshold bin holds whole rows, beyond the
-    gathered list: the refinement path, and the lowest indices win."""
-    wl = small_workload(batch=1, q_len=8, total_len=200000, top_k=2048, seed=1206)
+@pytest.mark.parametrize("S,zero", [(8, False), (8, True), (16, False)])
+def test_decode_select_wide_slices(dsa, S, zero):
+    """Rows of up to 200,000 keys. Eight rows: clusters of 16 CTAs would not
+    all be resident at once, so the select takes 24 keys a thread in clusters
+    of 9. Sixteen rows: no shape fits them in one wave (15 clusters of 9), so
+    the fewest keys a thread that launch at all (16, clusters of 13) run in
+    waves; the indexer sums 16 queries per block with its histograms. With
+    every score equal the threshold bin holds whole rows, beyond the gathered
+    list: the refinement path, and the lowest indices win."""
+    wl = small_workload(batch=1, q_len=S, total_len=200000, top_k=2048, seed=1206 + S)
     cpu = make_inputs(wl)
     if zero:
         cpu["kI"].zero_()
     got = decode_vs_oracle(dsa, wl, cpu)
     if zero:
-        assert all(got[0, s].tolist() == list(range(2048)) for s in range(8))
+        assert all(got[0, s].tolist() == list(range(2048)) for s in range(S))

@@ -62,7 +62,10 @@ def test_prefill_deterministic_full_size(dsa):
 
 @pytest.mark.parametrize("kind", ["ties", "cont"])
 def test_topk_rows_deterministic(dsa, kind):
-    """Many rows (the streaming row select), tie-heavy or continuous scores."""
+    """Many rows (the streaming row select), tie-heavy or continuous scores.
+    The tie-heavy rows exercise the select's digit rounds: before the resets
+    of its search results were put behind a barrier, 6 of 200 such runs
+    differed from the first."""
     g = torch.Generator().manual_seed(9)
     S, T, k = 512, 5000, 700
     sc = (torch.randint(-3, 4, (1, S, T), generator=g).float() if kind == "ties"
@@ -70,7 +73,7 @@ def test_topk_rows_deterministic(dsa, kind):
     p = dsa.make_problem(batch=1, q_len=S, total_len=[T], top_k=k, cache_capacity=T)
     ws = dsa.alloc_workspace(p, dsa.DSA_OP_TOPK)
     first = None
-    for rep in range(20):
+    for rep in range(200):
         idx = torch.full((1, S, k), -99, dtype=torch.int32, device="cuda")
         dsa.dsa_topk(p, sc, idx, ws)
         torch.cuda.synchronize()

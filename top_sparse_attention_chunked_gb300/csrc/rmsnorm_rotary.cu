@@ -96,7 +96,12 @@ __device__ __forceinline__ void load16(const void* base, long long i, bool fp16,
 // are aligned for vector loads.
 constexpr int kHeadsPerWarp = 4;
 
-template <int D>
+// FULL: the rotary width is the head dim and the caches take vector loads
+// (the common case). Every element then rotates, element i's partner i +- D/2
+// sits in lane ^ 16 (D/2 / E = 16 for either head dim) and the first half of
+// each pair is lanes 0-15, so the per-element width checks and the general
+// partner lookup drop out; the arithmetic is the same.
+template <int D, bool FULL>
 __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const RopeParams p,
                                                                          long long units,
                                                                          int groups, bool vec_cs) {
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
   const bool cf32 = p.cos_dtype == DSA_FP32;
   const int h = p.rotary_dim >> 1;
   const int i0 = lane * E;                       // this lane's first element
-  const bool rot = i0 < p.rotary_dim;            // all E elements rotate (vec_cs) or check each
+  const bool rot = FULL || i0 < p.rotary_dim;   // all E elements rotate (vec_cs) or check each
   float g[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) g[e] = __ldg(p.gamma + i0 + e);
@@ -120,11 +125,11 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
     const int nh = min(kHeadsPerWarp, p.heads - h0);
     // the token's angles for this lane's elements
     float c[E], sn[E];
-    if (h > 0) {
+    if (FULL || h > 0) {
       int pos = __ldg(p.positions + tok);
       pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);   // clamped to the cache
       const long long row = static_cast<long long>(pos) * h;
-      if (vec_cs && rot) {
+      if (FULL || (vec_cs && rot)) {
         const long long j0 = row + (i0 < h ? i0 : i0 - h);
         if (cf32) {
           if constexpr (E == 4) {
@@ -171,7 +176,10 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
       float y[E];
       rms_normalize<E, D>(x, g, p.eps, y);
       float partner[E];
-      if (vec_cs) {
+      if constexpr (FULL) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) partner[e] = __shfl_xor_sync(0xffffffffu, y[e], 16);
+      } else if (vec_cs) {
         // r/2 is a multiple of E: element i's partner i +- r/2 sits in lane
         // lane +- r/(2E) at the same slot, one shuffle away
         const int src = !rot ? lane : (i0 < h ? lane + h / E : lane - h / E);
@@ -193,7 +201,8 @@ __global__ void __launch_bounds__(kRopeWarps * 32) rmsnorm_rotary_kernel(const R
       for (int e = 0; e < E; ++e) {
         const int i = i0 + e;
         float v = y[e];
-        if (i < p.rotary_dim) v = rope_rotate(v, partner[e], c[e], sn[e], i < h);
+        if constexpr (FULL) v = rope_rotate(v, partner[e], c[e], sn[e], lane < 16);
+        else if (i < p.rotary_dim) v = rope_rotate(v, partner[e], c[e], sn[e], i < h);
         o[e] = to_out(v, yf16);
       }
       uint16_t* out = static_cast<uint16_t*>(p.y) + base;
@@ -278,13 +287,17 @@ extern "C" int dsa_rmsnorm_rotary(const dsa_rope_problem* rp, const void* x, con
   const bool vec_cs = r > 0 && ((r / 2) % E) == 0 && aligned_to(cos_cache, cs_vec) &&
                       aligned_to(sin_cache, cs_vec);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool full = vec_cs && r == D;
+  const dim3 grid(static_cast<unsigned>(blocks)), block(kRopeWarps * 32);
   const cudaError_t e =
-      D == 128 ? launch_kernel("rmsnorm_rotary_kernel", rmsnorm_rotary_kernel<128>,
-                               dim3(static_cast<unsigned>(blocks)), dim3(kRopeWarps * 32), 0, st, false, p,
-                               units, groups, vec_cs)
-               : launch_kernel("rmsnorm_rotary_kernel", rmsnorm_rotary_kernel<64>,
-                               dim3(static_cast<unsigned>(blocks)), dim3(kRopeWarps * 32), 0, st, false, p,
-                               units, groups, vec_cs);
+      D == 128 ? (full ? launch_kernel("rmsnorm_rotary_kernel", rmsnorm_rotary_kernel<128, true>, grid, block, 0,
+                                       st, false, p, units, groups, vec_cs)
+                       : launch_kernel("rmsnorm_rotary_kernel", rmsnorm_rotary_kernel<128, false>, grid, block,
+                                       0, st, false, p, units, groups, vec_cs))
+               : (full ? launch_kernel("rmsnorm_rotary_kernel", rmsnorm_rotary_kernel<64, true>, grid, block, 0,
+                                       st, false, p, units, groups, vec_cs)
+                       : launch_kernel("rmsnorm_rotary_kernel", rmsnorm_rotary_kernel<64, false>, grid, block,
+                                       0, st, false, p, units, groups, vec_cs));
   if (e != cudaSuccess) {
     char buf[160];
     snprintf(buf, sizeof(buf), "rmsnorm_rotary launch: %s", cudaGetErrorString(e));

@@ -54,6 +54,9 @@ struct RopeAppendParams {
   int B, S, Hq, Hkv, cap;
   int q_dtype, kv_dtype, cos_dtype;
   int rot, rot_i, max_pos;
+  // the rotary width is the head dim and the caches take vector loads (128-
+  // and 64-element heads): partners one shuffle away, no per-element checks
+  int full, full_i;
   float eps;
   SeqLens lens;
 };
@@ -95,7 +98,8 @@ __device__ __forceinline__ void store_row(void* base, long long i, const uint16_
 template <int D>
 __device__ __forceinline__ void rope_row(const RopeAppendParams& p, const void* src, bool src_f16,
                                          long long elem0, long long tok, const float* gamma, int rot,
-                                         const void* cs, const void* sn, float* s_y, float* out) {
+                                         const void* cs, const void* sn, float* s_y, float* out,
+                                         bool full) {
   constexpr int E = D / 32;
   const int lane = threadIdx.x & 31;
   const int i0 = lane * E;
@@ -109,6 +113,43 @@ __device__ __forceinline__ void rope_row(const RopeAppendParams& p, const void* 
   }
   rms_normalize<E, D>(x, g, p.eps, y);
   const int h = rot >> 1;
+  if (full) {
+    // rot = D: every element rotates; element i's partner i +- D/2 sits in
+    // lane ^ 16 (D/2 / E = 16), lanes 0-15 hold the first halves, and the
+    // lane's E angles are consecutive
+    const int b = static_cast<int>(tok / p.S);
+    const int s = static_cast<int>(tok - static_cast<long long>(b) * p.S);
+    int pos = p.lens.T[b] - p.S + s;
+    pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);   // clamped to the cache
+    const long long j0 = static_cast<long long>(pos) * h + (lane < 16 ? i0 : i0 - h);
+    float c[E], sv[E];
+    if (p.cos_dtype == DSA_FP32) {
+      const float* cf = static_cast<const float*>(cs) + j0;
+      const float* sf = static_cast<const float*>(sn) + j0;
+      if constexpr (E == 4) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(cf)), bq = __ldg(reinterpret_cast<const float4*>(sf));
+        c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+        sv[0] = bq.x; sv[1] = bq.y; sv[2] = bq.z; sv[3] = bq.w;
+      } else {
+        const float2 a = __ldg(reinterpret_cast<const float2*>(cf)), bq = __ldg(reinterpret_cast<const float2*>(sf));
+        c[0] = a.x; c[1] = a.y;
+        sv[0] = bq.x; sv[1] = bq.y;
+      }
+    } else {
+      uint16_t cu[E], su[E];
+      load_row<E>(cs, j0, cu);
+      load_row<E>(sn, j0, su);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        c[e] = half_to_float(cu[e], false);
+        sv[e] = half_to_float(su[e], false);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      out[e] = rope_rotate(y[e], __shfl_xor_sync(0xffffffffu, y[e], 16), c[e], sv[e], lane < 16);
+    return;
+  }
   if (h > 0) {
     const int b = static_cast<int>(tok / p.S);
     const int s = static_cast<int>(tok - static_cast<long long>(b) * p.S);
@@ -181,7 +222,8 @@ __global__ void __launch_bounds__(kRaWarps * 32) rope_append_kernel(const RopeAp
     long long r = u;
     float out[4];
     if (r < p.n_q) {                                   // q: rotate in place
-      rope_row<128>(p, p.q, qf16, r * DSA_HEAD_DIM, r / p.Hq, p.g_q, p.rot, p.cos, p.sin, s_y[warp], out);
+      rope_row<128>(p, p.q, qf16, r * DSA_HEAD_DIM, r / p.Hq, p.g_q, p.rot, p.cos, p.sin, s_y[warp], out,
+                    p.full != 0);
       uint16_t o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[e] = float_to_half(out[e], qf16);
@@ -191,7 +233,7 @@ __global__ void __launch_bounds__(kRaWarps * 32) rope_append_kernel(const RopeAp
     r -= p.n_q;
     if (r < p.n_qi) {                                  // qI: rotate in place (BF16)
       rope_row<64>(p, p.qI, false, r * DSA_IDX_DIM, r / DSA_IDX_HEADS, p.g_qI, p.rot_i, p.cos_i,
-                   p.sin_i, s_y[warp], out);
+                   p.sin_i, s_y[warp], out, p.full_i != 0);
       uint16_t o[2] = {float_to_half(out[0], false), float_to_half(out[1], false)};
       store_row<2>(p.qI, r * DSA_IDX_DIM + lane * 2, o);
       continue;
@@ -208,7 +250,8 @@ __global__ void __launch_bounds__(kRaWarps * 32) rope_append_kernel(const RopeAp
       uint16_t bits[4];
       float xv[4];
       if (is_k) {
-        rope_row<128>(p, p.k_new, qf16, row * DSA_HEAD_DIM, tok, p.g_k, p.rot, p.cos, p.sin, s_y[warp], out);
+        rope_row<128>(p, p.k_new, qf16, row * DSA_HEAD_DIM, tok, p.g_k, p.rot, p.cos, p.sin, s_y[warp], out,
+                      p.full != 0);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           bits[e] = float_to_half(out[e], qf16);        // the rotated k in the q dtype
@@ -228,7 +271,7 @@ __global__ void __launch_bounds__(kRaWarps * 32) rope_append_kernel(const RopeAp
       const int b = static_cast<int>(tok / p.S);
       const int s = static_cast<int>(tok - static_cast<long long>(b) * p.S);
       rope_row<64>(p, p.kI_new, false, tok * DSA_IDX_DIM, tok, p.g_kI, p.rot_i, p.cos_i, p.sin_i,
-                   s_y[warp], out);
+                   s_y[warp], out, p.full_i != 0);
       uint16_t o[2] = {float_to_half(out[0], false), float_to_half(out[1], false)};
       const long long dst = (static_cast<long long>(b) * p.cap + (p.lens.T[b] - p.S + s)) * DSA_IDX_DIM;
       store_row<2>(p.kI, dst + lane * 2, o);
@@ -336,6 +379,14 @@ extern "C" int dsa_rope_append(const dsa_problem* p, const dsa_rope_params* rp, 
   a.cos_dtype = rp->cos_dtype;
   a.rot = rp->rotary_dim;
   a.rot_i = rp->rotary_dim_index;
+  {
+    // vector loads of a lane's E consecutive angles need the caches aligned
+    // to E elements (the row starts then stay aligned)
+    const size_t es = rp->cos_dtype == DSA_FP32 ? 4 : 2;
+    auto al = [](const void* ptr, size_t n) { return (reinterpret_cast<uintptr_t>(ptr) % n) == 0; };
+    a.full = rp->rotary_dim == DSA_HEAD_DIM && al(rp->cos, 4 * es) && al(rp->sin, 4 * es);
+    a.full_i = rp->rotary_dim_index == DSA_IDX_DIM && al(rp->cos_index, 2 * es) && al(rp->sin_index, 2 * es);
+  }
   a.max_pos = rp->max_pos;
   a.eps = rp->eps;
   for (int b = 0; b < p->batch; ++b) a.lens.T[b] = p->total_len[b];
